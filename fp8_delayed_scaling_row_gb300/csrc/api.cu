@@ -1,0 +1,482 @@
+// The C ABI of liblnfp8: argument validation, error reporting and the
+// LayerNormLinear / LayerNormMLP forward and backward sequences.
+//
+// Each module call is a fixed sequence of the library's kernels on the
+// caller's stream (TE tutorial, code blocks 1 and 3: te.LayerNormLinear /
+// te.LayerNormMLP under fp8_autocast with the DelayedScaling recipe):
+//   forward  : weight casts (K2) -> LayerNorm + cast (K1) -> FP8 GEMMs (K3,
+//              GELU and the next cast fused into FC1's epilogue) -> state update (K4)
+//   backward : dY cast + bias gradient (K2) -> dgrad GEMM with dGELU + dH cast
+//              fused (K3) -> wgrad / dgrad GEMMs (K3) -> LayerNorm backward (K5)
+//              -> state update (K4)
+// The casts of a step all use the scales decided before the step (delayed
+// scaling); the forward's scale_inv is saved for the backward because the
+// update at the end of the forward replaces it.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lnfp8 {
+
+static thread_local char g_msg[512] = "";
+
+lnfp8_status set_error(lnfp8_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+void clear_error() { g_msg[0] = 0; }
+
+lnfp8_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return LNFP8_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQ(p, who)                                                                       \
+  do {                                                                                    \
+    if (!(p)) return set_error(LNFP8_ERR_INVALID_ARG, "%s: %s is NULL", who, #p);          \
+    if (!al16(p)) return set_error(LNFP8_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", who, #p); \
+  } while (0)
+#define OPT(p, who)                                                                       \
+  do {                                                                                    \
+    if ((p) && !al16(p)) return set_error(LNFP8_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", who, #p); \
+  } while (0)
+#define TRY(x)                             \
+  do {                                     \
+    const lnfp8_status _s = (x);           \
+    if (_s != LNFP8_OK) return _s;         \
+  } while (0)
+
+lnfp8_status feat(int64_t v, const char* name, const char* who) {
+  if (v <= 0 || v % 16 != 0)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: %s = %lld must be a positive multiple of 16", who, name,
+                     (long long)v);
+  if (v > (1LL << 30)) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: %s = %lld too large", who, name, (long long)v);
+  return LNFP8_OK;
+}
+
+lnfp8_status tokens(int64_t M, const char* who) {
+  if (M < 0) return set_error(LNFP8_ERR_INVALID_ARG, "%s: M = %lld < 0", who, (long long)M);
+  if (M > (1LL << 31) - 1) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: M = %lld too large", who, (long long)M);
+  return LNFP8_OK;
+}
+
+lnfp8_status check_dtype(int dt, const char* who) {
+  if (dt != LNFP8_E4M3 && dt != LNFP8_E5M2) return set_error(LNFP8_ERR_INVALID_ARG, "%s: bad FP8 dtype %d", who, dt);
+  return LNFP8_OK;
+}
+
+lnfp8_status check_recipe(const lnfp8_recipe* r, const lnfp8_meta* m, const char* who) {
+  if (!r) return set_error(LNFP8_ERR_INVALID_ARG, "%s: recipe is NULL", who);
+  if (r->format < LNFP8_FORMAT_E4M3 || r->format > LNFP8_FORMAT_E5M2)
+    return set_error(LNFP8_ERR_INVALID_ARG, "%s: bad recipe format %d", who, r->format);
+  if (r->algo != 0) return set_error(LNFP8_ERR_UNSUPPORTED, "%s: amax_compute_algo %d (only 0 = max)", who, r->algo);
+  if (r->margin < 0 || r->margin > 30) return set_error(LNFP8_ERR_INVALID_ARG, "%s: margin %d", who, r->margin);
+  if (m && r->history_len != m->history_len)
+    return set_error(LNFP8_ERR_INVALID_ARG, "%s: recipe.history_len %d != meta.history_len %d", who, r->history_len,
+                     m->history_len);
+  return LNFP8_OK;
+}
+
+int fwd_dtype(const lnfp8_recipe* r) { return r->format == LNFP8_FORMAT_E5M2 ? LNFP8_E5M2 : LNFP8_E4M3; }
+int bwd_dtype(const lnfp8_recipe* r) { return r->format == LNFP8_FORMAT_E4M3 ? LNFP8_E4M3 : LNFP8_E5M2; }
+uint64_t mask_all(int n, int dt) { return dt == LNFP8_E5M2 ? (n >= 64 ? ~0ull : ((1ull << n) - 1)) : 0ull; }
+
+// End of a forward/backward: either the state update (which also saves the
+// pre-update scale_inv) or, when deferred, only the snapshot.
+lnfp8_status finish_state(const lnfp8_meta* m, const lnfp8_recipe* r, int dt, float* sinv_saved, int defer,
+                          cudaStream_t st) {
+  if (!defer) return update_launch(m, mask_all(m->n, dt), r->margin, sinv_saved, st);
+  if (sinv_saved && cudaMemcpyAsync(sinv_saved, m->scale_inv, m->n * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return check_launch("saving scale_inv");
+  return LNFP8_OK;
+}
+
+GemmArgs gemm_args(const uint8_t* a, int al, int adt, const uint8_t* b, int bl, int bdt, int64_t M, int64_t N,
+                   int64_t K, const float* sa, const float* sb) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a = a; g.a_layout = al; g.a_dtype = adt;
+  g.b = b; g.b_layout = bl; g.b_dtype = bdt;
+  g.M = M; g.N = N; g.K = K;
+  g.sinv_a = sa; g.sinv_b = sb;
+  g.epi = EPI_STORE;
+  return g;
+}
+
+// A weight-gradient GEMM contracts over the tokens; with no tokens it is zero.
+lnfp8_status wgrad(const GemmArgs& g, uint16_t* out, cudaStream_t st) {
+  if (g.K == 0) {
+    if (cudaMemsetAsync(out, 0, g.M * g.N * sizeof(uint16_t), st) != cudaSuccess) return check_launch("zero wgrad");
+    return LNFP8_OK;
+  }
+  return gemm_launch(g, st);
+}
+
+}  // namespace
+}  // namespace lnfp8
+
+using namespace lnfp8;
+
+extern "C" {
+
+const char* lnfp8_last_error(void) { return g_msg; }
+
+int lnfp8_version(void) { return 100; }
+
+lnfp8_status lnfp8_sync_status(lnfp8_stream stream) {
+  clear_error();
+  unsigned int word = 0;
+  TRY(status_read_clear((cudaStream_t)stream, &word));
+  if (word & kStatusTimeout) return set_error(LNFP8_ERR_TIMEOUT, "a bounded device wait gave up");
+  return LNFP8_OK;
+}
+
+lnfp8_status lnfp8_selftest_timeout(int64_t limit_ns, lnfp8_stream stream) {
+  clear_error();
+  if (limit_ns < 1000 || limit_ns > 1000000000LL)
+    return set_error(LNFP8_ERR_INVALID_ARG, "lnfp8_selftest_timeout: limit_ns must be in [1e3, 1e9]");
+  return selftest_timeout_launch(limit_ns, (cudaStream_t)stream);
+}
+
+lnfp8_status lnfp8_meta_init(const lnfp8_meta* meta, lnfp8_stream stream) {
+  clear_error();
+  TRY(validate_meta(meta, 0, "lnfp8_meta_init"));
+  return meta_init_launch(meta, (cudaStream_t)stream);
+}
+
+lnfp8_status amax_history_update(const lnfp8_meta* meta, const lnfp8_recipe* recipe, const int* dtype_per_tensor,
+                                 float* scale_inv_before, lnfp8_stream stream) {
+  const char* who = "amax_history_update";
+  clear_error();
+  TRY(validate_meta(meta, 0, who));
+  TRY(check_recipe(recipe, meta, who));
+  if (!dtype_per_tensor) return set_error(LNFP8_ERR_INVALID_ARG, "%s: dtype_per_tensor is NULL", who);
+  uint64_t mask = 0;
+  for (int i = 0; i < meta->n; ++i) {
+    TRY(check_dtype(dtype_per_tensor[i], who));
+    if (dtype_per_tensor[i] == LNFP8_E5M2) mask |= 1ull << i;
+  }
+  return update_launch(meta, mask, recipe->margin, scale_inv_before, (cudaStream_t)stream);
+}
+
+lnfp8_status fp8_quantize(const void* in, int in_is_fp32, int64_t rows, int64_t cols, int dtype, const float* scale,
+                          float* amax_cur, uint8_t* out, uint8_t* out_t, float* colsum, lnfp8_stream stream) {
+  const char* who = "fp8_quantize";
+  clear_error();
+  TRY(tokens(rows, who));
+  TRY(feat(cols, "cols", who));
+  TRY(check_dtype(dtype, who));
+  if (rows > 0) REQ(in, who);
+  if (!scale || !amax_cur) return set_error(LNFP8_ERR_INVALID_ARG, "%s: scale and amax_cur are required", who);
+  OPT(out, who);
+  OPT(out_t, who);
+  OPT(colsum, who);
+  return cast_launch(in, in_is_fp32 != 0, rows, cols, dtype, scale, amax_cur, out, out_t, colsum, (cudaStream_t)stream);
+}
+
+lnfp8_status ln_fwd_cast(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int64_t D,
+                         int dtype, const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
+                         float* y_debug, lnfp8_stream stream) {
+  const char* who = "ln_fwd_cast";
+  clear_error();
+  TRY(tokens(M, who));
+  TRY(feat(D, "D", who));
+  TRY(check_dtype(dtype, who));
+  if (D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: D = %lld > 8192", who, (long long)D);
+  if (!(eps >= 0.f)) return set_error(LNFP8_ERR_INVALID_ARG, "%s: eps must be >= 0", who);
+  REQ(gamma, who);
+  REQ(beta, who);
+  if (!scale || !amax_cur) return set_error(LNFP8_ERR_INVALID_ARG, "%s: scale and amax_cur are required", who);
+  if (M > 0) {
+    REQ(x, who);
+    REQ(out, who);
+    REQ(mu, who);
+    REQ(rsigma, who);
+  }
+  OPT(y_debug, who);
+  return ln_fwd_launch(x, gamma, beta, eps, M, D, dtype, scale, amax_cur, out, mu, rsigma, y_debug, (cudaStream_t)stream);
+}
+
+lnfp8_status ln_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu, const float* rsigma,
+                    int64_t M, int64_t D, uint16_t* dx, float* dgamma, float* dbeta, lnfp8_stream stream) {
+  const char* who = "ln_bwd";
+  clear_error();
+  TRY(tokens(M, who));
+  TRY(feat(D, "D", who));
+  if (D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: D = %lld > 8192", who, (long long)D);
+  REQ(gamma, who);
+  REQ(dgamma, who);
+  REQ(dbeta, who);
+  if (M > 0) {
+    REQ(dy, who);
+    REQ(x, who);
+    REQ(mu, who);
+    REQ(rsigma, who);
+    REQ(dx, who);
+  }
+  return ln_bwd_launch(dy, x, gamma, mu, rsigma, M, D, dx, dgamma, dbeta, (cudaStream_t)stream);
+}
+
+lnfp8_status fp8_gemm(const uint8_t* A, int a_layout, int a_dtype, const uint8_t* B, int b_layout, int b_dtype, int64_t M,
+                      int64_t N, int64_t K, const float* sinv_a, const float* sinv_b, const uint16_t* bias,
+                      uint16_t* out, lnfp8_stream stream) {
+  const char* who = "fp8_gemm";
+  clear_error();
+  TRY(tokens(M, who));
+  TRY(feat(N, "N", who));
+  TRY(feat(K, "K", who));
+  TRY(check_dtype(a_dtype, who));
+  TRY(check_dtype(b_dtype, who));
+  if ((a_layout != 0 && a_layout != 1) || (b_layout != 0 && b_layout != 1))
+    return set_error(LNFP8_ERR_INVALID_ARG, "%s: layouts must be 0 or 1", who);
+  if (a_layout == 1 && M % 16 != 0)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: M must be a multiple of 16 when A is stored [K, M]", who);
+  if (!sinv_a || !sinv_b) return set_error(LNFP8_ERR_INVALID_ARG, "%s: sinv_a and sinv_b are required", who);
+  OPT(bias, who);
+  if (M > 0) {
+    REQ(A, who);
+    REQ(out, who);
+  }
+  REQ(B, who);
+  GemmArgs g = gemm_args(A, a_layout, a_dtype, B, b_layout, b_dtype, M, N, K, sinv_a, sinv_b);
+  g.bias = bias;
+  g.out = out;
+  return gemm_launch(g, (cudaStream_t)stream);
+}
+
+lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream stream) {
+  const char* who = "ln_linear_fwd";
+  clear_error();
+  if (!a) return set_error(LNFP8_ERR_INVALID_ARG, "%s: args is NULL", who);
+  cudaStream_t st = (cudaStream_t)stream;
+  TRY(tokens(a->M, who));
+  TRY(feat(a->K, "K", who));
+  TRY(feat(a->N, "N", who));
+  TRY(validate_meta(&a->meta, 2, who));
+  TRY(check_recipe(&a->recipe, &a->meta, who));
+  const bool ln = a->gamma != nullptr;
+  if (ln) {
+    REQ(a->beta, who);
+    if (a->K > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: K > 8192 with LayerNorm", who);
+  }
+  REQ(a->w, who);
+  REQ(a->wq, who);
+  OPT(a->bias, who);
+  OPT(a->ln_out_debug, who);
+  if (!a->sinv_saved) return set_error(LNFP8_ERR_INVALID_ARG, "%s: sinv_saved is NULL", who);
+  if (a->M > 0) {
+    REQ(a->x, who);
+    REQ(a->y, who);
+    REQ(a->xq, who);
+    if (ln) {
+      REQ(a->mu, who);
+      REQ(a->rsigma, who);
+    }
+  }
+  const int fdt = fwd_dtype(&a->recipe);
+  const lnfp8_meta& m = a->meta;
+  TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
+  if (ln)
+    TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,
+                      a->rsigma, a->ln_out_debug, st));
+  else
+    TRY(cast_launch(a->x, false, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, nullptr, nullptr, st));
+  GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, m.scale_inv + 0, m.scale_inv + 1);
+  g.bias = a->bias;
+  g.out = a->y;
+  TRY(gemm_launch(g, st));
+  return finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st);
+}
+
+lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream stream) {
+  const char* who = "ln_linear_bwd";
+  clear_error();
+  if (!a) return set_error(LNFP8_ERR_INVALID_ARG, "%s: args is NULL", who);
+  cudaStream_t st = (cudaStream_t)stream;
+  TRY(tokens(a->M, who));
+  TRY(feat(a->K, "K", who));
+  TRY(feat(a->N, "N", who));
+  TRY(validate_meta(&a->meta, 1, who));
+  TRY(check_recipe(&a->recipe, &a->meta, who));
+  const bool ln = a->gamma != nullptr;
+  REQ(a->wq, who);
+  REQ(a->dw, who);
+  OPT(a->dbias, who);
+  if (!a->sinv_saved) return set_error(LNFP8_ERR_INVALID_ARG, "%s: sinv_saved is NULL", who);
+  if (ln) {
+    if (a->K > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: K > 8192 with LayerNorm", who);
+    REQ(a->dgamma, who);
+    REQ(a->dbeta, who);
+  }
+  if (a->M > 0) {
+    REQ(a->dy, who);
+    REQ(a->xq, who);
+    REQ(a->dx, who);
+    REQ(a->dyq, who);
+    if (ln) {
+      REQ(a->x, who);
+      REQ(a->mu, who);
+      REQ(a->rsigma, who);
+      REQ(a->dln, who);
+    }
+  }
+  const int fdt = fwd_dtype(&a->recipe), bdt = bwd_dtype(&a->recipe);
+  const lnfp8_meta& m = a->meta;
+  TRY(cast_launch(a->dy, false, a->M, a->N, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->dbias, st));
+  uint16_t* dln = ln ? a->dln : a->dx;
+  GemmArgs dg = gemm_args(a->dyq, 0, bdt, a->wq, 1, fdt, a->M, a->K, a->N, m.scale_inv + 0, a->sinv_saved + 1);
+  dg.out = dln;
+  TRY(gemm_launch(dg, st));
+  GemmArgs wg = gemm_args(a->dyq, 1, bdt, a->xq, 1, fdt, a->N, a->K, a->M, m.scale_inv + 0, a->sinv_saved + 0);
+  wg.out = a->dw;
+  TRY(wgrad(wg, a->dw, st));
+  if (ln) TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st));
+  return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
+}
+
+lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
+  const char* who = "ln_mlp_fwd";
+  clear_error();
+  if (!a) return set_error(LNFP8_ERR_INVALID_ARG, "%s: args is NULL", who);
+  cudaStream_t st = (cudaStream_t)stream;
+  TRY(tokens(a->M, who));
+  TRY(feat(a->D, "D", who));
+  TRY(feat(a->F, "F", who));
+  if (a->D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: D > 8192", who);
+  TRY(validate_meta(&a->meta, 4, who));
+  TRY(check_recipe(&a->recipe, &a->meta, who));
+  REQ(a->gamma, who);
+  REQ(a->beta, who);
+  REQ(a->w1, who);
+  REQ(a->w2, who);
+  REQ(a->w1q, who);
+  REQ(a->w2q, who);
+  OPT(a->b1, who);
+  OPT(a->b2, who);
+  OPT(a->ln_out_debug, who);
+  OPT(a->act_debug, who);
+  if (!a->sinv_saved) return set_error(LNFP8_ERR_INVALID_ARG, "%s: sinv_saved is NULL", who);
+  if (a->M > 0) {
+    REQ(a->x, who);
+    REQ(a->y, who);
+    REQ(a->lnq, who);
+    REQ(a->mu, who);
+    REQ(a->rsigma, who);
+    REQ(a->h, who);
+    REQ(a->aq, who);
+  }
+  const int fdt = fwd_dtype(&a->recipe);
+  const lnfp8_meta& m = a->meta;
+  TRY(cast_launch(a->w1, false, a->F, a->D, fdt, m.scale + 1, m.amax_cur + 1, a->w1q, nullptr, nullptr, st));
+  TRY(cast_launch(a->w2, false, a->D, a->F, fdt, m.scale + 3, m.amax_cur + 3, a->w2q, nullptr, nullptr, st));
+  TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
+                    a->rsigma, a->ln_out_debug, st));
+  GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0, m.scale_inv + 1);
+  f1.epi = EPI_GELU;
+  f1.bias = a->b1;
+  f1.out = a->h;
+  f1.out_q = a->aq;
+  f1.q_dtype = fdt;
+  f1.scale_q = m.scale + 2;
+  f1.amax_q = m.amax_cur + 2;
+  f1.dbg = a->act_debug;
+  TRY(gemm_launch(f1, st));
+  GemmArgs f2 = gemm_args(a->aq, 0, fdt, a->w2q, 0, fdt, a->M, a->D, a->F, m.scale_inv + 2, m.scale_inv + 3);
+  f2.bias = a->b2;
+  f2.out = a->y;
+  TRY(gemm_launch(f2, st));
+  return finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st);
+}
+
+lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
+  const char* who = "ln_mlp_bwd";
+  clear_error();
+  if (!a) return set_error(LNFP8_ERR_INVALID_ARG, "%s: args is NULL", who);
+  cudaStream_t st = (cudaStream_t)stream;
+  TRY(tokens(a->M, who));
+  TRY(feat(a->D, "D", who));
+  TRY(feat(a->F, "F", who));
+  if (a->D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: D > 8192", who);
+  TRY(validate_meta(&a->meta, 2, who));
+  TRY(check_recipe(&a->recipe, &a->meta, who));
+  REQ(a->gamma, who);
+  REQ(a->w1q, who);
+  REQ(a->w2q, who);
+  REQ(a->dw1, who);
+  REQ(a->dw2, who);
+  REQ(a->dgamma, who);
+  REQ(a->dbeta, who);
+  OPT(a->db1, who);
+  OPT(a->db2, who);
+  OPT(a->dh_debug, who);
+  if (!a->sinv_saved) return set_error(LNFP8_ERR_INVALID_ARG, "%s: sinv_saved is NULL", who);
+  if (a->M > 0) {
+    REQ(a->dy, who);
+    REQ(a->x, who);
+    REQ(a->lnq, who);
+    REQ(a->mu, who);
+    REQ(a->rsigma, who);
+    REQ(a->h, who);
+    REQ(a->aq, who);
+    REQ(a->dx, who);
+    REQ(a->dyq, who);
+    REQ(a->dhq, who);
+    REQ(a->dln, who);
+  }
+  const int fdt = fwd_dtype(&a->recipe), bdt = bwd_dtype(&a->recipe);
+  const lnfp8_meta& m = a->meta;
+  TRY(cast_launch(a->dy, false, a->M, a->D, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->db2, st));
+  if (a->db1 && cudaMemsetAsync(a->db1, 0, a->F * sizeof(float), st) != cudaSuccess) return check_launch("clearing db1");
+  // FC2 dgrad with the GELU derivative and the dH cast fused: dH = (dYq . W2q) * s * gelu'(H)
+  GemmArgs d2 = gemm_args(a->dyq, 0, bdt, a->w2q, 1, fdt, a->M, a->F, a->D, m.scale_inv + 0, a->sinv_saved + 3);
+  d2.epi = EPI_DGELU;
+  d2.h_in = a->h;
+  d2.out_q = a->dhq;
+  d2.q_dtype = bdt;
+  d2.scale_q = m.scale + 1;
+  d2.amax_q = m.amax_cur + 1;
+  d2.colsum = a->db1;
+  d2.dbg = a->dh_debug;
+  TRY(gemm_launch(d2, st));
+  // FC2 wgrad: dW2 = dYq^T . Aq
+  GemmArgs w2 = gemm_args(a->dyq, 1, bdt, a->aq, 1, fdt, a->D, a->F, a->M, m.scale_inv + 0, a->sinv_saved + 2);
+  w2.out = a->dw2;
+  TRY(wgrad(w2, a->dw2, st));
+  // FC1 dgrad: dLN = dHq . W1q
+  GemmArgs d1 = gemm_args(a->dhq, 0, bdt, a->w1q, 1, fdt, a->M, a->D, a->F, m.scale_inv + 1, a->sinv_saved + 1);
+  d1.out = a->dln;
+  TRY(gemm_launch(d1, st));
+  // FC1 wgrad: dW1 = dHq^T . LNq
+  GemmArgs w1 = gemm_args(a->dhq, 1, bdt, a->lnq, 1, fdt, a->F, a->D, a->M, m.scale_inv + 1, a->sinv_saved + 0);
+  w1.out = a->dw1;
+  TRY(wgrad(w1, a->dw1, st));
+  TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st));
+  return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// K2: scaled FP8 cast with amax, optional transposed copy and column sums.
+//
+// The cast of delayed scaling (Turbo-charging guide, "Playing with
+// lower-precision formats: BF16 vs FP8": the recipe tracks the amax of each
+// tensor and rescales it): code = fp8(x * scale) with the scale decided before
+// the step, while max|x| is folded into the tensor's running amax. Used for
+// the weights every step, for the upstream gradient dY (with its column sums,
+// the bias gradient) and for a Linear layer's un-normalised input.
+//
+// HBM-bound: each element is read once (2 or 4 bytes) and written once
+// (1 byte, plus 1 for the transpose). A CTA walks one 64-column strip over a
+// range of rows, 64 x 64 tiles at a time, with 16-byte loads.
+#include "common.cuh"
+#include "internal.h"
+
+namespace lnfp8 {
+namespace {
+
+constexpr int kTC = 64;   // tile columns
+constexpr int kTR = 64;   // tile rows
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* v);
+
+template <>
+__device__ __forceinline__ void load8<uint16_t>(const uint16_t* p, float* v) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float* v) {
+  float4 a = reinterpret_cast<const float4*>(p)[0];
+  float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <typename T, int DT>
+__global__ void __launch_bounds__(kThreads)
+cast_kernel(const T* __restrict__ in, int64_t rows, int64_t cols, int64_t rows_per_cta,
+            const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
+            uint8_t* __restrict__ out_t, float* colsum) {
+  __shared__ __align__(16) uint8_t tq[kTC][kTR + 16];
+  __shared__ float red[32][kTC + 1];
+  __shared__ uint32_t ared[kThreads / 32];
+
+  const int t = threadIdx.x;
+  const int cv = t & 7;          // which 8-column vector of the strip
+  const int rr = t >> 3;         // 0..31
+  const int64_t c0 = (int64_t)blockIdx.x * kTC;
+  const int64_t cc = c0 + cv * 8;
+  const bool col_ok = cc < cols;
+  const int64_t r_begin = (int64_t)blockIdx.y * rows_per_cta;
+  const int64_t r_end = min(rows, r_begin + rows_per_cta);
+  const float s = *scale_p;
+  const bool t_vec = (rows % 16) == 0;
+
+  uint32_t am = 0;
+  float csum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) csum[i] = 0.f;
+
+  for (int64_t r0 = r_begin; r0 < r_end; r0 += kTR) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rl = rr + 32 * h;
+      const int64_t r = r0 + rl;
+      uint2 q = make_uint2(0, 0);
+      if (r < r_end && col_ok) {
+        float v[8];
+        load8<T>(in + r * cols + cc, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          am = max(am, abs_bits(v[i]));
+          csum[i] += v[i];
+        }
+        q = cvt_fp8x8<DT>(v, s);
+        if (out) *reinterpret_cast<uint2*>(out + r * cols + cc) = q;
+      }
+      if (out_t) {
+        const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tq[cv * 8 + i][rl] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+      }
+    }
+    if (out_t) {
+      __syncthreads();
+      const int col = t >> 2, chunk = (t & 3) * 16;
+      const int64_t c = c0 + col;
+      if (c < cols) {
+        uint8_t* dst = out_t + c * rows + r0 + chunk;
+        const int64_t nvalid = min64(16, r_end - (r0 + chunk));
+        if (nvalid == 16 && t_vec) {
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tq[col][chunk]);
+        } else {
+          for (int i = 0; i < nvalid; ++i) dst[i] = tq[col][chunk + i];
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  if (colsum) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[rr][cv * 8 + i] = csum[i];
+    __syncthreads();
+    if (t < kTC) {
+      float acc = 0.f;
+      for (int j = 0; j < 32; ++j) acc += red[j][t];
+      if (c0 + t < cols) atomicAdd(colsum + c0 + t, acc);
+    }
+  }
+  block_amax_commit(am, ared, amax_cur);
+}
+
+}  // namespace
+
+lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
+                         const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
+                         float* colsum, cudaStream_t st) {
+  if (colsum && cols > 0 && cudaMemsetAsync(colsum, 0, cols * sizeof(float), st) != cudaSuccess)
+    return check_launch("fp8_quantize: clearing colsum");
+  if (rows == 0 || cols == 0) return LNFP8_OK;
+  const int64_t strips = (cols + kTC - 1) / kTC;
+  const int64_t row_tiles = (rows + kTR - 1) / kTR;
+  const int64_t want = 4LL * num_sms();
+  int64_t ysplit = (want + strips - 1) / strips;
+  ysplit = max64(1, min64(ysplit, row_tiles));
+  const int64_t rows_per_cta = ((row_tiles + ysplit - 1) / ysplit) * kTR;
+  ysplit = (rows + rows_per_cta - 1) / rows_per_cta;
+  if (strips > 0x7FFFFFFF || ysplit > 65535)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8_quantize: tensor too large");
+  dim3 grid((unsigned)strips, (unsigned)ysplit);
+  if (in_fp32) {
+    if (dtype == LNFP8_E4M3)
+      cast_kernel<float, LNFP8_E4M3><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+    else
+      cast_kernel<float, LNFP8_E5M2><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+  } else {
+    if (dtype == LNFP8_E4M3)
+      cast_kernel<uint16_t, LNFP8_E4M3><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+    else
+      cast_kernel<uint16_t, LNFP8_E5M2><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+  }
+  return check_launch("fp8_quantize");
+}
+
+}  // namespace lnfp8

@@ -1,0 +1,640 @@
+// K3: FP8 GEMM on the 5th-generation tensor cores (tcgen05, kind::f8f6f4),
+// operands staged by TMA, fp32 accumulators in tensor memory, fused epilogues.
+//
+// The linear layers of LayerNormLinear / LayerNormMLP run on "FP8 tensor
+// cores" (TE tutorial, code block 1 prose) with per-tensor scales: the codes
+// of both operands are multiplied with fp32 accumulation and the product is
+// dequantised by sinv_a * sinv_b (the recorded reciprocals of the two cast
+// scales). Three epilogues cover the MLP:
+//   EPI_STORE  out = bf16(acc * s + bias)                       (FC2, dgrad, wgrad, Linear)
+//   EPI_GELU   h = bf16(acc * s + b1) saved; a = gelu_tanh(h);
+//              amax(a); aq = fp8(a * scale_a)                   (FC1 forward)
+//   EPI_DGELU  dh = acc * s * gelu_tanh'(h); amax(dh);
+//              dhq = fp8(dh * scale_dh); db1 += column sums     (FC2 dgrad)
+// so the GELU output and the gradient dH are written only as FP8 codes.
+//
+// Kernel shape (persistent, one CTA per SM, 384 threads):
+//   warp 0      TMA producer (one elected thread), STAGES-deep smem ring
+//   warp 1      MMA issuer (one thread): 128 x BN x 32 tcgen05.mma per K step
+//   warp 2      tensor-memory allocator (2 x BN fp32 columns: double-buffered
+//               accumulator so the epilogue of tile i overlaps the MMAs of i+1)
+//   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and
+//               one half of the tile's columns with tcgen05.ld
+// Operands may be K-major ([rows, K]) or MN-major ([K, rows]); FP8 MN-major
+// operands are native to tcgen05, so the backward GEMMs read dY, A, dH and the
+// LN output in the layout the forward wrote them, with no transposed copies.
+// Every mbarrier wait is bounded: on a timeout the CTA records it in the
+// library's status word, drains its in-flight copies and MMAs, frees its
+// tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lnfp8 {
+
+__device__ unsigned int g_status = 0;
+
+lnfp8_status status_read_clear(cudaStream_t st, unsigned int* word) {
+  *word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return check_launch("lnfp8_sync_status");
+  if (cudaMemcpyFromSymbol(word, g_status, sizeof(unsigned int)) != cudaSuccess)
+    return check_launch("lnfp8_sync_status: reading the status word");
+  const unsigned int zero = 0;
+  if (*word && cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int)) != cudaSuccess)
+    return check_launch("lnfp8_sync_status: clearing the status word");
+  return LNFP8_OK;
+}
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;  // bytes (= FP8 elements) of K per pipeline stage
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + 32 * kEpiWarps;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int CSUM_BYTES = 2 * 4 * BN * 4;  // [acc buffer][row quarter][BN] fp32
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + CSUM_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+};
+
+struct KParams {
+  int M, N, K;
+  int num_m, num_n, num_kb;
+  uint32_t idesc;  // instruction descriptor of one MMA
+  const float* sinv_a;
+  const float* sinv_b;
+  const uint16_t* bias;
+  uint16_t* out;
+  const uint16_t* h_in;
+  uint8_t* out_q;
+  const float* scale_q;
+  float* amax_q;
+  float* colsum;
+  float* dbg;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after ~limit_ns or when another role has aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicOr(&g_status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout type 2,
+// descriptor version 1 in bits 46-47). Both byte offsets are 1024 for
+// MN-major tiles (one 128-byte atom wide, 8-row groups 1024 B apart); for
+// K-major tiles the stride offset is the 1024 B between 8-row groups and the
+// leading offset is unused.
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kGeluK = 0.7978845608028654f;  // sqrt(2/pi)
+constexpr float kGeluC = 0.044715f;
+
+// Column sums of a 32 x 32 block held one row per lane: after the exchange,
+// lane c holds the sum over the 32 rows of column c (31 shuffles).
+__device__ __forceinline__ float transpose_reduce32(float* v, int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// ------------------------------------------------------------ the kernel
+template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, csum[2 acc][2 halves]
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
+  uint32_t* tmem_slot = misc;
+  volatile uint32_t* abort_flag = misc + 1;
+  float* csred = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + C::BAR_BYTES);  // [2][4][BN]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto csum_bar = [&](int a, int h) { return bar0 + 8u * (2 * STAGES + 5 + 2 * a + h); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    for (int a = 0; a < 2; ++a)
+      for (int h = 0; h < 2; ++h) mbar_init(csum_bar(a, h), 4);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.num_m * p.num_n;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_dst = a_dst + C::A_BYTES;
+          if (!A_MN) tma_load_2d(a_dst, &tmA, kb * BK, m_blk * BM, fb);
+          else       tma_load_2d(a_dst, &tmA, m_blk * BM, kb * BK, fb);
+          if (!B_MN) {
+            tma_load_2d(b_dst, &tmB, kb * BK, n_blk * BN, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j) tma_load_2d(b_dst + j * 128 * BK, &tmB, n_blk * BN + j * 128, kb * BK, fb);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) for the copies of the last armed stages to land
+        const int64_t pending = issued < STAGES ? issued : STAGES;
+        int s = stage;
+        uint32_t ph = phase;
+        for (int64_t i = 0; i < pending; ++i) {
+          if (--s < 0) { s = STAGES - 1; ph ^= 1; }
+          uint32_t dummy_flag = 0;
+          mbar_wait(full_bar(s), ph, &dummy_flag, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_base = a_base + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t accum = (kb | kk) != 0;
+            const uint64_t ad = A_MN ? make_desc(a_base + kk * 32 * 128, 1024, 1024) : make_desc(a_base + kk * 32, 16, 1024);
+            if (!B_MN) {
+              mma_f8(d_tmem, ad, make_desc(b_base + kk * 32, 16, 1024), p.idesc, accum);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j)
+                mma_f8(d_tmem + j * 128, ad, make_desc(b_base + j * 128 * BK + kk * 32 * 128, 1024, 1024), p.idesc, accum);
+            }
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      if (!ok) {
+        // make sure no MMA still writes tensor memory before it is freed
+        mma_commit(drain_bar);
+        uint32_t dummy_flag = 0;
+        mbar_wait(drain_bar, 0, &dummy_flag, 100000000ull);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
+    const int half = (warp - 4) >> 2;      // column half of the tile
+    const int row_in_tile = quarter * 32 + lane;
+    constexpr int HALF_COLS = BN / 2;
+    constexpr int CHUNKS = HALF_COLS / 32;
+    const float s = __fmul_rn(*p.sinv_a, *p.sinv_b);
+    float scale_q = 0.f;
+    if constexpr (EPI != EPI_STORE) scale_q = *p.scale_q;
+    uint32_t am = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    // With column sums, warp quarter 0 of each half combines the four 32-row
+    // partials of the tile; it releases the accumulator only after reading
+    // them, which keeps the partial buffer of this parity from being reused early.
+    const bool combiner = EPI == EPI_DGELU && p.colsum != nullptr && quarter == 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const int64_t m = (int64_t)m_blk * BM + row_in_tile;
+      const bool row_ok = m < p.M;
+#pragma unroll 1
+      for (int ch = 0; ch < CHUNKS; ++ch) {
+        const int col0 = half * HALF_COLS + ch * 32;
+        const int64_t n0 = (int64_t)n_blk * BN + col0;
+        uint32_t r[32];
+        if (p.num_kb > 0) {
+          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + col0), r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (ch == CHUNKS - 1 && !combiner) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        float v[32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int64_t n = n0 + g * 8;
+          const bool ok = row_ok && n < p.N;
+          float e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) e[i] = __uint_as_float(r[g * 8 + i]);
+          if constexpr (EPI == EPI_STORE) {
+            if (ok) {
+              float b[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) b[i] = 0.f;
+              if (p.bias) {
+                const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
+                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { b[2 * i] = bf16_bits_to_f32(bw[i] & 0xFFFFu); b[2 * i + 1] = bf16_bits_to_f32(bw[i] >> 16); }
+              }
+              uint4 o;
+              o.x = pack_bf16x2(fmaf(e[0], s, b[0]), fmaf(e[1], s, b[1]));
+              o.y = pack_bf16x2(fmaf(e[2], s, b[2]), fmaf(e[3], s, b[3]));
+              o.z = pack_bf16x2(fmaf(e[4], s, b[4]), fmaf(e[5], s, b[5]));
+              o.w = pack_bf16x2(fmaf(e[6], s, b[6]), fmaf(e[7], s, b[7]));
+              *reinterpret_cast<uint4*>(p.out + m * p.N + n) = o;
+            }
+          } else if constexpr (EPI == EPI_GELU) {
+            if (ok) {
+              float b[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) b[i] = 0.f;
+              if (p.bias) {
+                const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
+                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { b[2 * i] = bf16_bits_to_f32(bw[i] & 0xFFFFu); b[2 * i + 1] = bf16_bits_to_f32(bw[i] >> 16); }
+              }
+              uint32_t hw[4];
+              float a[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                hw[i] = pack_bf16x2(fmaf(e[2 * i], s, b[2 * i]), fmaf(e[2 * i + 1], s, b[2 * i + 1]));
+                const float h0 = bf16_bits_to_f32(hw[i] & 0xFFFFu), h1 = bf16_bits_to_f32(hw[i] >> 16);
+                a[2 * i] = 0.5f * h0 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h0 * h0, h0, h0)));
+                a[2 * i + 1] = 0.5f * h1 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h1 * h1, h1, h1)));
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) am = max(am, abs_bits(a[i]));
+              *reinterpret_cast<uint4*>(p.out + m * p.N + n) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint2*>(p.out_q + m * p.N + n) = cvt_fp8x8<QDT>(a, scale_q);
+              if (p.dbg) {
+                float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
+                d4[0] = make_float4(a[0], a[1], a[2], a[3]);
+                d4[1] = make_float4(a[4], a[5], a[6], a[7]);
+              }
+            }
+          } else {  // EPI_DGELU
+            float dh[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dh[i] = 0.f;
+            if (ok) {
+              const uint4 hu = *reinterpret_cast<const uint4*>(p.h_in + m * p.N + n);
+              const uint32_t hw[4] = {hu.x, hu.y, hu.z, hu.w};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float h = bf16_bits_to_f32(i & 1 ? hw[i >> 1] >> 16 : hw[i >> 1] & 0xFFFFu);
+                const float t = tanh_fast(kGeluK * fmaf(kGeluC * h * h, h, h));
+                const float gp = fmaf(0.5f * h * (1.0f - t * t), kGeluK * fmaf(3.0f * kGeluC, h * h, 1.0f), 0.5f * (1.0f + t));
+                dh[i] = __fmul_rn(e[i], s) * gp;
+                am = max(am, abs_bits(dh[i]));
+              }
+              *reinterpret_cast<uint2*>(p.out_q + m * p.N + n) = cvt_fp8x8<QDT>(dh, scale_q);
+              if (p.dbg) {
+                float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
+                d4[0] = make_float4(dh[0], dh[1], dh[2], dh[3]);
+                d4[1] = make_float4(dh[4], dh[5], dh[6], dh[7]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[g * 8 + i] = dh[i];
+          }
+        }
+        if constexpr (EPI == EPI_DGELU) {
+          if (p.colsum) csred[(acc * 4 + quarter) * BN + col0 + lane] = transpose_reduce32(v, lane);
+        }
+      }
+      if constexpr (EPI == EPI_DGELU) {
+        if (p.colsum) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(csum_bar(acc, half));
+          if (combiner) {
+            if (!mbar_wait(csum_bar(acc, half), acc_phase, abort_flag)) break;
+            for (int c = lane; c < HALF_COLS; c += 32) {
+              const int col = half * HALF_COLS + c;
+              const int64_t n = (int64_t)n_blk * BN + col;
+              const float* cs = csred + acc * 4 * BN + col;
+              const float tot = (cs[0] + cs[BN]) + (cs[2 * BN] + cs[3 * BN]);
+              if (n < p.N) atomicAdd(p.colsum + n, tot);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+          }
+        }
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+    if constexpr (EPI != EPI_STORE) {
+      am = warp_max_u32(am);
+      if (lane == 0 && am != 0u) atomic_max_amax(p.amax_q, am);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
+  }
+}
+
+// Diagnostic: one bounded wait on an mbarrier that nothing arrives on. It
+// gives up after limit_ns, sets the status word and returns, which is how the
+// timeout path of every pipeline wait above is exercised without a hang.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &flag, limit_ns);
+}
+
+// ------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D uint8 tensor map: inner extent `inner` (contiguous), `outer` rows, box
+// {128, box_outer}, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, int box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)inner};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint32_t make_idesc(int n_mma, int a_dt, int b_dt, bool a_mn, bool b_mn) {
+  return (1u << 4) |                       // accumulator fp32
+         ((uint32_t)a_dt << 7) |           // A: 0 E4M3, 1 E5M2
+         ((uint32_t)b_dt << 10) |          // B
+         ((a_mn ? 1u : 0u) << 15) |        // A major (1 = MN)
+         ((b_mn ? 1u : 0u) << 16) |        // B major
+         ((uint32_t)(n_mma >> 3) << 17) |  // N / 8
+         ((uint32_t)(BM >> 4) << 24);      // M / 16
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
+lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, cudaStream_t st) {
+  auto k = gemm_kernel<BN, A_MN, B_MN, EPI, QDT>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) != cudaSuccess)
+      return check_launch("fp8 gemm: shared memory attribute");
+    attr = true;
+  }
+  const int tiles = kp.num_m * kp.num_n;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  k<<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, kp);
+  return check_launch("fp8 gemm");
+}
+
+template <int BN, int EPI, int QDT>
+lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp,
+                            cudaStream_t st) {
+  if (!a_mn && !b_mn) return launch_t<BN, false, false, EPI, QDT>(ta, tb, kp, st);
+  if (!a_mn && b_mn) return launch_t<BN, false, true, EPI, QDT>(ta, tb, kp, st);
+  if (a_mn && b_mn) return launch_t<BN, true, true, EPI, QDT>(ta, tb, kp, st);
+  return launch_t<BN, true, false, EPI, QDT>(ta, tb, kp, st);
+}
+
+}  // namespace
+
+lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>((uint64_t)limit_ns);
+  return check_launch("lnfp8_selftest_timeout");
+}
+
+lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
+  if (g.M == 0 || g.N == 0) return LNFP8_OK;
+  if (g.M > 0x7FFFFFFF || g.N > 0x7FFFFFFF || g.K > 0x7FFFFFFF)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm: dimension above 2^31");
+  const bool a_mn = g.a_layout == 1, b_mn = g.b_layout == 1;
+  // Tile width: 256 columns unless that leaves most SMs idle.
+  const int64_t num_m = (g.M + BM - 1) / BM;
+  int bn = 256;
+  if (g.epi == EPI_STORE && num_m * ((g.N + 255) / 256) < (int64_t)num_sms()) bn = 128;
+  const int64_t num_n = (g.N + bn - 1) / bn;
+  if (num_m * num_n > 0x7FFFFFFF) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm: too many tiles");
+
+  CUtensorMap ta, tb;
+  const int64_t K = g.K > 0 ? g.K : 1;  // a zero-K product never loads; keep the map valid
+  bool ok = a_mn ? make_map(&ta, g.a, g.M, K, BK) : make_map(&ta, g.a, K, g.M, BM);
+  ok = ok && (b_mn ? make_map(&tb, g.b, g.N, K, BK) : make_map(&tb, g.b, K, g.N, bn));
+  if (!ok) return set_error(LNFP8_ERR_CUDA, "fp8 gemm: cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+
+  KParams kp;
+  kp.M = (int)g.M;
+  kp.N = (int)g.N;
+  kp.K = (int)g.K;
+  kp.num_m = (int)num_m;
+  kp.num_n = (int)num_n;
+  kp.num_kb = (int)((g.K + BK - 1) / BK);
+  kp.idesc = make_idesc(b_mn ? 128 : bn, g.a_dtype, g.b_dtype, a_mn, b_mn);
+  kp.sinv_a = g.sinv_a;
+  kp.sinv_b = g.sinv_b;
+  kp.bias = g.bias;
+  kp.out = g.out;
+  kp.h_in = g.h_in;
+  kp.out_q = g.out_q;
+  kp.scale_q = g.scale_q;
+  kp.amax_q = g.amax_q;
+  kp.colsum = g.colsum;
+  kp.dbg = g.dbg;
+
+  if (g.epi == EPI_STORE) {
+    if (bn == 256) return launch_layouts<256, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, kp, st);
+    return launch_layouts<128, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, kp, st);
+  }
+  if (g.epi == EPI_GELU && !a_mn && !b_mn) {
+    if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, false, EPI_GELU, LNFP8_E4M3>(ta, tb, kp, st);
+    return launch_t<256, false, false, EPI_GELU, LNFP8_E5M2>(ta, tb, kp, st);
+  }
+  if (g.epi == EPI_DGELU && !a_mn && b_mn) {
+    if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, true, EPI_DGELU, LNFP8_E4M3>(ta, tb, kp, st);
+    return launch_t<256, false, true, EPI_DGELU, LNFP8_E5M2>(ta, tb, kp, st);
+  }
+  return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: epilogue %d with layouts (%d, %d) is not built", g.epi,
+                   g.a_layout, g.b_layout);
+}
+
+}  // namespace lnfp8

@@ -1,0 +1,59 @@
+// Internal launchers of liblnfp8 (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lnfp8.h"
+
+namespace lnfp8 {
+
+lnfp8_status validate_meta(const lnfp8_meta* m, int expect_n, const char* who);
+lnfp8_status meta_init_launch(const lnfp8_meta* m, cudaStream_t st);
+lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, float* sinv_before,
+                           cudaStream_t st);
+
+lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
+                         const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
+                         float* colsum, cudaStream_t st);
+
+lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
+                           int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
+                           uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st);
+lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
+                           const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
+                           float* dbeta, cudaStream_t st);
+
+// Epilogues of the FP8 GEMM.
+enum GemmEpilogue {
+  EPI_STORE = 0,  // out = acc * sinv_a * sinv_b (+ bias) -> bf16
+  EPI_GELU = 1,   // h = bf16(acc * s + bias) -> out; a = gelu(h) -> fp8(a * scale_q) + amax
+  EPI_DGELU = 2,  // dh = acc * s * gelu'(h_in) -> fp8(dh * scale_q) + amax + column sums
+};
+
+struct GemmArgs {
+  // operands: layout 0 = [rows, K] K-contiguous, 1 = [K, rows] rows-contiguous
+  const uint8_t* a;
+  int a_layout, a_dtype;
+  const uint8_t* b;
+  int b_layout, b_dtype;
+  int64_t M, N, K;
+  const float* sinv_a;
+  const float* sinv_b;
+  int epi;
+  const uint16_t* bias;  // [N] bf16 or NULL
+  uint16_t* out;         // [M, N] bf16 (STORE, GELU)
+  // GELU / DGELU
+  const uint16_t* h_in;  // [M, N] bf16 (DGELU)
+  uint8_t* out_q;        // [M, N] codes
+  int q_dtype;
+  const float* scale_q;
+  float* amax_q;
+  float* colsum;         // [N] fp32 (DGELU), accumulated: the caller clears it
+  float* dbg;            // optional [M, N] fp32 pre-cast value
+};
+
+lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st);
+lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st);
+
+}  // namespace lnfp8

@@ -1,0 +1,313 @@
+// K1: row LayerNorm + amax + FP8 cast, and K5: LayerNorm backward.
+//
+// LayerNormLinear / LayerNormMLP open with a LayerNorm over each token row
+// (TE tutorial, code block 1: te.LayerNormLinear, te.LayerNormMLP; Turbo-charging
+// guide, "The building blocks: fused modules you'll use"). The forward kernel
+// fuses the normalisation with the delayed-scaling cast of its output: y is
+// formed in fp32, its max |y| folds into the tensor's running amax, and
+// fp8(y * scale) is written with the scale decided before the step, so the
+// fp32/bf16 LayerNorm output never reaches HBM.
+//
+// Both kernels are HBM-bound. A group of TPR threads owns one row (TPR = 32 is
+// a warp per row; wider rows use 64..256 threads so that a thread keeps at
+// most 4 x 16-byte vectors of the row in registers). Loads are 128-bit,
+// consecutive threads read consecutive 16-byte chunks, and row sums are warp
+// shuffles (plus one shared-memory exchange when TPR > 32).
+#include "common.cuh"
+#include "internal.h"
+
+namespace lnfp8 {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void unpack8(uint4 u, float* v) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+}
+
+// Sum over the TPR threads of a row group. `xch` holds kThreads/32 floats.
+template <int TPR>
+__device__ __forceinline__ float group_sum(float v, float* xch) {
+  v = warp_sum(v);
+  if constexpr (TPR == 32) {
+    return v;
+  } else {
+    const int warp = threadIdx.x >> 5;
+    const int group = threadIdx.x / TPR;
+    constexpr int WPG = TPR / 32;
+    if ((threadIdx.x & 31) == 0) xch[warp] = v;
+    asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(TPR) : "memory");
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < WPG; ++w) s += xch[group * WPG + w];
+    asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(TPR) : "memory");
+    return s;
+  }
+}
+
+template <int TPR, int NV, int DT>
+__global__ void __launch_bounds__(kThreads)
+ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+              const uint16_t* __restrict__ beta, float eps, int64_t M, int D,
+              const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
+              float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg) {
+  __shared__ float xch[kThreads / 32];
+  __shared__ uint32_t ared[kThreads / 32];
+  constexpr int GPB = kThreads / TPR;  // row groups per block
+  const int g = threadIdx.x / TPR;
+  const int gt = threadIdx.x % TPR;
+  const float s = *scale_p;
+  const float inv_d = 1.0f / (float)D;
+  uint32_t am = 0;
+
+  for (int64_t row = (int64_t)blockIdx.x * GPB + g; row - g < M; row += (int64_t)gridDim.x * GPB) {
+    // every thread of the block runs the same trip count (group_sum has barriers)
+    const bool active = row < M;
+    uint4 raw[NV];
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      raw[j] = make_uint4(0, 0, 0, 0);
+      if (active && c < D) raw[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
+      float v[8];
+      unpack8(raw[j], v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += v[i];
+    }
+    const float mu = group_sum<TPR>(sum, xch) * inv_d;
+    float sq = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      if (c < D) {
+        float v[8];
+        unpack8(raw[j], v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float d = v[i] - mu;
+          sq += d * d;
+        }
+      }
+    }
+    const float var = group_sum<TPR>(sq, xch) * inv_d;
+    const float rs = 1.0f / sqrtf(var + eps);
+    if (!active) continue;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      if (c >= D) continue;
+      float v[8], gm[8], bt[8], y[8];
+      unpack8(raw[j], v);
+      unpack8(*reinterpret_cast<const uint4*>(gamma + c), gm);
+      unpack8(*reinterpret_cast<const uint4*>(beta + c), bt);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        y[i] = fmaf((v[i] - mu) * rs, gm[i], bt[i]);
+        am = max(am, abs_bits(y[i]));
+      }
+      *reinterpret_cast<uint2*>(out + row * D + c) = cvt_fp8x8<DT>(y, s);
+      if (ydbg) {
+        float4* d4 = reinterpret_cast<float4*>(ydbg + row * D + c);
+        d4[0] = make_float4(y[0], y[1], y[2], y[3]);
+        d4[1] = make_float4(y[4], y[5], y[6], y[7]);
+      }
+    }
+    if (gt == 0) {
+      mu_out[row] = mu;
+      rs_out[row] = rs;
+    }
+  }
+  block_amax_commit(am, ared, amax_cur);
+}
+
+template <int TPR, int NV>
+__global__ void __launch_bounds__(kThreads)
+ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
+              const uint16_t* __restrict__ gamma, const float* __restrict__ mu_in,
+              const float* __restrict__ rs_in, int64_t M, int D, uint16_t* __restrict__ dx,
+              float* dgamma, float* dbeta) {
+  __shared__ float xch[kThreads / 32];
+  extern __shared__ float colred[];  // [2][D] block partials of dgamma, dbeta
+  constexpr int GPB = kThreads / TPR;
+  const int g = threadIdx.x / TPR;
+  const int gt = threadIdx.x % TPR;
+  const float inv_d = 1.0f / (float)D;
+
+  for (int c = threadIdx.x; c < 2 * D; c += kThreads) colred[c] = 0.f;
+
+  float accg[NV][8], accb[NV][8], gm[NV][8];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int c = (gt + TPR * j) * 8;
+    uint4 graw = make_uint4(0, 0, 0, 0);
+    if (c < D) graw = *reinterpret_cast<const uint4*>(gamma + c);
+    unpack8(graw, gm[j]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) accg[j][i] = accb[j][i] = 0.f;
+  }
+
+  for (int64_t row = (int64_t)blockIdx.x * GPB + g; row - g < M; row += (int64_t)gridDim.x * GPB) {
+    const bool active = row < M;
+    const float mu = active ? mu_in[row] : 0.f;
+    const float rs = active ? rs_in[row] : 0.f;
+    uint4 rx[NV], rd[NV];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      rx[j] = rd[j] = make_uint4(0, 0, 0, 0);
+      if (active && c < D) {
+        rx[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
+        rd[j] = *reinterpret_cast<const uint4*>(dy + row * D + c);
+      }
+      float xv[8], dv[8];
+      unpack8(rx[j], xv);
+      unpack8(rd[j], dv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float xh = (xv[i] - mu) * rs;
+        const float gg = dv[i] * gm[j][i];
+        s1 += gg;
+        s2 += gg * xh;
+        accg[j][i] = fmaf(dv[i], xh, accg[j][i]);
+        accb[j][i] += dv[i];
+      }
+    }
+    const float mean_g = group_sum<TPR>(s1, xch) * inv_d;
+    const float mean_gx = group_sum<TPR>(s2, xch) * inv_d;
+    if (!active) continue;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      if (c >= D) continue;
+      float xv[8], dv[8], o[8];
+      unpack8(rx[j], xv);
+      unpack8(rd[j], dv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float xh = (xv[i] - mu) * rs;
+        o[i] = rs * (dv[i] * gm[j][i] - mean_g - xh * mean_gx);
+      }
+      uint4 p;
+      p.x = pack_bf16x2(o[0], o[1]);
+      p.y = pack_bf16x2(o[2], o[3]);
+      p.z = pack_bf16x2(o[4], o[5]);
+      p.w = pack_bf16x2(o[6], o[7]);
+      *reinterpret_cast<uint4*>(dx + row * D + c) = p;
+    }
+  }
+
+  // block reduction of the column partials, then one atomic per column per block
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int c = (gt + TPR * j) * 8;
+    if (c >= D) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      atomicAdd(&colred[c + i], accg[j][i]);
+      atomicAdd(&colred[D + c + i], accb[j][i]);
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += kThreads) {
+    atomicAdd(dgamma + c, colred[c]);
+    atomicAdd(dbeta + c, colred[D + c]);
+  }
+}
+
+// Threads per row and 16-byte vectors per thread for a row of D bf16.
+struct RowShape { int tpr, nv; };
+RowShape row_shape(int64_t D) {
+  const int64_t vecs = (D + 7) / 8;
+  for (int tpr = 32; tpr <= 256; tpr *= 2) {
+    const int64_t nv = (vecs + tpr - 1) / tpr;
+    if (nv <= 4) return {tpr, (int)nv};
+  }
+  return {0, 0};
+}
+
+template <int DT>
+lnfp8_status ln_fwd_dispatch(RowShape rsh, dim3 grid, cudaStream_t st, const uint16_t* x,
+                             const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int D,
+                             const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
+                             float* ydbg) {
+#define LNF(TPR, NV) ln_fwd_kernel<TPR, NV, DT><<<grid, kThreads, 0, st>>>(x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg)
+  switch (rsh.tpr * 10 + rsh.nv) {
+    case 321: LNF(32, 1); break;
+    case 322: LNF(32, 2); break;
+    case 323: LNF(32, 3); break;
+    case 324: LNF(32, 4); break;
+    case 643: LNF(64, 3); break;
+    case 644: LNF(64, 4); break;
+    case 1283: LNF(128, 3); break;
+    case 1284: LNF(128, 4); break;
+    case 2563: LNF(256, 3); break;
+    case 2564: LNF(256, 4); break;
+    default: return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: unsupported D");
+  }
+#undef LNF
+  return check_launch("ln_fwd_cast");
+}
+
+}  // namespace
+
+lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
+                           int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
+                           uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st) {
+  if (M == 0) return LNFP8_OK;
+  const RowShape rsh = row_shape(D);
+  if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: D = %lld > 8192", (long long)D);
+  const int64_t gpb = kThreads / rsh.tpr;
+  const int64_t blocks = min64((M + gpb - 1) / gpb, 8LL * num_sms());
+  dim3 grid((unsigned)blocks);
+  if (dtype == LNFP8_E4M3)
+    return ln_fwd_dispatch<LNFP8_E4M3>(rsh, grid, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
+  return ln_fwd_dispatch<LNFP8_E5M2>(rsh, grid, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
+}
+
+lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
+                           const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
+                           float* dbeta, cudaStream_t st) {
+  if (D > 0) {
+    if (cudaMemsetAsync(dgamma, 0, D * sizeof(float), st) != cudaSuccess ||
+        cudaMemsetAsync(dbeta, 0, D * sizeof(float), st) != cudaSuccess)
+      return check_launch("ln_bwd: clearing dgamma/dbeta");
+  }
+  if (M == 0) return LNFP8_OK;
+  const RowShape rsh = row_shape(D);
+  if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: D = %lld > 8192", (long long)D);
+  const int64_t gpb = kThreads / rsh.tpr;
+  const int64_t blocks = min64((M + gpb - 1) / gpb, 2LL * num_sms());
+  const size_t smem = 2 * D * sizeof(float);
+  dim3 grid((unsigned)blocks);
+#define LNB(TPR, NV)                                                                                   \
+  do {                                                                                                 \
+    auto k = ln_bwd_kernel<TPR, NV>;                                                                   \
+    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    k<<<grid, kThreads, smem, st>>>(dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta);          \
+  } while (0)
+  switch (rsh.tpr * 10 + rsh.nv) {
+    case 321: LNB(32, 1); break;
+    case 322: LNB(32, 2); break;
+    case 323: LNB(32, 3); break;
+    case 324: LNB(32, 4); break;
+    case 643: LNB(64, 3); break;
+    case 644: LNB(64, 4); break;
+    case 1283: LNB(128, 3); break;
+    case 1284: LNB(128, 4); break;
+    case 2563: LNB(256, 3); break;
+    case 2564: LNB(256, 4); break;
+    default: return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: unsupported D");
+  }
+#undef LNB
+  return check_launch("ln_bwd");
+}
+
+}  // namespace lnfp8

@@ -1,0 +1,269 @@
+"""LayerNormMLP / LayerNormLinear / Linear forward + backward through the C ABI
+against the CPU oracle, over several delayed-scaling steps (GPU).
+
+Each step is checked three ways:
+  * step by step on the GPU's own intermediates (codes bit-exact against the
+    oracle's cast of the kernel's fp32 pre-cast dumps, GEMMs against the
+    oracle's GEMM of the GPU's codes);
+  * end to end against an independent oracle run from the same inputs and the
+    same (teacher-forced) pre-step state: bf16 outputs and gradients within
+    1e-2 relative Frobenius error;
+  * the delayed-scaling state after the step equals, bit for bit, the oracle's
+    state machine fed the amaxes the GPU recorded; amaxes of exact inputs (the
+    weights, dY) equal the oracle's bit for bit, amaxes of computed tensors
+    agree within 2e-3 (LN output) and 1e-2 (GELU output, dH).
+"""
+import numpy as np
+import pytest
+
+from fp8_delayed_scaling_row_gb300 import synth
+from oracle import fp8 as ofp8
+from oracle import gelu as ogelu
+from oracle import modules as omod
+from oracle.delayed_scaling import Recipe as ORecipe, ScalingState
+from oracle.gemm import bf16_to_f32, dequant_scale, to_bf16_bits
+from helpers import bf16_dev, host, rel_fro
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_delayed_scaling_row_gb300 import lnfp8
+    return lnfp8
+
+
+def _state_from_gpu(meta):
+    s = ScalingState(meta.n, meta.history_len)
+    s.scale[:] = host(meta.scale)
+    s.scale_inv[:] = host(meta.scale_inv)
+    s.amax_history[:] = host(meta.amax_history)
+    s.amax_cur[:] = host(meta.amax_cur)
+    return s
+
+
+def _assert_state_equal(meta, ost, what):
+    for name in ("scale", "scale_inv", "amax_history", "amax_cur"):
+        g = host(getattr(meta, name)).astype(np.float32)
+        assert np.array_equal(g.view(np.uint32), getattr(ost, name).view(np.uint32)), (what, name)
+
+
+def _teacher_forced(pre: ScalingState, meta, fmts):
+    """The oracle state machine run from the pre-step state with the amaxes the GPU recorded."""
+    st = pre.copy()
+    am = host(meta.amax_history)[0].astype(np.float32)
+    for i in range(st.n):
+        st.record(i, am[i])
+    st.update(fmts)
+    return st
+
+
+def _bf16(x):
+    return bf16_to_f32(to_bf16_bits(x)).astype(np.float64)
+
+
+def _rel_amax(a, b):
+    return abs(float(a) - float(b)) / max(abs(float(b)), 1e-30)
+
+
+def run_mlp(L, M, D, F, steps, fmt="hybrid", hist=4, dist="outliers", bias_std=0.02, seed=11, full_check_steps=None,
+            sample_rows=None):
+    rec = L.Recipe(fmt, hist)
+    orec = ORecipe(fmt, hist)
+    p = synth.mlp_params(D, F, seed=seed, bias_std=bias_std)
+    dev = {k: bf16_dev(v) for k, v in p.items()}
+    fm, bm = L.ScalingMeta(4, hist), L.ScalingMeta(2, hist)
+    ffmt, gfmt = orec.fwd_fmt(), orec.bwd_fmt()
+    full_check_steps = range(steps) if full_check_steps is None else full_check_steps
+    ctx = L.mlp_ctx(M, D, F, debug=True)
+    grads = L.mlp_grads(M, D, F, debug=True)
+    for step in range(steps):
+        x = synth.activations(M, D, dist=dist, seed=seed, step=step)
+        dy = synth.grad(M, D, seed=seed, step=step)
+        xt, dyt = bf16_dev(x), bf16_dev(dy)
+        fpre, bpre = _state_from_gpu(fm), _state_from_gpu(bm)
+        y, _ = L.ln_mlp_fwd(xt, dev["gamma"], dev["beta"], dev["w1"], dev["b1"], dev["w2"], dev["b2"], fm, rec, ctx=ctx)
+        g = L.ln_mlp_bwd(dyt, xt, dev["gamma"], ctx, bm, rec, grads=grads)
+        L.sync_status()
+
+        # state: bit-exact against the oracle state machine fed the GPU's amaxes
+        _assert_state_equal(fm, _teacher_forced(fpre, fm, [ffmt] * 4), f"fwd step {step}")
+        _assert_state_equal(bm, _teacher_forced(bpre, bm, [gfmt] * 2), f"bwd step {step}")
+        am_f = host(fm.amax_history)[0]
+        am_b = host(bm.amax_history)[0]
+        W1, W2 = bf16_to_f32(p["w1"]), bf16_to_f32(p["w2"])
+        assert am_f[1] == ofp8.amax(W1) and am_f[3] == ofp8.amax(W2)
+        assert am_b[0] == ofp8.amax(bf16_to_f32(dy))
+        sc, gsc = fpre.scale, bpre.scale
+        si, gsi = fpre.scale_inv, bpre.scale_inv
+        assert np.array_equal(host(ctx.sinv_saved).view(np.uint32), si.view(np.uint32))
+
+        # weights: exact inputs -> bit-exact codes
+        assert np.array_equal(host(ctx.w1q), ofp8.quantize(W1, sc[1], ffmt))
+        assert np.array_equal(host(ctx.w2q), ofp8.quantize(W2, sc[3], ffmt))
+
+        if step not in full_check_steps:
+            continue
+        rows = np.arange(M) if sample_rows is None else sample_rows
+        # ---- step-by-step on the GPU's intermediates
+        ydbg = host(ctx.ln_out_debug)
+        lnq = host(ctx.lnq)
+        assert np.array_equal(lnq, ofp8.quantize(ydbg, sc[0], ffmt))
+        assert am_f[0] == ofp8.amax(ydbg)
+        hq = host(ctx.h)
+        w1q, w2q = host(ctx.w1q), host(ctx.w2q)
+        h_ref = ofp8.decode(lnq[rows], ffmt) @ ofp8.decode(w1q, ffmt).T * np.float64(dequant_scale(si[0], si[1])) \
+            + bf16_to_f32(p["b1"])[None, :]
+        assert np.abs(hq[rows] - h_ref).max() <= 2.0 ** -7 * np.abs(h_ref).max() + 1e-6
+        assert rel_fro(hq[rows], _bf16(h_ref)) < 1e-3
+        adbg = host(ctx.act_debug)
+        a_ref = ogelu.gelu(hq[rows])
+        assert np.abs(adbg[rows] - a_ref).max() <= 2e-3 * np.abs(a_ref).max()
+        aq = host(ctx.aq)
+        assert np.array_equal(aq, ofp8.quantize(adbg, sc[2], ffmt))
+        assert am_f[2] == ofp8.amax(adbg)
+        yv = host(y)
+        y_ref = ofp8.decode(aq[rows], ffmt) @ ofp8.decode(w2q, ffmt).T * np.float64(dequant_scale(si[2], si[3])) \
+            + bf16_to_f32(p["b2"])[None, :]
+        assert rel_fro(yv[rows], _bf16(y_ref)) < 1e-3
+        dyq = host(g.dyq)
+        assert np.array_equal(dyq, ofp8.quantize(bf16_to_f32(dy), gsc[0], gfmt))
+        dhd = host(g.dh_debug)
+        da_ref = ofp8.decode(dyq[rows], gfmt) @ ofp8.decode(w2q, ffmt) * np.float64(dequant_scale(gsi[0], si[3]))
+        dh_ref = da_ref * ogelu.gelu_grad(hq[rows])
+        assert rel_fro(dhd[rows], dh_ref) < 2e-3
+        dhq = host(g.dhq)
+        assert np.array_equal(dhq, ofp8.quantize(dhd, gsc[1], gfmt))
+        assert am_b[1] == ofp8.amax(dhd)
+        if sample_rows is None:
+            dw2_ref = ofp8.decode(dyq, gfmt).T @ ofp8.decode(aq, ffmt) * np.float64(dequant_scale(gsi[0], si[2]))
+            assert rel_fro(host(g.dw2), _bf16(dw2_ref)) < 1e-3
+            dw1_ref = ofp8.decode(dhq, gfmt).T @ ofp8.decode(lnq, ffmt) * np.float64(dequant_scale(gsi[1], si[0]))
+            assert rel_fro(host(g.dw1), _bf16(dw1_ref)) < 1e-3
+            assert rel_fro(host(g.db1), dhd.astype(np.float64).sum(axis=0)) < 1e-4
+        dln_ref = ofp8.decode(dhq[rows], gfmt) @ ofp8.decode(w1q, ffmt) * np.float64(dequant_scale(gsi[1], si[1]))
+        assert rel_fro(host(g.dln)[rows], _bf16(dln_ref)) < 1e-3
+
+        # ---- end to end against the independent oracle (same inputs, same pre-step state)
+        fo, bo = fpre.copy(), bpre.copy()
+        Y, octx, aux = omod.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], fo, orec)
+        og = omod.ln_mlp_bwd(dy, octx, bo, orec)
+        assert rel_fro(yv, Y) < TOL
+        for k in ("dx", "dw1", "dw2", "db1", "db2", "dgamma", "dbeta"):
+            gv = host(getattr(g, k))
+            assert rel_fro(gv, og[k]) < TOL, (step, k, rel_fro(gv, og[k]))
+        # independent amaxes of computed tensors
+        assert _rel_amax(am_f[0], ofp8.amax(aux["y"])) < 2e-3
+        assert _rel_amax(am_f[2], ofp8.amax(aux["a"])) < TOL
+        assert _rel_amax(am_b[1], ofp8.amax(og["dh"])) < TOL
+        # the oracle's own state machine agrees on the exact-input slots
+        for i in (1, 3):
+            assert fo.scale[i] == host(fm.scale)[i]
+        assert bo.scale[0] == host(bm.scale)[0]
+    return fm, bm
+
+
+def test_mlp_small_multistep_hybrid(L):
+    run_mlp(L, M=300, D=256, F=512, steps=4, hist=3)
+
+
+def test_mlp_e4m3_format_and_t3_inputs(L):
+    run_mlp(L, M=200, D=128, F=384, steps=3, fmt="e4m3", hist=2, dist="t3")
+
+
+def test_mlp_e5m2_format(L):
+    run_mlp(L, M=130, D=128, F=256, steps=2, fmt="e5m2", hist=16, dist="normal")
+
+
+def test_mlp_without_bias_and_single_row(L):
+    run_mlp(L, M=1, D=64, F=128, steps=2, bias_std=0.0)
+
+
+def test_mlp_empty_batch(L):
+    rec = L.Recipe("hybrid", 4)
+    D, F = 64, 128
+    p = {k: bf16_dev(v) for k, v in synth.mlp_params(D, F, seed=3).items()}
+    fm, bm = L.ScalingMeta(4, 4), L.ScalingMeta(2, 4)
+    x = torch.empty(0, D, dtype=torch.bfloat16, device="cuda")
+    y, ctx = L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], fm, rec)
+    g = L.ln_mlp_bwd(torch.empty(0, D, dtype=torch.bfloat16, device="cuda"), x, p["gamma"], ctx, bm, rec)
+    L.sync_status()
+    assert y.shape == (0, D)
+    for t in (g.dw1, g.dw2, g.db1, g.db2, g.dgamma, g.dbeta):
+        assert (host(t) == 0).all()
+    am = host(fm.amax_history)[0]
+    assert am[0] == 0 and am[2] == 0 and am[1] > 0 and am[3] > 0
+
+
+def test_mlp_config2_full_size_two_steps(L):
+    # LayerNormMLP 768 -> 3072 -> 768 over 8192 tokens (32 x 256), HYBRID, history 16
+    run_mlp(L, M=8192, D=768, F=3072, steps=2, hist=16, bias_std=0.0, seed=1234)
+
+
+def test_mlp_config2_twenty_steps_state(L):
+    # the 20-step run of the same workload: state bit-exact (teacher-forced) every step,
+    # full parity on the first and last step
+    run_mlp(L, M=8192, D=768, F=3072, steps=20, hist=16, bias_std=0.0, seed=1234, full_check_steps={0, 19},
+            sample_rows=np.arange(0, 8192, 37))
+
+
+def test_mlp_d2048_sampled_rows(L):
+    # LayerNormMLP 2048 -> 8192 -> 2048 over 2048 tokens, history 1024
+    run_mlp(L, M=2048, D=2048, F=8192, steps=2, hist=1024, bias_std=0.0, seed=1234, dist="t3",
+            sample_rows=np.arange(0, 2048, 17))
+
+
+# ------------------------------------------------------------------ LayerNormLinear / Linear
+def run_linear(L, M, K, N, steps, ln=True, fmt="hybrid", hist=16, bias_std=0.02, seed=21):
+    rec = L.Recipe(fmt, hist)
+    orec = ORecipe(fmt, hist)
+    p = synth.linear_params(N, K, ln=ln, bias_std=bias_std, seed=seed)
+    w, b = bf16_dev(p["w"]), bf16_dev(p["b"])
+    gma = bf16_dev(p["gamma"]) if ln else None
+    bta = bf16_dev(p["beta"]) if ln else None
+    fm, bm = L.ScalingMeta(2, hist), L.ScalingMeta(1, hist)
+    ffmt, gfmt = orec.fwd_fmt(), orec.bwd_fmt()
+    for step in range(steps):
+        x = synth.activations(M, K, dist="outliers", seed=seed, step=step)
+        dy = synth.grad(M, N, seed=seed, step=step)
+        xt = bf16_dev(x)
+        fpre, bpre = _state_from_gpu(fm), _state_from_gpu(bm)
+        y, ctx = L.ln_linear_fwd(xt, gma, bta, w, b, fm, rec, debug=ln)
+        g = L.ln_linear_bwd(bf16_dev(dy), xt, gma, ctx, bm, rec)
+        L.sync_status()
+        _assert_state_equal(fm, _teacher_forced(fpre, fm, [ffmt] * 2), f"fwd {step}")
+        _assert_state_equal(bm, _teacher_forced(bpre, bm, [gfmt]), f"bwd {step}")
+        xq = host(ctx.xq)
+        if ln:
+            ydbg = host(ctx.ln_out_debug)
+            assert np.array_equal(xq, ofp8.quantize(ydbg, fpre.scale[0], ffmt))
+        else:
+            assert np.array_equal(xq, ofp8.quantize(bf16_to_f32(x), fpre.scale[0], ffmt))
+        assert np.array_equal(host(ctx.wq), ofp8.quantize(bf16_to_f32(p["w"]), fpre.scale[1], ffmt))
+        fo, bo = fpre.copy(), bpre.copy()
+        Y, octx, _ = omod.ln_linear_fwd(x, p["gamma"], p["beta"], p["w"], p["b"], fo, orec)
+        og = omod.ln_linear_bwd(dy, octx, bo, orec)
+        assert rel_fro(host(y), Y) < TOL
+        assert rel_fro(host(g.dx), og["dx"]) < TOL
+        assert rel_fro(host(g.dw), og["dw"]) < TOL
+        assert rel_fro(host(g.dbias), og["db"]) < 1e-4
+        if ln:
+            assert rel_fro(host(g.dgamma), og["dgamma"]) < TOL
+            assert rel_fro(host(g.dbeta), og["dbeta"]) < TOL
+    return fm, bm
+
+
+def test_linear_config1_qkv_forward_e4m3(L):
+    # LayerNormLinear 768 -> 2304 over 256 tokens (8 x 32), E4M3, history 16, one step, bias 0
+    run_linear(L, M=256, K=768, N=2304, steps=1, fmt="e4m3", bias_std=0.0, seed=1234)
+
+
+def test_linear_with_ln_multistep_ragged(L):
+    run_linear(L, M=333, K=192, N=400, steps=3, hist=2)
+
+
+def test_linear_without_ln(L):
+    run_linear(L, M=250, K=256, N=128, steps=2, ln=False)
