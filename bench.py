@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""FP8 delayed-scaling LayerNormMLP forward+backward throughput on GB300.
+
+One step = ln_mlp_fwd + ln_mlp_bwd through the C ABI over one fresh batch:
+8192 tokens (32 x 256) of d_model 768, FFN 3072, HYBRID (E4M3 forward, E5M2
+gradients), amax_history_len 16, X ~ N(0,1) with 0.1% x50 outliers, dY ~
+N(0, 0.01), weights ~ N(0, 0.02), bias 0. FLOPs are the six FP8 GEMMs,
+12 * M * D * F per step.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle on the
+same metric instead (rank 0 only; other ranks exit at once).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 LayerNormMLP fwd+bwd TFLOP/s (D=768/2048) and % of GB300 FP8 dense peak"
+M_TOK, D_MODEL, FFN = 8192, 768, 3072
+HIST = 16
+FMT = "hybrid"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def flops_per_step(m=M_TOK, d=D_MODEL, f=FFN):
+    return 12.0 * m * d * f
+
+
+def workload(m=M_TOK, d=D_MODEL, f=FFN, fmt=FMT, hist=HIST, dist="outliers"):
+    return {"workload": f"LayerNormMLP fwd+bwd, {m} tokens x {d} -> {f} -> {d}, {fmt.upper()} "
+                        f"(E4M3 fwd / E5M2 grads), amax_history_len {hist}, fresh X and dY each step",
+            "tokens": m, "d_model": d, "ffn": f, "fp8_format": fmt, "amax_history_len": hist,
+            "x_dist": {"outliers": "N(0,1) + 0.1% entries x50", "normal": "N(0,1)", "t3": "Student-t(3)"}[dist],
+            "dy_dist": "N(0, 0.01)", "weights": "N(0, 0.02), bias 0",
+            "l2": "flushed (256 MiB write) between timed steps", "parallelism": "replicas (one per GPU)"}
+
+
+# ----------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def _num(d, *keys):
+    for k in keys:
+        if k in d and isinstance(d[k], (int, float)):
+            return float(d[k])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.idx)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gemm_traffic_from_profile():
+    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if the
+    kernel source is unchanged since it was captured (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        src = open(os.path.join(ROOT, "fp8_delayed_scaling_row_gb300", "csrc", "gemm.cu"), "rb").read()
+        if d.get("gemm_cu_sha1") != hashlib.sha1(src).hexdigest():
+            return None
+        return d.get("bytes_per_launch_step_avg")
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- CPU oracle arm
+def _oracle_setup(rows, ffn, seed=1234):
+    from fp8_delayed_scaling_row_gb300 import synth
+    from oracle.delayed_scaling import Recipe as ORecipe, ScalingState
+    p = synth.mlp_params(D_MODEL, ffn, seed=seed)
+    return p, ORecipe(FMT, HIST), ScalingState(4, HIST), ScalingState(2, HIST)
+
+
+def _oracle_step(p, rec, fs, bs, rows, step, seed=1234):
+    """One oracle step (LayerNormMLP fwd + bwd) on `rows` fresh tokens; returns its seconds."""
+    from fp8_delayed_scaling_row_gb300 import synth
+    from oracle import modules as om
+    x = synth.activations(rows, D_MODEL, dist="outliers", seed=seed, step=step)
+    dy = synth.grad(rows, D_MODEL, seed=seed, step=step)
+    t0 = time.perf_counter()
+    _, ctx, _ = om.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], fs, rec)
+    om.ln_mlp_bwd(dy, ctx, bs, rec)
+    return time.perf_counter() - t0
+
+
+def oracle_rate(seconds: float, rows: int, ffn: int = FFN):
+    """The oracle as it stands on `rows` tokens x `ffn` FFN columns per step, repeated for
+    about `seconds`; returns (TFLOP/s, steps, elapsed)."""
+    p, rec, fs, bs = _oracle_setup(rows, ffn)
+    el, n = 0.0, 0
+    while el < seconds:
+        el += _oracle_step(p, rec, fs, bs, rows, n)
+        n += 1
+    return flops_per_step(rows, D_MODEL, ffn) * n / el / 1e12, n, el
+
+
+def reference_sample(total_steps: int):
+    """(tokens, FFN columns) of one oracle step so that the whole run stays within a few minutes."""
+    budget = 150.0 / max(total_steps, 1)
+    if budget >= 6.0:
+        return 1024, FFN
+    if budget >= 1.8:
+        return 256, FFN
+    if budget >= 0.5:
+        return 128, 768
+    return 32, 256
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rows, ffn = reference_sample(args.steps + args.warmup)
+    p, rec, fs, bs = _oracle_setup(rows, ffn)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = _oracle_step(p, rec, fs, bs, rows, i)
+        if i >= args.warmup:
+            times.append(t)
+    el = sum(times)
+    val = flops_per_step(rows, D_MODEL, ffn) * len(times) / el / 1e12
+    sample = (f"each step: {rows} of the {M_TOK} tokens and {ffn} of the {FFN} FFN columns (LayerNormMLP "
+              f"{D_MODEL} -> {ffn} -> {D_MODEL}); numpy oracle, fp64 BLAS matmuls with the library's default "
+              f"threads; {args.steps} timed steps after {args.warmup} warm-up")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / len(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp8 codes decoded)",
+            "data": "synthetic", "config": workload(),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+class MlpRun:
+    """Device-resident workload: weights, state, saved tensors, gradient buffers,
+    and P pre-generated input batches cycled over the steps."""
+
+    def __init__(self, L, torch, dev, m, d, f, fmt, hist, dist, n_sets, seed):
+        from fp8_delayed_scaling_row_gb300 import synth
+        import numpy as np
+
+        def bf(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        self.L, self.torch, self.m, self.d, self.f = L, torch, m, d, f
+        p = synth.mlp_params(d, f, seed=seed)
+        self.p = {k: bf(v) for k, v in p.items()}
+        self.rec = L.Recipe(fmt, hist)
+        self.fm, self.bm = L.ScalingMeta(4, hist, device=dev), L.ScalingMeta(2, hist, device=dev)
+        self.ctx = L.mlp_ctx(m, d, f, device=dev)
+        self.grads = L.mlp_grads(m, d, f, device=dev)
+        self.y = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
+        self.xs_host, self.dys_host = [], []
+        for i in range(n_sets):
+            self.xs_host.append(synth.activations(m, d, dist=dist, seed=seed, step=i))
+            self.dys_host.append(synth.grad(m, d, seed=seed, step=i))
+        self.xs = [bf(x) for x in self.xs_host]
+        self.dys = [bf(x) for x in self.dys_host]
+
+    def step(self, i, x=None, dy=None):
+        L, p = self.L, self.p
+        x = self.xs[i % len(self.xs)] if x is None else x
+        dy = self.dys[i % len(self.dys)] if dy is None else dy
+        L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], self.fm, self.rec, y=self.y,
+                     ctx=self.ctx)
+        L.ln_mlp_bwd(dy, x, p["gamma"], self.ctx, self.bm, self.rec, grads=self.grads)
+
+
+def timed_steps(torch, run, steps, warmup, flush, barrier):
+    """W untimed warm-up steps, then K steps each bracketed by CUDA events on the
+    launching (current) stream, an L2 flush between them outside the events.
+    Returns (device ms summed over the K steps, library kernel launches in them)."""
+    for i in range(warmup):
+        run.step(i)
+    torch.cuda.synchronize()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    n0 = run.L.launch_count()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record()
+        run.step(warmup + i)
+        ev[i][1].record()
+    n1 = run.L.launch_count()
+    torch.cuda.synchronize()
+    barrier()
+    return sum(a.elapsed_time(b) for a, b in ev), n1 - n0
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from fp8_delayed_scaling_row_gb300 import lnfp8 as L
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_sets = min(args.steps + args.warmup, 8)
+    run = MlpRun(L, torch, dev, M_TOK, D_MODEL, FFN, FMT, HIST, "outliers", n_sets, seed=1234 + 7919 * rank)
+
+    # ---- main timed region (device time, CUDA events, L2 flushed between steps)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms, gpu_launches = timed_steps(torch, run, args.steps, args.warmup, flush, barrier)
+    clk = clocks.stop()
+    L.sync_status()
+    ms = max_over_ranks(ms)
+    ms_step = ms / args.steps
+    value = flops_per_step() * args.steps * world / (ms / 1e3) / 1e12
+
+    # ---- per-kernel times inside the same workload (events on the launching stream)
+    L.profile_enable(True)
+    prof_steps = min(args.steps, 50)
+    for i in range(prof_steps):
+        flush.zero_()
+        run.step(i)
+    prof = L.profile_collect()
+    L.profile_enable(False)
+    gemm_kinds = {k: v for k, v in prof.items() if k.startswith("gemm")}
+    g_ms = sum(v[0] for v in gemm_kinds.values())
+    g_n = sum(v[1] for v in gemm_kinds.values())
+    pk, how = peaks()
+    bf16 = _num(pk, "bf16_tflops", "bf16_tflops_burst") or FALLBACK["bf16_tflops"]
+    fp8_peak = bf16 * FP8_PER_BF16
+    g_flops = 2.0 * M_TOK * D_MODEL * FFN
+    achieved = g_flops / (g_ms / g_n / 1e3) / 1e12 if g_n else None
+    roofline = {"kernel": "fp8_gemm (tcgen05 kind::f8f6f4; the six GEMMs of the step)", "bound": "tensor",
+                "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak if achieved else None, "traffic": gemm_traffic_from_profile(),
+                "peak_source": f"{how} bf16 dense x {FP8_PER_BF16:g} (nominal FP8/BF16 ratio)",
+                "flops_per_launch": g_flops, "launches_timed": g_n,
+                "share_of_step": g_ms / sum(v[0] for v in prof.values()) if prof else None}
+    hbm = _num(pk, "hbm_gbs", "hbm_GBs", "hbm_copy_gbs") or FALLBACK["hbm_gbs"]
+    per_kernel = {}
+    for k, (kms, cnt) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
+        per_kernel[k] = {"ms_per_launch": kms / cnt, "launches_per_step": cnt / prof_steps,
+                         "share": kms / sum(v[0] for v in prof.values())}
+    # LayerNorm / cast kernels against HBM (algorithmic bytes per launch)
+    hbm_kernels = {
+        "ln_fwd_cast": M_TOK * D_MODEL * (2 + 1) + M_TOK * 8,
+        "ln_bwd": M_TOK * D_MODEL * (2 + 2 + 2) + M_TOK * 8,
+    }
+    for k, nbytes in hbm_kernels.items():
+        if k in per_kernel:
+            gbs = nbytes / (per_kernel[k]["ms_per_launch"] / 1e3) / 1e9
+            per_kernel[k].update({"algorithmic_bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / hbm})
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    e2e_steps = min(args.steps, 200)
+    xh = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in run.xs_host]
+    dyh = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in run.dys_host]
+    yh = torch.empty(M_TOK, D_MODEL, dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty(M_TOK, D_MODEL, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(M_TOK, D_MODEL, dtype=torch.bfloat16, device=dev)
+    dyd = torch.empty_like(xd)
+    for i in range(3):
+        xd.copy_(xh[i % len(xh)], non_blocking=True)
+        dyd.copy_(dyh[i % len(dyh)], non_blocking=True)
+        run.step(i, xd, dyd)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        xd.copy_(xh[i % len(xh)], non_blocking=True)
+        dyd.copy_(dyh[i % len(dyh)], non_blocking=True)
+        run.step(i, xd, dyd)
+        yh.copy_(run.y, non_blocking=True)
+        dxh.copy_(run.grads.dx, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e = {"value": flops_per_step() * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": 2 * M_TOK * D_MODEL * 2, "d2h_bytes_per_step": 2 * M_TOK * D_MODEL * 2,
+           "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+           "copies": "X, dY host->device (pinned) and Y, dX device->host, each step"}
+
+    # ---- D = 2048: LayerNormMLP 2048 -> 8192 -> 2048 over 16384 tokens (the scale-up width)
+    d2048 = None
+    if not args.no_d2048:
+        m2, d2, f2 = 16384, 2048, 8192
+        del run
+        torch.cuda.empty_cache()
+        run2 = MlpRun(L, torch, dev, m2, d2, f2, FMT, HIST, "normal", 4, seed=4321 + rank)
+        k2 = max(3, min(args.steps, 100))
+        ms2 = max_over_ranks(timed_steps(torch, run2, k2, 3, flush, barrier)[0])
+        d2048 = {"value": flops_per_step(m2, d2, f2) * k2 * world / (ms2 / 1e3) / 1e12, "unit": "TFLOP/s",
+                 "ms_per_step": ms2 / k2, "steps": k2, "frac_of_fp8_peak": None,
+                 "config": workload(m2, d2, f2, FMT, HIST, "normal")}
+        d2048["frac_of_fp8_peak"] = d2048["value"] / world / fp8_peak
+        del run2
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rows = args.cpu_rows
+        val, n, el = oracle_rate(args.cpu_seconds, rows)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n} oracle steps of {rows} of the {M_TOK} tokens, full FFN ({el:.1f} s of CPU time; "
+                         f"numpy, fp64 BLAS matmuls with the library's default threads)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)", "data": "synthetic",
+                "config": workload(), "frac_of_fp8_peak": value / world / fp8_peak,
+                "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline,
+                "per_kernel": per_kernel, "hbm_peak_gbs": hbm, "cpu_baseline": cpu, "d2048": d2048}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="tokens per oracle step of the cpu_baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-d2048", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -12,9 +12,13 @@
 // The casts of a step all use the scales decided before the step (delayed
 // scaling); the forward's scale_inv is saved for the backward because the
 // update at the end of the forward replaces it.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -50,6 +54,54 @@ int num_sms() {
     cache[dev] = n > 0 ? n : 1;
   }
   return cache[dev];
+}
+
+// ------------------------------------------------------------ launch accounting
+namespace {
+struct ProfRec {
+  const char* kind;
+  cudaEvent_t a, b;
+};
+struct ProfRow {
+  std::string kind;
+  double ms;
+  long long launches;
+};
+std::atomic<long long> g_launches{0};
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof_open;      // recorded, not yet collected
+std::vector<cudaEvent_t> g_event_pool;  // reusable events
+std::vector<ProfRow> g_prof_rows;      // the last collection
+thread_local int g_open_idx = -1;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+void launch_begin(const char* kind, cudaStream_t st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ProfRec r{kind, pool_event(), pool_event()};
+  cudaEventRecord(r.a, st);
+  g_prof_open.push_back(r);
+  g_open_idx = (int)g_prof_open.size() - 1;
+}
+
+void launch_end(cudaStream_t st) {
+  if (!g_prof_on.load(std::memory_order_relaxed) || g_open_idx < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_open_idx < (int)g_prof_open.size()) cudaEventRecord(g_prof_open[g_open_idx].b, st);
+  g_open_idx = -1;
 }
 
 namespace {
@@ -147,6 +199,55 @@ extern "C" {
 const char* lnfp8_last_error(void) { return g_msg; }
 
 int lnfp8_version(void) { return 100; }
+
+long long lnfp8_launch_count(void) { return g_launches.load(); }
+
+lnfp8_status lnfp8_profile_enable(int on) {
+  clear_error();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof_open) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof_open.clear();
+  g_prof_rows.clear();
+  g_prof_on.store(on != 0);
+  return LNFP8_OK;
+}
+
+int lnfp8_profile_collect(void) {
+  clear_error();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_rows.clear();
+  for (auto& r : g_prof_open) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      bool found = false;
+      for (auto& row : g_prof_rows)
+        if (row.kind == r.kind) {
+          row.ms += ms;
+          row.launches += 1;
+          found = true;
+          break;
+        }
+      if (!found) g_prof_rows.push_back({r.kind, (double)ms, 1});
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof_open.clear();
+  return (int)g_prof_rows.size();
+}
+
+lnfp8_status lnfp8_profile_get(int i, const char** kind, double* total_ms, long long* launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (i < 0 || i >= (int)g_prof_rows.size() || !kind || !total_ms || !launches)
+    return set_error(LNFP8_ERR_INVALID_ARG, "lnfp8_profile_get: bad index or NULL output");
+  *kind = g_prof_rows[i].kind.c_str();
+  *total_ms = g_prof_rows[i].ms;
+  *launches = g_prof_rows[i].launches;
+  return LNFP8_OK;
+}
 
 lnfp8_status lnfp8_sync_status(lnfp8_stream stream) {
   clear_error();

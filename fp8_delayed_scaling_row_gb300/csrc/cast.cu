@@ -138,6 +138,7 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
   if (strips > 0x7FFFFFFF || ysplit > 65535)
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8_quantize: tensor too large");
   dim3 grid((unsigned)strips, (unsigned)ysplit);
+  LaunchScope ls(colsum ? "cast_colsum" : "cast", st);
   if (in_fp32) {
     if (dtype == LNFP8_E4M3)
       cast_kernel<float, LNFP8_E4M3><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);

@@ -17,6 +17,16 @@ lnfp8_status check_launch(const char* what);
 void clear_error();
 int num_sms();
 
+// Launch accounting (api.cu): every kernel the library launches is counted,
+// and, while the profiler is on, bracketed by CUDA events on its stream.
+void launch_begin(const char* kind, cudaStream_t st);
+void launch_end(cudaStream_t st);
+struct LaunchScope {
+  cudaStream_t st;
+  LaunchScope(const char* kind, cudaStream_t s) : st(s) { launch_begin(kind, s); }
+  ~LaunchScope() { launch_end(st); }
+};
+
 // Sticky device status word (defined next to the kernels that set it, in
 // gemm.cu): bit 0 = a bounded wait gave up. Read and cleared from the host.
 constexpr unsigned int kStatusTimeout = 1u;

@@ -564,6 +564,9 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const KParam
   }
   const int tiles = kp.num_m * kp.num_n;
   const int grid = tiles < num_sms() ? tiles : num_sms();
+  static const char* kind = EPI == EPI_GELU ? "gemm_gelu" : EPI == EPI_DGELU ? "gemm_dgelu" :
+                            (A_MN ? (B_MN ? "gemm_mn_mn" : "gemm_mn_k") : (B_MN ? "gemm_k_mn" : "gemm_k_k"));
+  LaunchScope ls(kind, st);
   k<<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, kp);
   return check_launch("fp8 gemm");
 }
@@ -580,6 +583,7 @@ lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const C
 }  // namespace
 
 lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st) {
+  LaunchScope ls("selftest_wait", st);
   selftest_wait_kernel<<<1, 32, 0, st>>>((uint64_t)limit_ns);
   return check_launch("lnfp8_selftest_timeout");
 }

@@ -267,6 +267,7 @@ lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint1
   const int64_t gpb = kThreads / rsh.tpr;
   const int64_t blocks = min64((M + gpb - 1) / gpb, 8LL * num_sms());
   dim3 grid((unsigned)blocks);
+  LaunchScope ls("ln_fwd_cast", st);
   if (dtype == LNFP8_E4M3)
     return ln_fwd_dispatch<LNFP8_E4M3>(rsh, grid, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
   return ln_fwd_dispatch<LNFP8_E5M2>(rsh, grid, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
@@ -287,6 +288,7 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
   const int64_t blocks = min64((M + gpb - 1) / gpb, 2LL * num_sms());
   const size_t smem = 2 * D * sizeof(float);
   dim3 grid((unsigned)blocks);
+  LaunchScope ls("ln_bwd", st);
 #define LNB(TPR, NV)                                                                                   \
   do {                                                                                                 \
     auto k = ln_bwd_kernel<TPR, NV>;                                                                   \

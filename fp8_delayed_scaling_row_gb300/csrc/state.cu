@@ -83,6 +83,7 @@ lnfp8_status validate_meta(const lnfp8_meta* m, int expect_n, const char* who) {
 lnfp8_status meta_init_launch(const lnfp8_meta* m, cudaStream_t st) {
   const int64_t total = (int64_t)m->n * m->history_len;
   const int blocks = (int)min64((total + 255) / 256, 1024);
+  LaunchScope ls("state_init", st);
   init_kernel<<<blocks, 256, 0, st>>>(m->scale, m->scale_inv, m->amax_history, m->amax_cur, m->n, m->history_len);
   return check_launch("lnfp8_meta_init");
 }
@@ -94,6 +95,7 @@ lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, 
     if (cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return check_launch("amax_history_update: smem attribute");
   }
+  LaunchScope ls("state_update", st);
   update_kernel<<<m->n, kThreads, smem, st>>>(m->scale, m->scale_inv, m->amax_history, m->amax_cur, m->n,
                                               m->history_len, e5m2_mask, margin, sinv_before);
   return check_launch("amax_history_update");

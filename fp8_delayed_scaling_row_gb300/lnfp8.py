@@ -28,7 +28,8 @@ FORMAT_E4M3, FORMAT_HYBRID, FORMAT_E5M2 = 0, 1, 2
 _FORMATS = {"e4m3": FORMAT_E4M3, "hybrid": FORMAT_HYBRID, "e5m2": FORMAT_E5M2}
 
 EXPORTED = [
-    "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_meta_init", "amax_history_update",
+    "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_launch_count",
+    "lnfp8_profile_enable", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
     "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd", "ln_mlp_fwd",
     "ln_mlp_bwd",
 ]
@@ -95,6 +96,11 @@ _lib.lnfp8_last_error.argtypes = []
 _c_sync = _sig("lnfp8_sync_status", [_P])
 _c_version = _sig("lnfp8_version", [])
 _c_selftest = _sig("lnfp8_selftest_timeout", [_I64, _P])
+_c_launch_count = _sig("lnfp8_launch_count", [], C.c_longlong)
+_c_prof_enable = _sig("lnfp8_profile_enable", [C.c_int])
+_c_prof_collect = _sig("lnfp8_profile_collect", [])
+_c_prof_get = _sig("lnfp8_profile_get", [C.c_int, C.POINTER(C.c_char_p), C.POINTER(C.c_double),
+                                         C.POINTER(C.c_longlong)])
 _c_meta_init = _sig("lnfp8_meta_init", [C.POINTER(CMeta), _P])
 _c_update = _sig("amax_history_update", [C.POINTER(CMeta), C.POINTER(CRecipe), C.POINTER(C.c_int), _P, _P])
 _c_quant = _sig("fp8_quantize", [_P, C.c_int, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P])
@@ -132,6 +138,27 @@ def last_error() -> str:
 def lnfp8_selftest_timeout(limit_ns: int, stream=None) -> None:
     """Enqueue the bounded-wait diagnostic; the next sync_status() raises ERR_TIMEOUT."""
     _check(_c_selftest(int(limit_ns), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(_c_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    """Per-kernel CUDA-event timing on the launching stream (discards old records)."""
+    _check(_c_prof_enable(int(on)))
+
+
+def profile_collect() -> dict:
+    """{kernel kind: (total_ms, launches)} for everything recorded since profile_enable."""
+    n = _c_prof_collect()
+    out = {}
+    for i in range(n):
+        k, ms, cnt = C.c_char_p(), C.c_double(), C.c_longlong()
+        _check(_c_prof_get(i, C.byref(k), C.byref(ms), C.byref(cnt)))
+        out[k.value.decode()] = (ms.value, cnt.value)
+    return out
 
 
 def sync_status(stream=None) -> None:

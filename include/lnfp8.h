@@ -112,6 +112,25 @@ int lnfp8_version(void);
  * The pipeline waits of the GEMM use the same bounded wait (limit 1 s). */
 lnfp8_status lnfp8_selftest_timeout(int64_t limit_ns, lnfp8_stream stream);
 
+/* Launch accounting and per-kernel timing ------------------------------- */
+
+/* Number of kernels this library has launched in this process. */
+long long lnfp8_launch_count(void);
+
+/* Switches per-kernel timing on (1) or off (0) and discards earlier records.
+ * While on, every kernel launch is bracketed by two CUDA events recorded on
+ * the launch's own stream (host-side cost only; no device memory). */
+lnfp8_status lnfp8_profile_enable(int on);
+
+/* Waits for the recorded events, aggregates them by kernel kind and returns
+ * the number of kinds; the records are consumed. */
+int lnfp8_profile_collect(void);
+
+/* Kind i (0 <= i < the count lnfp8_profile_collect returned): its name (owned
+ * by the library, valid until the next collect), total milliseconds and
+ * number of launches. */
+lnfp8_status lnfp8_profile_get(int i, const char** kind, double* total_ms, long long* launches);
+
 /* Delayed-scaling state -------------------------------------------------- */
 
 /* Initial state (TE tutorial code block 1 recipe; step 1 casts with scale 1):

@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:long\s+long|[a-z_0-9]+)\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)))
 
 
 def test_header_declares_the_hot_path_calls():
