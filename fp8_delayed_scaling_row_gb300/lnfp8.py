@@ -30,7 +30,8 @@ _FORMATS = {"e4m3": FORMAT_E4M3, "hybrid": FORMAT_HYBRID, "e5m2": FORMAT_E5M2}
 EXPORTED = [
     "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_launch_count",
     "lnfp8_profile_enable", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
-    "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd", "ln_mlp_fwd",
+    "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
+    "ln_linear_bwd_noalloc", "ln_mlp_fwd",
     "ln_mlp_bwd",
 ]
 
@@ -109,6 +110,7 @@ _c_ln_bwd = _sig("ln_bwd", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P])
 _c_gemm = _sig("fp8_gemm", [_P, C.c_int, C.c_int, _P, C.c_int, C.c_int, _I64, _I64, _I64, _P, _P, _P, _P, _P])
 _c_lin_fwd = _sig("ln_linear_fwd", [C.POINTER(CLnLinearFwd), _P])
 _c_lin_bwd = _sig("ln_linear_bwd", [C.POINTER(CLnLinearBwd), _P])
+_c_lin_bwd_noalloc = _sig("ln_linear_bwd_noalloc", [C.POINTER(CLnLinearBwd), _P])
 _c_mlp_fwd = _sig("ln_mlp_fwd", [C.POINTER(CLnMlpFwd), _P])
 _c_mlp_bwd = _sig("ln_mlp_bwd", [C.POINTER(CLnMlpBwd), _P])
 
@@ -337,6 +339,21 @@ def ln_linear_bwd(dy, x, gamma, ctx: LinearCtx, meta: ScalingMeta, recipe: Recip
                      defer_update=int(defer_update))
     _check(_c_lin_bwd(C.byref(a), _stream(stream)))
     return g
+
+
+def ln_linear_bwd_noalloc(dy, x, gamma, ctx: LinearCtx, meta: ScalingMeta, recipe: Recipe, *, dx, dw, dbias=None,
+                          dgamma=None, dbeta=None, defer_update=False, stream=None) -> None:
+    """LayerNormLinear backward for callers that cannot allocate device memory:
+    the caller passes inputs and outputs only; the library's built-in scratch
+    array holds the dY codes and the LayerNorm-output gradient (see the C
+    header for its size limit and sharing rules)."""
+    M, N = dy.shape
+    K = x.shape[1]
+    a = CLnLinearBwd(M=M, K=K, N=N, dy=_ptr(dy), x=_ptr(x), gamma=_ptr(gamma), xq=_ptr(ctx.xq), wq=_ptr(ctx.wq),
+                     mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma), sinv_saved=_ptr(ctx.sinv_saved), dx=_ptr(dx),
+                     dw=_ptr(dw), dbias=_ptr(dbias), dgamma=_ptr(dgamma), dbeta=_ptr(dbeta), dyq=None, dln=None,
+                     meta=meta.c(), recipe=recipe.c(), defer_update=int(defer_update))
+    _check(_c_lin_bwd_noalloc(C.byref(a), _stream(stream)))
 
 
 @dataclass

@@ -257,6 +257,27 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* args, lnfp8_stream st
  * (dx = dln without LayerNorm); then the backward state update. */
 lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* args, lnfp8_stream stream);
 
+/* LayerNormLinear backward without caller-provided scratch. The pages have no
+ * counterpart of this entry point. It is for callers that cannot allocate
+ * device memory (they may not call cudaMalloc, for example a plug-in that a
+ * host framework hands only the tensors of one layer, or a runtime whose
+ * device memory is fixed before start-up). It takes the same arguments as
+ * ln_linear_bwd; args->dyq and args->dln are ignored. Those two scratch
+ * buffers live instead in one fixed device array inside the library, 16 MiB
+ * (the dY codes, M*N bytes rounded up to 256, then the bf16 LayerNorm-output
+ * gradient, 2*M*K bytes, when gamma is given); every GPU that loads the
+ * library holds that array until the process exits. Sizes beyond it return
+ * LNFP8_ERR_UNSUPPORTED_SHAPE before anything is enqueued. It allocates
+ * nothing and runs the same kernels as ln_linear_bwd.
+ *   - The first call on each device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero (both buffers are fully written
+ *     before they are read). Calls whose work overlaps on the GPU (other
+ *     streams, or other host threads) race on it: serialise them. */
+lnfp8_status ln_linear_bwd_noalloc(const lnfp8_ln_linear_bwd_args* args, lnfp8_stream stream);
+
 /* LayerNormMLP ----------------------------------------------------------- */
 
 typedef struct {
