@@ -226,14 +226,47 @@ class MlpRun:
             self.dys_host.append(synth.grad(m, d, seed=seed, step=i))
         self.xs = [bf(x) for x in self.xs_host]
         self.dys = [bf(x) for x in self.dys_host]
+        self.graphs = None
 
     def step(self, i, x=None, dy=None):
+        """One fwd+bwd through the C ABI; replays the captured CUDA graph of this
+        input batch when graphs are on (same kernels, no per-launch host cost)."""
+        if x is None and self.graphs is not None:
+            self.graphs[i % len(self.graphs)].replay()
+            return
+        self._call(self.xs[i % len(self.xs)] if x is None else x, self.dys[i % len(self.dys)] if dy is None else dy)
+
+    def _call(self, x, dy):
         L, p = self.L, self.p
-        x = self.xs[i % len(self.xs)] if x is None else x
-        dy = self.dys[i % len(self.dys)] if dy is None else dy
         L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], self.fm, self.rec, y=self.y,
                      ctx=self.ctx)
         L.ln_mlp_bwd(dy, x, p["gamma"], self.ctx, self.bm, self.rec, grads=self.grads)
+
+    def capture(self):
+        """Capture one CUDA graph per input batch (the state buffers are shared, so
+        replays advance the delayed-scaling state exactly like direct calls)."""
+        torch = self.torch
+        self.graphs = None
+        sd_f, sd_b = self.fm.state_dict(), self.bm.state_dict()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graphs = []
+        with torch.cuda.stream(s):
+            for i in range(len(self.xs)):  # warm the stream once before capture
+                c0 = self.L.launch_count()
+                self._call(self.xs[i], self.dys[i])
+                self.launches_per_step = self.L.launch_count() - c0
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for i in range(len(self.xs)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._call(self.xs[i], self.dys[i])
+            graphs.append(g)
+        torch.cuda.synchronize()
+        self.fm.load_state_dict(sd_f)
+        self.bm.load_state_dict(sd_b)
+        self.graphs = graphs
 
 
 def timed_steps(torch, run, steps, warmup, flush, barrier):
@@ -254,7 +287,10 @@ def timed_steps(torch, run, steps, warmup, flush, barrier):
     n1 = run.L.launch_count()
     torch.cuda.synchronize()
     barrier()
-    return sum(a.elapsed_time(b) for a, b in ev), n1 - n0
+    launches = n1 - n0
+    if run.graphs is not None:
+        launches = run.launches_per_step * steps  # replays launch the captured kernels
+    return sum(a.elapsed_time(b) for a, b in ev), launches
 
 
 def run_gpu(args):
@@ -285,6 +321,8 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     n_sets = min(args.steps + args.warmup, 8)
     run = MlpRun(L, torch, dev, M_TOK, D_MODEL, FFN, FMT, HIST, "outliers", n_sets, seed=1234 + 7919 * rank)
+    if args.graph:
+        run.capture()
 
     # ---- main timed region (device time, CUDA events, L2 flushed between steps)
     clocks = ClockSampler(local)
@@ -299,9 +337,9 @@ def run_gpu(args):
     # ---- per-kernel times inside the same workload (events on the launching stream)
     L.profile_enable(True)
     prof_steps = min(args.steps, 50)
-    for i in range(prof_steps):
+    for i in range(prof_steps):  # direct calls: the library brackets each of its launches with events
         flush.zero_()
-        run.step(i)
+        run._call(run.xs[i % len(run.xs)], run.dys[i % len(run.dys)])
     prof = L.profile_collect()
     L.profile_enable(False)
     gemm_kinds = {k: v for k, v in prof.items() if k.startswith("gemm")}
@@ -371,6 +409,8 @@ def run_gpu(args):
         del run
         torch.cuda.empty_cache()
         run2 = MlpRun(L, torch, dev, m2, d2, f2, FMT, HIST, "normal", 4, seed=4321 + rank)
+        if args.graph:
+            run2.capture()
         k2 = max(3, min(args.steps, 100))
         ms2 = max_over_ranks(timed_steps(torch, run2, k2, 3, flush, barrier)[0])
         d2048 = {"value": flops_per_step(m2, d2, f2) * k2 * world / (ms2 / 1e3) / 1e12, "unit": "TFLOP/s",
@@ -392,7 +432,7 @@ def run_gpu(args):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)", "data": "synthetic",
-                "config": workload(), "frac_of_fp8_peak": value / world / fp8_peak,
+                "config": dict(workload(), cuda_graph=bool(args.graph)), "frac_of_fp8_peak": value / world / fp8_peak,
                 "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline,
                 "per_kernel": per_kernel, "hbm_peak_gbs": hbm, "cpu_baseline": cpu, "d2048": d2048}
         print(json.dumps(line), flush=True)
@@ -411,6 +451,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-d2048", action="store_true")
+    ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph (1) or call (0)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -17,7 +17,7 @@ namespace lnfp8 {
 namespace {
 
 constexpr int kTC = 64;   // tile columns
-constexpr int kTR = 64;   // tile rows
+constexpr int kTR = 128;  // tile rows per iteration (8 x 16-byte loads in flight per thread)
 constexpr int kThreads = 256;
 
 template <typename T>
@@ -42,12 +42,15 @@ __device__ __forceinline__ void load8<float>(const float* p, float* v) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <typename T, int DT>
+template <typename T, int DT, int TR>
 __global__ void __launch_bounds__(kThreads)
 cast_kernel(const T* __restrict__ in, int64_t rows, int64_t cols, int64_t rows_per_cta,
             const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
             uint8_t* __restrict__ out_t, float* colsum) {
-  __shared__ __align__(16) uint8_t tq[kTC][kTR + 16];
+  // TR rows x 64 columns per iteration; each thread owns one 8-column vector
+  // of TR/32 rows and issues all of their loads before converting any.
+  constexpr int RPT = TR / 32;
+  __shared__ __align__(16) uint8_t tq[kTC][TR + 16];
   __shared__ float red[32][kTC + 1];
   __shared__ uint32_t ared[kThreads / 32];
 
@@ -67,21 +70,30 @@ cast_kernel(const T* __restrict__ in, int64_t rows, int64_t cols, int64_t rows_p
 #pragma unroll
   for (int i = 0; i < 8; ++i) csum[i] = 0.f;
 
-  for (int64_t r0 = r_begin; r0 < r_end; r0 += kTR) {
+  for (int64_t r0 = r_begin; r0 < r_end; r0 += TR) {
+    float v[RPT][8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < RPT; ++h) {
+      const int64_t r = r0 + rr + 32 * h;
+      if (r < r_end && col_ok) {
+        load8<T>(in + r * cols + cc, v[h]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[h][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < RPT; ++h) {
       const int rl = rr + 32 * h;
       const int64_t r = r0 + rl;
       uint2 q = make_uint2(0, 0);
       if (r < r_end && col_ok) {
-        float v[8];
-        load8<T>(in + r * cols + cc, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          am = max(am, abs_bits(v[i]));
-          csum[i] += v[i];
+          am = max(am, abs_bits(v[h][i]));
+          csum[i] += v[h][i];
         }
-        q = cvt_fp8x8<DT>(v, s);
+        q = cvt_fp8x8<DT>(v[h], s);
         if (out) *reinterpret_cast<uint2*>(out + r * cols + cc) = q;
       }
       if (out_t) {
@@ -92,15 +104,18 @@ cast_kernel(const T* __restrict__ in, int64_t rows, int64_t cols, int64_t rows_p
     }
     if (out_t) {
       __syncthreads();
-      const int col = t >> 2, chunk = (t & 3) * 16;
-      const int64_t c = c0 + col;
-      if (c < cols) {
-        uint8_t* dst = out_t + c * rows + r0 + chunk;
-        const int64_t nvalid = min64(16, r_end - (r0 + chunk));
-        if (nvalid == 16 && t_vec) {
-          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tq[col][chunk]);
-        } else {
-          for (int i = 0; i < nvalid; ++i) dst[i] = tq[col][chunk + i];
+      // TR rows x 64 columns of codes leave as 16-byte runs along the rows
+      for (int idx = t; idx < kTC * (TR / 16); idx += kThreads) {
+        const int col = idx / (TR / 16), chunk = (idx % (TR / 16)) * 16;
+        const int64_t c = c0 + col;
+        if (c < cols) {
+          uint8_t* dst = out_t + c * rows + r0 + chunk;
+          const int64_t nvalid = min64(16, r_end - (r0 + chunk));
+          if (nvalid == 16 && t_vec) {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tq[col][chunk]);
+          } else {
+            for (int i = 0; i < nvalid; ++i) dst[i] = tq[col][chunk + i];
+          }
         }
       }
       __syncthreads();
@@ -130,7 +145,7 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
   if (rows == 0 || cols == 0) return LNFP8_OK;
   const int64_t strips = (cols + kTC - 1) / kTC;
   const int64_t row_tiles = (rows + kTR - 1) / kTR;
-  const int64_t want = 4LL * num_sms();
+  const int64_t want = 2LL * num_sms();
   int64_t ysplit = (want + strips - 1) / strips;
   ysplit = max64(1, min64(ysplit, row_tiles));
   const int64_t rows_per_cta = ((row_tiles + ysplit - 1) / ysplit) * kTR;
@@ -141,14 +156,14 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
   LaunchScope ls(colsum ? "cast_colsum" : "cast", st);
   if (in_fp32) {
     if (dtype == LNFP8_E4M3)
-      cast_kernel<float, LNFP8_E4M3><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+      cast_kernel<float, LNFP8_E4M3, kTR><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
     else
-      cast_kernel<float, LNFP8_E5M2><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+      cast_kernel<float, LNFP8_E5M2, kTR><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
   } else {
     if (dtype == LNFP8_E4M3)
-      cast_kernel<uint16_t, LNFP8_E4M3><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+      cast_kernel<uint16_t, LNFP8_E4M3, kTR><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
     else
-      cast_kernel<uint16_t, LNFP8_E5M2><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+      cast_kernel<uint16_t, LNFP8_E5M2, kTR><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
   }
   return check_launch("fp8_quantize");
 }

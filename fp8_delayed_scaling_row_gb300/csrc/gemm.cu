@@ -60,10 +60,17 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  // per epilogue warp: a 32 x 32 bf16 box (2 KB, 64-byte swizzle) and a
+  // 32 x 32 FP8 box (1 KB, 32-byte swizzle) staged for TMA stores / loads
+  static constexpr int EPI_OUT_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_Q_OFF = EPI_OUT_OFF + kEpiWarps * 2048;
+  static constexpr int CSUM_OFF = EPI_Q_OFF + kEpiWarps * 1024;
   static constexpr int CSUM_BYTES = 2 * 4 * BN * 4;  // [acc buffer][row quarter][BN] fp32
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + CSUM_BYTES;
+  static constexpr int BAR_OFF = CSUM_OFF + CSUM_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct KParams {
@@ -141,6 +148,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Row r of a 32 x 32 box staged for TMA with the 64-byte (bf16) or 32-byte
+// (FP8) swizzle: the 16-byte chunk index is XORed with address bits 7..8
+// (resp. bit 7) of the row's offset, as the tensor map's swizzle mode expects.
+__device__ __forceinline__ uint32_t sw64(int r, int j) { return (uint32_t)(r * 64 + ((j ^ ((r >> 1) & 3)) << 4)); }
+__device__ __forceinline__ uint32_t sw32(int r, int j) { return (uint32_t)(r * 32 + ((j ^ ((r >> 2) & 1)) << 4)); }
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -205,17 +229,19 @@ __device__ __forceinline__ float transpose_reduce32(float* v, int lane) {
 // ------------------------------------------------------------ the kernel
 template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmQ,
+            const __grid_constant__ CUtensorMap tmH, const KParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, csum[2 acc][2 halves]
-  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, csum[2 acc][2 halves], hload[kEpiWarps]
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9 + kEpiWarps);
   uint32_t* tmem_slot = misc;
   volatile uint32_t* abort_flag = misc + 1;
-  float* csred = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES + C::BAR_BYTES);  // [2][4][BN]
+  float* csred = reinterpret_cast<float*>(smem + C::CSUM_OFF);  // [2][4][BN]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -226,6 +252,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   auto csum_bar = [&](int a, int h) { return bar0 + 8u * (2 * STAGES + 5 + 2 * a + h); };
+  auto hload_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 9 + w); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -239,6 +266,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     mbar_init(drain_bar, 1);
     for (int a = 0; a < 2; ++a)
       for (int h = 0; h < 2; ++h) mbar_init(csum_bar(a, h), 4);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(hload_bar(w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -343,11 +371,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
-    const int half = (warp - 4) >> 2;      // column half of the tile
-    const int row_in_tile = quarter * 32 + lane;
+    const int ew = warp - 4;
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. (this warp's 32 rows)
+    const int half = ew >> 2;              // column half of the tile
+    const int r = lane;                    // row within the warp's 32 x 32 box
     constexpr int HALF_COLS = BN / 2;
     constexpr int CHUNKS = HALF_COLS / 32;
+    uint8_t* so = smem + C::EPI_OUT_OFF + ew * 2048;  // bf16 box: output (STORE, GELU) or H input (DGELU)
+    uint8_t* sq = smem + C::EPI_Q_OFF + ew * 1024;    // FP8 box: codes output (GELU, DGELU)
+    const uint32_t so_a = smem_u32(so), sq_a = smem_u32(sq);
+    const uint32_t hbar = hload_bar(ew);
+    uint32_t hphase = 0;
+    bool h_pending = false;
     const float s = __fmul_rn(*p.sinv_a, *p.sinv_b);
     float scale_q = 0.f;
     if constexpr (EPI != EPI_STORE) scale_q = *p.scale_q;
@@ -358,100 +393,115 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // partials of the tile; it releases the accumulator only after reading
     // them, which keeps the partial buffer of this parity from being reused early.
     const bool combiner = EPI == EPI_DGELU && p.colsum != nullptr && quarter == 0;
+    auto issue_h = [&](int tile, int ch) {
+      // prefetch the 32 x 32 block of H this warp needs for (tile, chunk)
+      const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(hbar, 2048);
+        tma_load_2d(so_a, &tmH, n_blk * BN + half * HALF_COLS + ch * 32, m_blk * BM + quarter * 32, hbar);
+      }
+      h_pending = true;
+    };
+    if constexpr (EPI == EPI_DGELU) {
+      if ((int)blockIdx.x < num_tiles) issue_h(blockIdx.x, 0);
+    }
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
-      const int64_t m = (int64_t)m_blk * BM + row_in_tile;
+      const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
       const bool row_ok = m < p.M;
+      bool aborted = false;
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
         const int col0 = half * HALF_COLS + ch * 32;
         const int64_t n0 = (int64_t)n_blk * BN + col0;
-        uint32_t r[32];
+        uint32_t rr[32];
         if (p.num_kb > 0) {
-          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + col0), r);
+          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + col0), rr);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
         if (ch == CHUNKS - 1 && !combiner) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
+        uint4 hin[4];
+        if constexpr (EPI == EPI_DGELU) {
+          if (!mbar_wait(hbar, hphase, abort_flag)) { aborted = true; break; }
+          hphase ^= 1;
+          h_pending = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) hin[j] = *reinterpret_cast<const uint4*>(so + sw64(r, j));
+          // the box is free again: prefetch the next one this warp will need
+          fence_async_smem();
+          __syncwarp();
+          if (ch + 1 < CHUNKS) issue_h(tile, ch + 1);
+          else if (tile + (int)gridDim.x < num_tiles) issue_h(tile + gridDim.x, 0);
+        }
         float v[32];
+        uint4 ob[4];  // bf16 output row chunk
+        uint2 oq[4];  // FP8 output row chunk
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int64_t n = n0 + g * 8;
           const bool ok = row_ok && n < p.N;
           float e[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) e[i] = __uint_as_float(r[g * 8 + i]);
-          if constexpr (EPI == EPI_STORE) {
-            if (ok) {
-              float b[8];
+          for (int i = 0; i < 8; ++i) e[i] = __uint_as_float(rr[g * 8 + i]);
+          float b[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) b[i] = 0.f;
-              if (p.bias) {
-                const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
-                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
+          for (int i = 0; i < 8; ++i) b[i] = 0.f;
+          if constexpr (EPI != EPI_DGELU) {
+            if (p.bias && n < p.N) {
+              const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
+              const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) { b[2 * i] = bf16_bits_to_f32(bw[i] & 0xFFFFu); b[2 * i + 1] = bf16_bits_to_f32(bw[i] >> 16); }
-              }
-              uint4 o;
-              o.x = pack_bf16x2(fmaf(e[0], s, b[0]), fmaf(e[1], s, b[1]));
-              o.y = pack_bf16x2(fmaf(e[2], s, b[2]), fmaf(e[3], s, b[3]));
-              o.z = pack_bf16x2(fmaf(e[4], s, b[4]), fmaf(e[5], s, b[5]));
-              o.w = pack_bf16x2(fmaf(e[6], s, b[6]), fmaf(e[7], s, b[7]));
-              *reinterpret_cast<uint4*>(p.out + m * p.N + n) = o;
+              for (int i = 0; i < 4; ++i) { b[2 * i] = bf16_bits_to_f32(bw[i] & 0xFFFFu); b[2 * i + 1] = bf16_bits_to_f32(bw[i] >> 16); }
             }
+          }
+          if constexpr (EPI == EPI_STORE) {
+            ob[g].x = pack_bf16x2(fmaf(e[0], s, b[0]), fmaf(e[1], s, b[1]));
+            ob[g].y = pack_bf16x2(fmaf(e[2], s, b[2]), fmaf(e[3], s, b[3]));
+            ob[g].z = pack_bf16x2(fmaf(e[4], s, b[4]), fmaf(e[5], s, b[5]));
+            ob[g].w = pack_bf16x2(fmaf(e[6], s, b[6]), fmaf(e[7], s, b[7]));
           } else if constexpr (EPI == EPI_GELU) {
+            uint32_t hw[4];
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              hw[i] = pack_bf16x2(fmaf(e[2 * i], s, b[2 * i]), fmaf(e[2 * i + 1], s, b[2 * i + 1]));
+              const float h0 = bf16_bits_to_f32(hw[i] & 0xFFFFu), h1 = bf16_bits_to_f32(hw[i] >> 16);
+              a[2 * i] = 0.5f * h0 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h0 * h0, h0, h0)));
+              a[2 * i + 1] = 0.5f * h1 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h1 * h1, h1, h1)));
+            }
             if (ok) {
-              float b[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) b[i] = 0.f;
-              if (p.bias) {
-                const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
-                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) { b[2 * i] = bf16_bits_to_f32(bw[i] & 0xFFFFu); b[2 * i + 1] = bf16_bits_to_f32(bw[i] >> 16); }
-              }
-              uint32_t hw[4];
-              float a[8];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                hw[i] = pack_bf16x2(fmaf(e[2 * i], s, b[2 * i]), fmaf(e[2 * i + 1], s, b[2 * i + 1]));
-                const float h0 = bf16_bits_to_f32(hw[i] & 0xFFFFu), h1 = bf16_bits_to_f32(hw[i] >> 16);
-                a[2 * i] = 0.5f * h0 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h0 * h0, h0, h0)));
-                a[2 * i + 1] = 0.5f * h1 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h1 * h1, h1, h1)));
-              }
 #pragma unroll
               for (int i = 0; i < 8; ++i) am = max(am, abs_bits(a[i]));
-              *reinterpret_cast<uint4*>(p.out + m * p.N + n) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              *reinterpret_cast<uint2*>(p.out_q + m * p.N + n) = cvt_fp8x8<QDT>(a, scale_q);
               if (p.dbg) {
                 float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
                 d4[0] = make_float4(a[0], a[1], a[2], a[3]);
                 d4[1] = make_float4(a[4], a[5], a[6], a[7]);
               }
             }
+            ob[g] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            oq[g] = cvt_fp8x8<QDT>(a, scale_q);
           } else {  // EPI_DGELU
+            const uint32_t hw[4] = {hin[g].x, hin[g].y, hin[g].z, hin[g].w};
             float dh[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dh[i] = 0.f;
+            for (int i = 0; i < 8; ++i) {
+              const float h = bf16_bits_to_f32(i & 1 ? hw[i >> 1] >> 16 : hw[i >> 1] & 0xFFFFu);
+              const float t = tanh_fast(kGeluK * fmaf(kGeluC * h * h, h, h));
+              const float gp = fmaf(0.5f * h * (1.0f - t * t), kGeluK * fmaf(3.0f * kGeluC, h * h, 1.0f), 0.5f * (1.0f + t));
+              dh[i] = __fmul_rn(e[i], s) * gp;
+            }
+            oq[g] = cvt_fp8x8<QDT>(dh, scale_q);
             if (ok) {
-              const uint4 hu = *reinterpret_cast<const uint4*>(p.h_in + m * p.N + n);
-              const uint32_t hw[4] = {hu.x, hu.y, hu.z, hu.w};
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float h = bf16_bits_to_f32(i & 1 ? hw[i >> 1] >> 16 : hw[i >> 1] & 0xFFFFu);
-                const float t = tanh_fast(kGeluK * fmaf(kGeluC * h * h, h, h));
-                const float gp = fmaf(0.5f * h * (1.0f - t * t), kGeluK * fmaf(3.0f * kGeluC, h * h, 1.0f), 0.5f * (1.0f + t));
-                dh[i] = __fmul_rn(e[i], s) * gp;
-                am = max(am, abs_bits(dh[i]));
-              }
-              *reinterpret_cast<uint2*>(p.out_q + m * p.N + n) = cvt_fp8x8<QDT>(dh, scale_q);
+              for (int i = 0; i < 8; ++i) am = max(am, abs_bits(dh[i]));
               if (p.dbg) {
                 float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
                 d4[0] = make_float4(dh[0], dh[1], dh[2], dh[3]);
@@ -459,13 +509,34 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               }
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[g * 8 + i] = dh[i];
+            for (int i = 0; i < 8; ++i) v[g * 8 + i] = ok ? dh[i] : 0.f;
           }
+        }
+        // stage the 32 x 32 results in swizzled shared memory, then one TMA
+        // store per box (rows past M and columns past N are clipped by TMA)
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        if constexpr (EPI != EPI_DGELU) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(so + sw64(r, j)) = ob[j];
+        }
+        if constexpr (EPI != EPI_STORE) {
+          *reinterpret_cast<uint4*>(sq + sw32(r, 0)) = make_uint4(oq[0].x, oq[0].y, oq[1].x, oq[1].y);
+          *reinterpret_cast<uint4*>(sq + sw32(r, 1)) = make_uint4(oq[2].x, oq[2].y, oq[3].x, oq[3].y);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int y = m_blk * BM + quarter * 32;
+          if constexpr (EPI != EPI_DGELU) tma_store_2d(&tmO, so_a, (int)n0, y);
+          if constexpr (EPI != EPI_STORE) tma_store_2d(&tmQ, sq_a, (int)n0, y);
+          bulk_commit();
         }
         if constexpr (EPI == EPI_DGELU) {
           if (p.colsum) csred[(acc * 4 + quarter) * BN + col0 + lane] = transpose_reduce32(v, lane);
         }
       }
+      if (aborted) break;
       if constexpr (EPI == EPI_DGELU) {
         if (p.colsum) {
           __syncwarp();
@@ -487,6 +558,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    if constexpr (EPI == EPI_DGELU) {
+      if (h_pending) {  // an abort left a prefetch in flight: let it land first
+        uint32_t dummy_flag = 0;
+        if (lane == 0) mbar_wait(hbar, hphase, &dummy_flag, 100000000ull);
+        __syncwarp();
+      }
+    }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
     if constexpr (EPI != EPI_STORE) {
       am = warp_max_u32(am);
       if (lane == 0 && am != 0u) atomic_max_amax(p.amax_q, am);
@@ -529,19 +609,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D uint8 tensor map: inner extent `inner` (contiguous), `outer` rows, box
-// {128, box_outer}, 128-byte swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, int box_outer) {
+// 2-D tensor map over a row-major [outer, inner] tensor of 1- or 2-byte
+// elements: box {box_inner, box_outer}, the given swizzle, zero fill outside.
+bool make_map(CUtensorMap* tm, const void* base, int elem_bytes, int64_t inner, int64_t outer, int box_inner,
+              int box_outer, CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)inner};
-  cuuint32_t box[2] = {128u, (cuuint32_t)box_outer};
+  cuuint64_t strides[1] = {(cuuint64_t)(inner * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
   cuuint32_t estr[2] = {1u, 1u};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// FP8 operand tile: 128-byte rows, 128-byte swizzle.
+bool make_operand_map(CUtensorMap* tm, const void* base, int64_t inner, int64_t outer, int box_outer) {
+  return make_map(tm, base, 1, inner, outer, 128, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+struct EpiMaps {
+  CUtensorMap o, q, h;
+};
 
 uint32_t make_idesc(int n_mma, int a_dt, int b_dt, bool a_mn, bool b_mn) {
   return (1u << 4) |                       // accumulator fp32
@@ -554,7 +644,8 @@ uint32_t make_idesc(int n_mma, int a_dt, int b_dt, bool a_mn, bool b_mn) {
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
-lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, cudaStream_t st) {
+lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em, const KParams& kp,
+                      cudaStream_t st) {
   auto k = gemm_kernel<BN, A_MN, B_MN, EPI, QDT>;
   static bool attr = false;
   if (!attr) {
@@ -567,17 +658,17 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const KParam
   static const char* kind = EPI == EPI_GELU ? "gemm_gelu" : EPI == EPI_DGELU ? "gemm_dgelu" :
                             (A_MN ? (B_MN ? "gemm_mn_mn" : "gemm_mn_k") : (B_MN ? "gemm_k_mn" : "gemm_k_k"));
   LaunchScope ls(kind, st);
-  k<<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, kp);
+  k<<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, em.o, em.q, em.h, kp);
   return check_launch("fp8 gemm");
 }
 
 template <int BN, int EPI, int QDT>
-lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp,
-                            cudaStream_t st) {
-  if (!a_mn && !b_mn) return launch_t<BN, false, false, EPI, QDT>(ta, tb, kp, st);
-  if (!a_mn && b_mn) return launch_t<BN, false, true, EPI, QDT>(ta, tb, kp, st);
-  if (a_mn && b_mn) return launch_t<BN, true, true, EPI, QDT>(ta, tb, kp, st);
-  return launch_t<BN, true, false, EPI, QDT>(ta, tb, kp, st);
+lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
+                            const KParams& kp, cudaStream_t st) {
+  if (!a_mn && !b_mn) return launch_t<BN, false, false, EPI, QDT>(ta, tb, em, kp, st);
+  if (!a_mn && b_mn) return launch_t<BN, false, true, EPI, QDT>(ta, tb, em, kp, st);
+  if (a_mn && b_mn) return launch_t<BN, true, true, EPI, QDT>(ta, tb, em, kp, st);
+  return launch_t<BN, true, false, EPI, QDT>(ta, tb, em, kp, st);
 }
 
 }  // namespace
@@ -602,8 +693,14 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
 
   CUtensorMap ta, tb;
   const int64_t K = g.K > 0 ? g.K : 1;  // a zero-K product never loads; keep the map valid
-  bool ok = a_mn ? make_map(&ta, g.a, g.M, K, BK) : make_map(&ta, g.a, K, g.M, BM);
-  ok = ok && (b_mn ? make_map(&tb, g.b, g.N, K, BK) : make_map(&tb, g.b, K, g.N, bn));
+  bool ok = a_mn ? make_operand_map(&ta, g.a, g.M, K, BK) : make_operand_map(&ta, g.a, K, g.M, BM);
+  ok = ok && (b_mn ? make_operand_map(&tb, g.b, g.N, K, BK) : make_operand_map(&tb, g.b, K, g.N, bn));
+  // epilogue boxes: 32 x 32 per warp; unused maps are copies of a valid one
+  EpiMaps em;
+  em.o = em.q = em.h = ta;
+  if (ok && g.epi != EPI_DGELU) ok = make_map(&em.o, g.out, 2, g.N, g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (ok && g.epi != EPI_STORE) ok = make_map(&em.q, g.out_q, 1, g.N, g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+  if (ok && g.epi == EPI_DGELU) ok = make_map(&em.h, g.h_in, 2, g.N, g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return set_error(LNFP8_ERR_CUDA, "fp8 gemm: cuTensorMapEncodeTiled failed (driver entry point or arguments)");
 
   KParams kp;
@@ -626,16 +723,16 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.dbg = g.dbg;
 
   if (g.epi == EPI_STORE) {
-    if (bn == 256) return launch_layouts<256, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, kp, st);
-    return launch_layouts<128, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, kp, st);
+    if (bn == 256) return launch_layouts<256, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, em, kp, st);
+    return launch_layouts<128, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, em, kp, st);
   }
   if (g.epi == EPI_GELU && !a_mn && !b_mn) {
-    if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, false, EPI_GELU, LNFP8_E4M3>(ta, tb, kp, st);
-    return launch_t<256, false, false, EPI_GELU, LNFP8_E5M2>(ta, tb, kp, st);
+    if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, false, EPI_GELU, LNFP8_E4M3>(ta, tb, em, kp, st);
+    return launch_t<256, false, false, EPI_GELU, LNFP8_E5M2>(ta, tb, em, kp, st);
   }
   if (g.epi == EPI_DGELU && !a_mn && b_mn) {
-    if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, true, EPI_DGELU, LNFP8_E4M3>(ta, tb, kp, st);
-    return launch_t<256, false, true, EPI_DGELU, LNFP8_E5M2>(ta, tb, kp, st);
+    if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, true, EPI_DGELU, LNFP8_E4M3>(ta, tb, em, kp, st);
+    return launch_t<256, false, true, EPI_DGELU, LNFP8_E5M2>(ta, tb, em, kp, st);
   }
   return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: epilogue %d with layouts (%d, %d) is not built", g.epi,
                    g.a_layout, g.b_layout);

@@ -58,23 +58,41 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
               float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg) {
   __shared__ float xch[kThreads / 32];
   __shared__ uint32_t ared[kThreads / 32];
+  extern __shared__ uint4 sgb[];  // gamma then beta, D/8 16-byte vectors each
   constexpr int GPB = kThreads / TPR;  // row groups per block
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
+  const int nvec = D >> 3;
+  for (int i = threadIdx.x; i < nvec; i += kThreads) {
+    sgb[i] = reinterpret_cast<const uint4*>(gamma)[i];
+    sgb[nvec + i] = reinterpret_cast<const uint4*>(beta)[i];
+  }
+  __syncthreads();
   const float s = *scale_p;
   const float inv_d = 1.0f / (float)D;
+  const int64_t stride = (int64_t)gridDim.x * GPB;
   uint32_t am = 0;
 
-  for (int64_t row = (int64_t)blockIdx.x * GPB + g; row - g < M; row += (int64_t)gridDim.x * GPB) {
-    // every thread of the block runs the same trip count (group_sum has barriers)
-    const bool active = row < M;
-    uint4 raw[NV];
-    float sum = 0.f;
+  auto load_row = [&](int64_t row, uint4* raw) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int c = (gt + TPR * j) * 8;
       raw[j] = make_uint4(0, 0, 0, 0);
-      if (active && c < D) raw[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
+      if (row < M && c < D) raw[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
+    }
+  };
+
+  int64_t row = (int64_t)blockIdx.x * GPB + g;
+  uint4 raw[NV];
+  load_row(row, raw);
+  // every thread of the block runs the same trip count (group_sum may use barriers)
+  for (; row - g < M; row += stride) {
+    uint4 nxt[NV];
+    load_row(row + stride, nxt);  // the next row's loads are in flight during this row's math
+    const bool active = row < M;
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
       float v[8];
       unpack8(raw[j], v);
 #pragma unroll
@@ -97,67 +115,69 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
     }
     const float var = group_sum<TPR>(sq, xch) * inv_d;
     const float rs = 1.0f / sqrtf(var + eps);
-    if (!active) continue;
+    if (active) {
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int c = (gt + TPR * j) * 8;
-      if (c >= D) continue;
-      float v[8], gm[8], bt[8], y[8];
-      unpack8(raw[j], v);
-      unpack8(*reinterpret_cast<const uint4*>(gamma + c), gm);
-      unpack8(*reinterpret_cast<const uint4*>(beta + c), bt);
+      for (int j = 0; j < NV; ++j) {
+        const int cv = gt + TPR * j;
+        const int c = cv * 8;
+        if (c >= D) continue;
+        float v[8], gm[8], bt[8], y[8];
+        unpack8(raw[j], v);
+        unpack8(sgb[cv], gm);
+        unpack8(sgb[nvec + cv], bt);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        y[i] = fmaf((v[i] - mu) * rs, gm[i], bt[i]);
-        am = max(am, abs_bits(y[i]));
+        for (int i = 0; i < 8; ++i) {
+          y[i] = fmaf((v[i] - mu) * rs, gm[i], bt[i]);
+          am = max(am, abs_bits(y[i]));
+        }
+        *reinterpret_cast<uint2*>(out + row * D + c) = cvt_fp8x8<DT>(y, s);
+        if (ydbg) {
+          float4* d4 = reinterpret_cast<float4*>(ydbg + row * D + c);
+          d4[0] = make_float4(y[0], y[1], y[2], y[3]);
+          d4[1] = make_float4(y[4], y[5], y[6], y[7]);
+        }
       }
-      *reinterpret_cast<uint2*>(out + row * D + c) = cvt_fp8x8<DT>(y, s);
-      if (ydbg) {
-        float4* d4 = reinterpret_cast<float4*>(ydbg + row * D + c);
-        d4[0] = make_float4(y[0], y[1], y[2], y[3]);
-        d4[1] = make_float4(y[4], y[5], y[6], y[7]);
+      if (gt == 0) {
+        mu_out[row] = mu;
+        rs_out[row] = rs;
       }
     }
-    if (gt == 0) {
-      mu_out[row] = mu;
-      rs_out[row] = rs;
-    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) raw[j] = nxt[j];
   }
   block_amax_commit(am, ared, amax_cur);
 }
 
 template <int TPR, int NV>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
               const uint16_t* __restrict__ gamma, const float* __restrict__ mu_in,
               const float* __restrict__ rs_in, int64_t M, int D, uint16_t* __restrict__ dx,
               float* dgamma, float* dbeta) {
   __shared__ float xch[kThreads / 32];
-  extern __shared__ float colred[];  // [2][D] block partials of dgamma, dbeta
+  extern __shared__ float colred[];  // [2][D] block partials of dgamma, dbeta, then gamma [D/8 uint4]
+  uint4* sg = reinterpret_cast<uint4*>(colred + 2 * D);
   constexpr int GPB = kThreads / TPR;
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
   const float inv_d = 1.0f / (float)D;
+  const int nvec = D >> 3;
 
   for (int c = threadIdx.x; c < 2 * D; c += kThreads) colred[c] = 0.f;
+  for (int i = threadIdx.x; i < nvec; i += kThreads) sg[i] = reinterpret_cast<const uint4*>(gamma)[i];
+  __syncthreads();
 
-  float accg[NV][8], accb[NV][8], gm[NV][8];
+  float accg[NV][8], accb[NV][8];
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int c = (gt + TPR * j) * 8;
-    uint4 graw = make_uint4(0, 0, 0, 0);
-    if (c < D) graw = *reinterpret_cast<const uint4*>(gamma + c);
-    unpack8(graw, gm[j]);
+  for (int j = 0; j < NV; ++j)
 #pragma unroll
     for (int i = 0; i < 8; ++i) accg[j][i] = accb[j][i] = 0.f;
-  }
 
   for (int64_t row = (int64_t)blockIdx.x * GPB + g; row - g < M; row += (int64_t)gridDim.x * GPB) {
     const bool active = row < M;
     const float mu = active ? mu_in[row] : 0.f;
     const float rs = active ? rs_in[row] : 0.f;
     uint4 rx[NV], rd[NV];
-    float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int c = (gt + TPR * j) * 8;
@@ -166,13 +186,19 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
         rx[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
         rd[j] = *reinterpret_cast<const uint4*>(dy + row * D + c);
       }
-      float xv[8], dv[8];
+    }
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int cv = gt + TPR * j;
+      float xv[8], dv[8], gm[8];
       unpack8(rx[j], xv);
       unpack8(rd[j], dv);
+      unpack8(cv < nvec ? sg[cv] : make_uint4(0, 0, 0, 0), gm);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float xh = (xv[i] - mu) * rs;
-        const float gg = dv[i] * gm[j][i];
+        const float gg = dv[i] * gm[i];
         s1 += gg;
         s2 += gg * xh;
         accg[j][i] = fmaf(dv[i], xh, accg[j][i]);
@@ -184,27 +210,28 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     if (!active) continue;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int c = (gt + TPR * j) * 8;
+      const int cv = gt + TPR * j;
+      const int c = cv * 8;
       if (c >= D) continue;
-      float xv[8], dv[8], o[8];
+      float xv[8], dv[8], gm[8], o[8];
       unpack8(rx[j], xv);
       unpack8(rd[j], dv);
+      unpack8(sg[cv], gm);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float xh = (xv[i] - mu) * rs;
-        o[i] = rs * (dv[i] * gm[j][i] - mean_g - xh * mean_gx);
+        o[i] = rs * (dv[i] * gm[i] - mean_g - xh * mean_gx);
       }
-      uint4 p;
-      p.x = pack_bf16x2(o[0], o[1]);
-      p.y = pack_bf16x2(o[2], o[3]);
-      p.z = pack_bf16x2(o[4], o[5]);
-      p.w = pack_bf16x2(o[6], o[7]);
-      *reinterpret_cast<uint4*>(dx + row * D + c) = p;
+      uint4 pk;
+      pk.x = pack_bf16x2(o[0], o[1]);
+      pk.y = pack_bf16x2(o[2], o[3]);
+      pk.z = pack_bf16x2(o[4], o[5]);
+      pk.w = pack_bf16x2(o[6], o[7]);
+      *reinterpret_cast<uint4*>(dx + row * D + c) = pk;
     }
   }
 
   // block reduction of the column partials, then one atomic per column per block
-  __syncthreads();
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     const int c = (gt + TPR * j) * 8;
@@ -224,30 +251,49 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
 
 // Threads per row and 16-byte vectors per thread for a row of D bf16.
 struct RowShape { int tpr, nv; };
-RowShape row_shape(int64_t D) {
+RowShape row_shape(int64_t D, int max_nv) {
   const int64_t vecs = (D + 7) / 8;
   for (int tpr = 32; tpr <= 256; tpr *= 2) {
     const int64_t nv = (vecs + tpr - 1) / tpr;
-    if (nv <= 4) return {tpr, (int)nv};
+    if (nv <= max_nv || tpr == 256) return nv <= 4 ? RowShape{tpr, (int)nv} : RowShape{0, 0};
   }
   return {0, 0};
 }
 
+// Resident blocks per SM for a kernel at kThreads threads and `smem` bytes.
+template <typename K>
+int64_t resident_blocks(K kernel, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem) != cudaSuccess || n < 1) n = 1;
+  return (int64_t)n * num_sms();
+}
+
 template <int DT>
-lnfp8_status ln_fwd_dispatch(RowShape rsh, dim3 grid, cudaStream_t st, const uint16_t* x,
+lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
                              const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int D,
                              const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
                              float* ydbg) {
-#define LNF(TPR, NV) ln_fwd_kernel<TPR, NV, DT><<<grid, kThreads, 0, st>>>(x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg)
+  const size_t smem = (size_t)D * 2 * sizeof(uint16_t);
+  const int64_t gpb = kThreads / rsh.tpr;
+#define LNF(TPR, NV)                                                                                    \
+  do {                                                                                                  \
+    auto k = ln_fwd_kernel<TPR, NV, DT>;                                                                \
+    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                        \
+    k<<<(unsigned)blocks, kThreads, smem, st>>>(x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg); \
+  } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
     case 321: LNF(32, 1); break;
     case 322: LNF(32, 2); break;
     case 323: LNF(32, 3); break;
     case 324: LNF(32, 4); break;
+    case 642: LNF(64, 2); break;
     case 643: LNF(64, 3); break;
     case 644: LNF(64, 4); break;
+    case 1282: LNF(128, 2); break;
     case 1283: LNF(128, 3); break;
     case 1284: LNF(128, 4); break;
+    case 2562: LNF(256, 2); break;
     case 2563: LNF(256, 3); break;
     case 2564: LNF(256, 4); break;
     default: return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: unsupported D");
@@ -262,15 +308,12 @@ lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint1
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st) {
   if (M == 0) return LNFP8_OK;
-  const RowShape rsh = row_shape(D);
+  const RowShape rsh = row_shape(D, 4);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: D = %lld > 8192", (long long)D);
-  const int64_t gpb = kThreads / rsh.tpr;
-  const int64_t blocks = min64((M + gpb - 1) / gpb, 8LL * num_sms());
-  dim3 grid((unsigned)blocks);
   LaunchScope ls("ln_fwd_cast", st);
   if (dtype == LNFP8_E4M3)
-    return ln_fwd_dispatch<LNFP8_E4M3>(rsh, grid, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
-  return ln_fwd_dispatch<LNFP8_E5M2>(rsh, grid, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
+    return ln_fwd_dispatch<LNFP8_E4M3>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
+  return ln_fwd_dispatch<LNFP8_E5M2>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
 }
 
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
@@ -282,28 +325,30 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
       return check_launch("ln_bwd: clearing dgamma/dbeta");
   }
   if (M == 0) return LNFP8_OK;
-  const RowShape rsh = row_shape(D);
+  const RowShape rsh = row_shape(D, 3);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: D = %lld > 8192", (long long)D);
   const int64_t gpb = kThreads / rsh.tpr;
-  const int64_t blocks = min64((M + gpb - 1) / gpb, 2LL * num_sms());
-  const size_t smem = 2 * D * sizeof(float);
-  dim3 grid((unsigned)blocks);
+  const size_t smem = 2 * D * sizeof(float) + D * sizeof(uint16_t);
   LaunchScope ls("ln_bwd", st);
 #define LNB(TPR, NV)                                                                                   \
   do {                                                                                                 \
     auto k = ln_bwd_kernel<TPR, NV>;                                                                   \
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-    k<<<grid, kThreads, smem, st>>>(dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta);          \
+    const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                       \
+    k<<<(unsigned)blocks, kThreads, smem, st>>>(dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta); \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
     case 321: LNB(32, 1); break;
     case 322: LNB(32, 2); break;
     case 323: LNB(32, 3); break;
     case 324: LNB(32, 4); break;
+    case 642: LNB(64, 2); break;
     case 643: LNB(64, 3); break;
     case 644: LNB(64, 4); break;
+    case 1282: LNB(128, 2); break;
     case 1283: LNB(128, 3); break;
     case 1284: LNB(128, 4); break;
+    case 2562: LNB(256, 2); break;
     case 2563: LNB(256, 3); break;
     case 2564: LNB(256, 4); break;
     default: return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: unsupported D");
