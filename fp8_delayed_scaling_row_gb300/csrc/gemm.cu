@@ -13,13 +13,15 @@
 //              dhq = fp8(dh * scale_dh); db1 += column sums     (FC2 dgrad)
 // so the GELU output and the gradient dH are written only as FP8 codes.
 //
-// Kernel shape (persistent, one CTA per SM, 384 threads):
+// Kernel shape (persistent, one CTA per SM, 640 threads):
 //   warp 0      TMA producer (one elected thread), STAGES-deep smem ring
 //   warp 1      MMA issuer (one thread): 128 x BN x 32 tcgen05.mma per K step
 //   warp 2      tensor-memory allocator (2 x BN fp32 columns: double-buffered
 //               accumulator so the epilogue of tile i overlaps the MMAs of i+1)
-//   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and
-//               one half of the tile's columns with tcgen05.ld
+//   warps 4-19  epilogue, two groups of 8: group g drains accumulator buffer g
+//               (every other tile), so two tiles' epilogues run at once; warp
+//               w reads TMEM lanes 32*(w%4).. (its 32 rows) and one half of
+//               the tile's columns with tcgen05.ld
 // Operands may be K-major ([rows, K]) or MN-major ([K, rows]); FP8 MN-major
 // operands are native to tcgen05, so the backward GEMMs read dY, A, dH and the
 // LN output in the layout the forward wrote them, with no transposed copies.
@@ -51,12 +53,15 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;  // bytes (= FP8 elements) of K per pipeline stage
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;  // two groups of 8, one per accumulator buffer
+// CTAs per cluster: a pair of CTAs works on two M tiles of the same N tile and
+// each loads half of the shared B tile, multicast to both.
+constexpr int CL = 2;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = BN == 256 ? 3 : 5;
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -67,7 +72,7 @@ struct Cfg {
   static constexpr int CSUM_OFF = EPI_Q_OFF + kEpiWarps * 1024;
   static constexpr int CSUM_BYTES = 2 * 4 * BN * 4;  // [acc buffer][row quarter][BN] fp32
   static constexpr int BAR_OFF = CSUM_OFF + CSUM_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -124,7 +129,7 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // Bounded wait: gives up after ~limit_ns or when another role has aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        uint64_t limit_ns = 1000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -146,6 +151,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// Multicast variant: the box lands at the same shared-memory offset, and
+// signals the same barrier offset, in every CTA of the cluster named by mask.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
@@ -188,6 +213,12 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// Arrive on the barrier at this offset in every CTA of the mask once the MMAs complete.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+               "h"(mask)
+               : "memory");
+}
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -209,6 +240,53 @@ __device__ __forceinline__ float tanh_fast(float x) {
 
 constexpr float kGeluK = 0.7978845608028654f;  // sqrt(2/pi)
 constexpr float kGeluC = 0.044715f;
+
+// Packed fp32 pairs (one 64-bit register pair) and the sm_100+ paired FMA /
+// MUL / SUB: two independent IEEE round-to-nearest results per instruction.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float lo(uint64_t r) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float hi(uint64_t r) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+  return b;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// bf16 pair (low, high halves of a 32-bit word) -> fp32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// running max of |x| in the fp32 magnitude order, NaN-propagating
+__device__ __forceinline__ float maxabs(float m, float x) {
+  float r;
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(x));
+  return r;
+}
+template <int DT>
+__device__ __forceinline__ uint16_t cvt_pair(uint64_t scaled) {
+  return cvt_fp8x2<DT>(lo(scaled), hi(scaled));
+}
 
 // Column sums of a 32 x 32 block held one row per lane: after the exchange,
 // lane c holds the sum over the 32 rows of column c (31 shuffles).
@@ -257,11 +335,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);  // released by the MMAs of both CTAs of the pair
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps);
+      mbar_init(tempty_bar(a), kEpiWarps / 2);  // the 8 warps of the group that drains buffer a
     }
     mbar_init(drain_bar, 1);
     for (int a = 0; a < 2; ++a)
@@ -270,6 +348,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // the peer multicasts into this CTA's ring and barriers: both must be initialised
+  cluster_sync();
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
@@ -285,7 +365,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_tiles = p.num_m * p.num_n;
+  // Work units: one N tile and CL consecutive M tiles, one per CTA of a cluster.
+  const int rank = CL == 2 ? (int)cluster_rank() : 0;
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  const int num_m2 = (p.num_m + CL - 1) / CL;
+  const int num_units = num_m2 * p.num_n;
+  auto unit_m = [&](int u) { return (u % num_m2) * CL + rank; };
+  auto unit_n = [&](int u) { return u / num_m2; };
+  constexpr uint16_t kPair = (1u << CL) - 1u;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -294,8 +381,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
+      for (int u = cid; u < num_units && ok; u += ncl) {
+        const int m_blk = unit_m(u), n_blk = unit_n(u);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
@@ -304,11 +391,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           const uint32_t b_dst = a_dst + C::A_BYTES;
           if (!A_MN) tma_load_2d(a_dst, &tmA, kb * BK, m_blk * BM, fb);
           else       tma_load_2d(a_dst, &tmA, m_blk * BM, kb * BK, fb);
+          // this CTA's half of the B tile, multicast to both CTAs of the pair
           if (!B_MN) {
-            tma_load_2d(b_dst, &tmB, kb * BK, n_blk * BN, fb);
+            tma_load_2d_mc(b_dst + rank * (BN / CL) * BK, &tmB, kb * BK, n_blk * BN + rank * (BN / CL), fb, kPair);
+          } else if (BN == 256) {
+            tma_load_2d_mc(b_dst + rank * 128 * BK, &tmB, n_blk * BN + rank * 128, kb * BK, fb, kPair);
           } else {
-#pragma unroll
-            for (int j = 0; j < BN / 128; ++j) tma_load_2d(b_dst + j * 128 * BK, &tmB, n_blk * BN + j * 128, kb * BK, fb);
+            tma_load_2d_mc(b_dst + rank * (BK / CL) * 128, &tmB, n_blk * BN, kb * BK + rank * (BK / CL), fb, kPair);
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -334,7 +423,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int u = cid; u < num_units && ok; u += ncl) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -355,7 +444,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 mma_f8(d_tmem + j * 128, ad, make_desc(b_base + j * 128 * BK + kk * 32 * 128, 1024, 1024), p.idesc, accum);
             }
           }
-          mma_commit(empty_bar(stage));
+          mma_commit_mc(empty_bar(stage), kPair);  // frees the stage in both CTAs
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -372,8 +461,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - 4;
+    const int grp = ew >> 3;               // accumulator buffer (and tile parity) this warp drains
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. (this warp's 32 rows)
-    const int half = ew >> 2;              // column half of the tile
+    const int half = (ew >> 2) & 1;        // column half of the tile
     const int r = lane;                    // row within the warp's 32 x 32 box
     constexpr int HALF_COLS = BN / 2;
     constexpr int CHUNKS = HALF_COLS / 32;
@@ -386,27 +476,28 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const float s = __fmul_rn(*p.sinv_a, *p.sinv_b);
     float scale_q = 0.f;
     if constexpr (EPI != EPI_STORE) scale_q = *p.scale_q;
-    uint32_t am = 0;
-    int acc = 0;
+    float am_f = 0.f;  // running max |x| of the cast values (GELU / dGELU epilogues)
+    const int acc = grp;
     uint32_t acc_phase = 0;
     // With column sums, warp quarter 0 of each half combines the four 32-row
     // partials of the tile; it releases the accumulator only after reading
     // them, which keeps the partial buffer of this parity from being reused early.
     const bool combiner = EPI == EPI_DGELU && p.colsum != nullptr && quarter == 0;
-    auto issue_h = [&](int tile, int ch) {
-      // prefetch the 32 x 32 block of H this warp needs for (tile, chunk)
-      const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
+    auto issue_h = [&](int u, int ch) {
+      // prefetch the 32 x 32 block of H this warp needs for (unit, chunk)
+      const int m_blk = unit_m(u), n_blk = unit_n(u);
       if (lane == 0) {
         mbar_arrive_expect_tx(hbar, 2048);
         tma_load_2d(so_a, &tmH, n_blk * BN + half * HALF_COLS + ch * 32, m_blk * BM + quarter * 32, hbar);
       }
       h_pending = true;
     };
+    const int u0 = cid + grp * ncl;  // this group's first unit; then every second one
     if constexpr (EPI == EPI_DGELU) {
-      if ((int)blockIdx.x < num_tiles) issue_h(blockIdx.x, 0);
+      if (u0 < num_units) issue_h(u0, 0);
     }
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile % p.num_m, n_blk = tile / p.num_m;
+    for (int u = u0; u < num_units; u += 2 * ncl) {
+      const int m_blk = unit_m(u), n_blk = unit_n(u);
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
@@ -438,78 +529,101 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           // the box is free again: prefetch the next one this warp will need
           fence_async_smem();
           __syncwarp();
-          if (ch + 1 < CHUNKS) issue_h(tile, ch + 1);
-          else if (tile + (int)gridDim.x < num_tiles) issue_h(tile + gridDim.x, 0);
+          if (ch + 1 < CHUNKS) issue_h(u, ch + 1);
+          else if (u + 2 * ncl < num_units) issue_h(u + 2 * ncl, 0);
         }
         float v[32];
         uint4 ob[4];  // bf16 output row chunk
         uint2 oq[4];  // FP8 output row chunk
+        const bool full = row_ok && n0 + 32 <= p.N;  // every element of this chunk is inside the tensor
+        const uint64_t s2 = f2(s, s);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int64_t n = n0 + g * 8;
           const bool ok = row_ok && n < p.N;
-          float e[8];
+          uint64_t e2[4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) e[i] = __uint_as_float(rr[g * 8 + i]);
-          float b[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) b[i] = 0.f;
+          for (int i = 0; i < 4; ++i) e2[i] = f2(__uint_as_float(rr[g * 8 + 2 * i]), __uint_as_float(rr[g * 8 + 2 * i + 1]));
+          uint64_t b2[4] = {0ull, 0ull, 0ull, 0ull};
           if constexpr (EPI != EPI_DGELU) {
             if (p.bias && n < p.N) {
               const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
-              const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) { b[2 * i] = bf16_bits_to_f32(bw[i] & 0xFFFFu); b[2 * i + 1] = bf16_bits_to_f32(bw[i] >> 16); }
+              b2[0] = bf2_to_f2(bu.x);
+              b2[1] = bf2_to_f2(bu.y);
+              b2[2] = bf2_to_f2(bu.z);
+              b2[3] = bf2_to_f2(bu.w);
             }
           }
           if constexpr (EPI == EPI_STORE) {
-            ob[g].x = pack_bf16x2(fmaf(e[0], s, b[0]), fmaf(e[1], s, b[1]));
-            ob[g].y = pack_bf16x2(fmaf(e[2], s, b[2]), fmaf(e[3], s, b[3]));
-            ob[g].z = pack_bf16x2(fmaf(e[4], s, b[4]), fmaf(e[5], s, b[5]));
-            ob[g].w = pack_bf16x2(fmaf(e[6], s, b[6]), fmaf(e[7], s, b[7]));
-          } else if constexpr (EPI == EPI_GELU) {
-            uint32_t hw[4];
-            float a[8];
+            uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              hw[i] = pack_bf16x2(fmaf(e[2 * i], s, b[2 * i]), fmaf(e[2 * i + 1], s, b[2 * i + 1]));
-              const float h0 = bf16_bits_to_f32(hw[i] & 0xFFFFu), h1 = bf16_bits_to_f32(hw[i] >> 16);
-              a[2 * i] = 0.5f * h0 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h0 * h0, h0, h0)));
-              a[2 * i + 1] = 0.5f * h1 * (1.0f + tanh_fast(kGeluK * fmaf(kGeluC * h1 * h1, h1, h1)));
+              const uint64_t y = fma2(e2[i], s2, b2[i]);
+              w[i] = pack_bf16x2(lo(y), hi(y));
             }
-            if (ok) {
+            ob[g] = make_uint4(w[0], w[1], w[2], w[3]);
+          } else if constexpr (EPI == EPI_GELU) {
+            // h = bf16(acc * s + b); a = h/2 * (1 + tanh(h * (k + k c h^2)))
+            const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC), H2 = f2(0.5f, 0.5f);
+            uint32_t hw[4];
+            uint64_t a2[4];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) am = max(am, abs_bits(a[i]));
+            for (int i = 0; i < 4; ++i) {
+              const uint64_t hf = fma2(e2[i], s2, b2[i]);
+              hw[i] = pack_bf16x2(lo(hf), hi(hf));
+              const uint64_t h = bf2_to_f2(hw[i]);
+              const uint64_t u = mul2(h, fma2(mul2(h, h), KC2, K2));
+              const uint64_t t = f2(tanh_fast(lo(u)), tanh_fast(hi(u)));
+              const uint64_t hh = mul2(h, H2);
+              a2[i] = fma2(hh, t, hh);
+            }
+            if (full || ok) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(a2[i])), hi(a2[i]));
               if (p.dbg) {
                 float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
-                d4[0] = make_float4(a[0], a[1], a[2], a[3]);
-                d4[1] = make_float4(a[4], a[5], a[6], a[7]);
+                d4[0] = make_float4(lo(a2[0]), hi(a2[0]), lo(a2[1]), hi(a2[1]));
+                d4[1] = make_float4(lo(a2[2]), hi(a2[2]), lo(a2[3]), hi(a2[3]));
               }
             }
             ob[g] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            oq[g] = cvt_fp8x8<QDT>(a, scale_q);
+            const uint64_t q2 = f2(scale_q, scale_q);
+            oq[g].x = (uint32_t)cvt_pair<QDT>(mul2(a2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[1], q2)) << 16);
+            oq[g].y = (uint32_t)cvt_pair<QDT>(mul2(a2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[3], q2)) << 16);
           } else {  // EPI_DGELU
+            // dh = (acc * s) * gelu'(h), gelu'(h) = (1+t)/2 + h/2 (1 - t^2) (k + 3 k c h^2)
+            const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC);
+            const uint64_t KC3 = f2(3.0f * kGeluK * kGeluC, 3.0f * kGeluK * kGeluC), H2 = f2(0.5f, 0.5f), O2 = f2(1.0f, 1.0f);
             const uint32_t hw[4] = {hin[g].x, hin[g].y, hin[g].z, hin[g].w};
-            float dh[8];
+            uint64_t d2[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float h = bf16_bits_to_f32(i & 1 ? hw[i >> 1] >> 16 : hw[i >> 1] & 0xFFFFu);
-              const float t = tanh_fast(kGeluK * fmaf(kGeluC * h * h, h, h));
-              const float gp = fmaf(0.5f * h * (1.0f - t * t), kGeluK * fmaf(3.0f * kGeluC, h * h, 1.0f), 0.5f * (1.0f + t));
-              dh[i] = __fmul_rn(e[i], s) * gp;
+            for (int i = 0; i < 4; ++i) {
+              const uint64_t h = bf2_to_f2(hw[i]);
+              const uint64_t hsq = mul2(h, h);
+              const uint64_t u = mul2(h, fma2(hsq, KC2, K2));
+              const uint64_t t = f2(tanh_fast(lo(u)), tanh_fast(hi(u)));
+              const uint64_t dudh = fma2(hsq, KC3, K2);
+              const uint64_t sech2 = sub2(O2, mul2(t, t));
+              const uint64_t gp = fma2(mul2(mul2(h, H2), sech2), dudh, fma2(t, H2, H2));
+              d2[i] = mul2(mul2(e2[i], s2), gp);
             }
-            oq[g] = cvt_fp8x8<QDT>(dh, scale_q);
-            if (ok) {
+            const uint64_t q2 = f2(scale_q, scale_q);
+            oq[g].x = (uint32_t)cvt_pair<QDT>(mul2(d2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[1], q2)) << 16);
+            oq[g].y = (uint32_t)cvt_pair<QDT>(mul2(d2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[3], q2)) << 16);
+            if (full || ok) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) am = max(am, abs_bits(dh[i]));
+              for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(d2[i])), hi(d2[i]));
               if (p.dbg) {
                 float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
-                d4[0] = make_float4(dh[0], dh[1], dh[2], dh[3]);
-                d4[1] = make_float4(dh[4], dh[5], dh[6], dh[7]);
+                d4[0] = make_float4(lo(d2[0]), hi(d2[0]), lo(d2[1]), hi(d2[1]));
+                d4[1] = make_float4(lo(d2[2]), hi(d2[2]), lo(d2[3]), hi(d2[3]));
               }
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[g * 8 + i] = ok ? dh[i] : 0.f;
+            for (int i = 0; i < 4; ++i) {
+              v[g * 8 + 2 * i] = ok ? lo(d2[i]) : 0.f;
+              v[g * 8 + 2 * i + 1] = ok ? hi(d2[i]) : 0.f;
+            }
           }
         }
         // stage the 32 x 32 results in swizzled shared memory, then one TMA
@@ -528,8 +642,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         __syncwarp();
         if (lane == 0) {
           const int y = m_blk * BM + quarter * 32;
-          if constexpr (EPI != EPI_DGELU) tma_store_2d(&tmO, so_a, (int)n0, y);
-          if constexpr (EPI != EPI_STORE) tma_store_2d(&tmQ, sq_a, (int)n0, y);
+          if (y < p.M) {  // boxes wholly below the last row (the pair's spare tile) are skipped
+            if constexpr (EPI != EPI_DGELU) tma_store_2d(&tmO, so_a, (int)n0, y);
+            if constexpr (EPI != EPI_STORE) tma_store_2d(&tmQ, sq_a, (int)n0, y);
+          }
           bulk_commit();
         }
         if constexpr (EPI == EPI_DGELU) {
@@ -556,7 +672,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           }
         }
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      acc_phase ^= 1;
     }
     if constexpr (EPI == EPI_DGELU) {
       if (h_pending) {  // an abort left a prefetch in flight: let it land first
@@ -568,7 +684,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (lane == 0) bulk_wait0();
     __syncwarp();
     if constexpr (EPI != EPI_STORE) {
-      am = warp_max_u32(am);
+      const uint32_t am = warp_max_u32(abs_bits(am_f));
       if (lane == 0 && am != 0u) atomic_max_amax(p.amax_q, am);
     }
   }
@@ -579,6 +695,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
   }
+  // neither CTA leaves while its peer may still multicast into it or arrive on its barriers
+  cluster_sync();
 }
 
 // Diagnostic: one bounded wait on an mbarrier that nothing arrives on. It
@@ -647,18 +765,40 @@ template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
 lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em, const KParams& kp,
                       cudaStream_t st) {
   auto k = gemm_kernel<BN, A_MN, B_MN, EPI, QDT>;
-  static bool attr = false;
-  if (!attr) {
+  static bool smem_set = false;
+  if (!smem_set) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) != cudaSuccess)
       return check_launch("fp8 gemm: shared memory attribute");
-    attr = true;
+    smem_set = true;
   }
-  const int tiles = kp.num_m * kp.num_n;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: as many clusters as can be resident at once, at most one per work unit
+  static int max_clusters = 0;
+  if (!max_clusters) {
+    cfg.gridDim = dim3(CL * num_sms() / CL);
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg) != cudaSuccess || max_clusters < 1) {
+      cudaGetLastError();
+      max_clusters = num_sms() / CL;
+    }
+  }
+  const int units = ((kp.num_m + CL - 1) / CL) * kp.num_n;
+  const int clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3(clusters * CL);
   static const char* kind = EPI == EPI_GELU ? "gemm_gelu" : EPI == EPI_DGELU ? "gemm_dgelu" :
                             (A_MN ? (B_MN ? "gemm_mn_mn" : "gemm_mn_k") : (B_MN ? "gemm_k_mn" : "gemm_k_k"));
   LaunchScope ls(kind, st);
-  k<<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ta, tb, em.o, em.q, em.h, kp);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, ta, tb, em.o, em.q, em.h, kp);
+  if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8 gemm launch: %s", cudaGetErrorString(e));
   return check_launch("fp8 gemm");
 }
 
@@ -694,7 +834,9 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   CUtensorMap ta, tb;
   const int64_t K = g.K > 0 ? g.K : 1;  // a zero-K product never loads; keep the map valid
   bool ok = a_mn ? make_operand_map(&ta, g.a, g.M, K, BK) : make_operand_map(&ta, g.a, K, g.M, BM);
-  ok = ok && (b_mn ? make_operand_map(&tb, g.b, g.N, K, BK) : make_operand_map(&tb, g.b, K, g.N, bn));
+  // each CTA of a pair loads half of the B tile: [bn/2 rows] K-major, [128 n] or [BK/2 k rows] MN-major
+  ok = ok && (b_mn ? make_operand_map(&tb, g.b, g.N, K, bn == 256 ? BK : BK / CL)
+                   : make_operand_map(&tb, g.b, K, g.N, bn / CL));
   // epilogue boxes: 32 x 32 per warp; unused maps are copies of a valid one
   EpiMaps em;
   em.o = em.q = em.h = ta;
