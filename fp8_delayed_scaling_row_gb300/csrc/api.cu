@@ -493,8 +493,8 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   }
   const int fdt = fwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
-  TRY(cast_launch(a->w1, false, a->F, a->D, fdt, m.scale + 1, m.amax_cur + 1, a->w1q, nullptr, nullptr, st));
-  TRY(cast_launch(a->w2, false, a->D, a->F, fdt, m.scale + 3, m.amax_cur + 3, a->w2q, nullptr, nullptr, st));
+  TRY(cast2_launch(a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q, a->w2, a->D, a->F, m.scale + 3,
+                   m.amax_cur + 3, a->w2q, fdt, st));
   TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
                     a->rsigma, a->ln_out_debug, st));
   GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0, m.scale_inv + 1);

@@ -13,6 +13,12 @@
 #include "common.cuh"
 #include "internal.h"
 
+#define TRY_CAST(x)                    \
+  do {                                 \
+    const lnfp8_status _s = (x);       \
+    if (_s != LNFP8_OK) return _s;     \
+  } while (0)
+
 namespace lnfp8 {
 namespace {
 
@@ -42,11 +48,30 @@ __device__ __forceinline__ void load8<float>(const float* p, float* v) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// One tensor of a (multi-tensor) cast launch; blockIdx.z picks the tensor.
+struct CastT {
+  const void* in;
+  int64_t rows, cols, rows_per_cta;
+  const float* scale;
+  float* amax_cur;
+  uint8_t* out;
+  uint8_t* out_t;
+  float* colsum;
+};
+
 template <typename T, int DT, int TR>
 __global__ void __launch_bounds__(kThreads)
-cast_kernel(const T* __restrict__ in, int64_t rows, int64_t cols, int64_t rows_per_cta,
-            const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
-            uint8_t* __restrict__ out_t, float* colsum) {
+cast_kernel(const CastT t0, const CastT t1) {
+  const CastT& ct = blockIdx.z ? t1 : t0;
+  const T* __restrict__ in = static_cast<const T*>(ct.in);
+  const int64_t rows = ct.rows, cols = ct.cols, rows_per_cta = ct.rows_per_cta;
+  const float* __restrict__ scale_p = ct.scale;
+  float* amax_cur = ct.amax_cur;
+  uint8_t* __restrict__ out = ct.out;
+  uint8_t* __restrict__ out_t = ct.out_t;
+  float* colsum = ct.colsum;
+  // blocks past this tensor's extent (the grid covers the larger tensor) leave at once
+  if ((int64_t)blockIdx.x * kTC >= cols || (int64_t)blockIdx.y * rows_per_cta >= rows) return;
   // TR rows x 64 columns per iteration; each thread owns one 8-column vector
   // of TR/32 rows and issues all of their loads before converting any.
   constexpr int RPT = TR / 32;
@@ -137,35 +162,64 @@ cast_kernel(const T* __restrict__ in, int64_t rows, int64_t cols, int64_t rows_p
 
 }  // namespace
 
+namespace {
+
+struct Grid2 {
+  int64_t strips, ysplit, rows_per_cta;
+};
+
+Grid2 cast_grid(int64_t rows, int64_t cols, int64_t want) {
+  Grid2 g;
+  g.strips = (cols + kTC - 1) / kTC;
+  const int64_t row_tiles = (rows + kTR - 1) / kTR;
+  int64_t ys = (want + g.strips - 1) / g.strips;
+  ys = max64(1, min64(ys, row_tiles));
+  g.rows_per_cta = ((row_tiles + ys - 1) / ys) * kTR;
+  g.ysplit = (rows + g.rows_per_cta - 1) / g.rows_per_cta;
+  return g;
+}
+
+template <typename T>
+lnfp8_status cast_dispatch(dim3 grid, int dtype, const CastT& a, const CastT& b, cudaStream_t st) {
+  if (dtype == LNFP8_E4M3)
+    cast_kernel<T, LNFP8_E4M3, kTR><<<grid, kThreads, 0, st>>>(a, b);
+  else
+    cast_kernel<T, LNFP8_E5M2, kTR><<<grid, kThreads, 0, st>>>(a, b);
+  return check_launch("fp8_quantize");
+}
+
+}  // namespace
+
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st) {
   if (colsum && cols > 0 && cudaMemsetAsync(colsum, 0, cols * sizeof(float), st) != cudaSuccess)
     return check_launch("fp8_quantize: clearing colsum");
   if (rows == 0 || cols == 0) return LNFP8_OK;
-  const int64_t strips = (cols + kTC - 1) / kTC;
-  const int64_t row_tiles = (rows + kTR - 1) / kTR;
-  const int64_t want = 2LL * num_sms();
-  int64_t ysplit = (want + strips - 1) / strips;
-  ysplit = max64(1, min64(ysplit, row_tiles));
-  const int64_t rows_per_cta = ((row_tiles + ysplit - 1) / ysplit) * kTR;
-  ysplit = (rows + rows_per_cta - 1) / rows_per_cta;
-  if (strips > 0x7FFFFFFF || ysplit > 65535)
+  const Grid2 g = cast_grid(rows, cols, 2LL * num_sms());
+  if (g.strips > 0x7FFFFFFF || g.ysplit > 65535)
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8_quantize: tensor too large");
-  dim3 grid((unsigned)strips, (unsigned)ysplit);
+  const CastT t{in, rows, cols, g.rows_per_cta, scale, amax_cur, out, out_t, colsum};
   LaunchScope ls(colsum ? "cast_colsum" : "cast", st);
-  if (in_fp32) {
-    if (dtype == LNFP8_E4M3)
-      cast_kernel<float, LNFP8_E4M3, kTR><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
-    else
-      cast_kernel<float, LNFP8_E5M2, kTR><<<grid, kThreads, 0, st>>>((const float*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
-  } else {
-    if (dtype == LNFP8_E4M3)
-      cast_kernel<uint16_t, LNFP8_E4M3, kTR><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
-    else
-      cast_kernel<uint16_t, LNFP8_E5M2, kTR><<<grid, kThreads, 0, st>>>((const uint16_t*)in, rows, cols, rows_per_cta, scale, amax_cur, out, out_t, colsum);
+  const dim3 grid((unsigned)g.strips, (unsigned)g.ysplit, 1);
+  return in_fp32 ? cast_dispatch<float>(grid, dtype, t, t, st) : cast_dispatch<uint16_t>(grid, dtype, t, t, st);
+}
+
+lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
+                          uint8_t* out0, const uint16_t* in1, int64_t rows1, int64_t cols1, const float* scale1,
+                          float* amax1, uint8_t* out1, int dtype, cudaStream_t st) {
+  if (rows0 == 0 || cols0 == 0 || rows1 == 0 || cols1 == 0) {
+    TRY_CAST(cast_launch(in0, false, rows0, cols0, dtype, scale0, amax0, out0, nullptr, nullptr, st));
+    return cast_launch(in1, false, rows1, cols1, dtype, scale1, amax1, out1, nullptr, nullptr, st);
   }
-  return check_launch("fp8_quantize");
+  const Grid2 g0 = cast_grid(rows0, cols0, num_sms()), g1 = cast_grid(rows1, cols1, num_sms());
+  if (max64(g0.strips, g1.strips) > 0x7FFFFFFF || max64(g0.ysplit, g1.ysplit) > 65535)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "weight cast: tensor too large");
+  const CastT a{in0, rows0, cols0, g0.rows_per_cta, scale0, amax0, out0, nullptr, nullptr};
+  const CastT b{in1, rows1, cols1, g1.rows_per_cta, scale1, amax1, out1, nullptr, nullptr};
+  LaunchScope ls("cast_pair", st);
+  const dim3 grid((unsigned)max64(g0.strips, g1.strips), (unsigned)max64(g0.ysplit, g1.ysplit), 2);
+  return cast_dispatch<uint16_t>(grid, dtype, a, b, st);
 }
 
 }  // namespace lnfp8

@@ -17,6 +17,11 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st);
 
+// Two bf16 tensors cast in one launch (the weights of a LayerNormMLP).
+lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
+                          uint8_t* out0, const uint16_t* in1, int64_t rows1, int64_t cols1, const float* scale1,
+                          float* amax1, uint8_t* out1, int dtype, cudaStream_t st);
+
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st);

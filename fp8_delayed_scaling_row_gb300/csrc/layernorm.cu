@@ -231,15 +231,23 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     }
   }
 
-  // block reduction of the column partials, then one atomic per column per block
+  // block reduction of the column partials: the row groups add their partials
+  // into shared memory one group at a time (plain 16-byte accesses, no bank
+  // conflicts), then one atomic per column per block
+  for (int turn = 0; turn < GPB; ++turn) {
+    __syncthreads();
+    if (g != turn) continue;
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int c = (gt + TPR * j) * 8;
-    if (c >= D) continue;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      atomicAdd(&colred[c + i], accg[j][i]);
-      atomicAdd(&colred[D + c + i], accb[j][i]);
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      if (c >= D) continue;
+      float4* pg = reinterpret_cast<float4*>(colred + c);
+      float4* pb = reinterpret_cast<float4*>(colred + D + c);
+      const float4 g0 = pg[0], g1 = pg[1], b0 = pb[0], b1 = pb[1];
+      pg[0] = make_float4(g0.x + accg[j][0], g0.y + accg[j][1], g0.z + accg[j][2], g0.w + accg[j][3]);
+      pg[1] = make_float4(g1.x + accg[j][4], g1.y + accg[j][5], g1.z + accg[j][6], g1.w + accg[j][7]);
+      pb[0] = make_float4(b0.x + accb[j][0], b0.y + accb[j][1], b0.z + accb[j][2], b0.w + accb[j][3]);
+      pb[1] = make_float4(b1.x + accb[j][4], b1.y + accb[j][5], b1.z + accb[j][6], b1.w + accb[j][7]);
     }
   }
   __syncthreads();
