@@ -59,11 +59,13 @@ constexpr int kEpiWarps = 16;  // two groups of 8, one per accumulator buffer
 constexpr int CL = 2;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 
-template <int BN>
+template <int BN, bool TWO>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 3 : 5;
+  // TWO: 2-SM MMA (cta_group::2): the pair computes a 256 x BN tile and each
+  // CTA keeps only its half of the B tile; otherwise each CTA keeps all of B.
+  static constexpr int STAGES = TWO ? 5 : (BN == 256 ? 3 : 5);
   static constexpr int A_BYTES = BM * BK;
-  static constexpr int B_BYTES = BN * BK;
+  static constexpr int B_BYTES = (TWO ? BN / 2 : BN) * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per epilogue warp: a 32 x 32 bf16 box (2 KB, 64-byte swizzle) and a
   // 32 x 32 FP8 box (1 KB, 32-byte swizzle) staged for TMA stores / loads
@@ -163,6 +165,23 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       : "memory");
 }
 
+// 2-SM forms: the load may signal a barrier in the peer CTA; the MMA / commit
+// are issued by the pair's leader for both CTAs.
+__device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -212,6 +231,18 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mma_f8_cg2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_cg2_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
 // Arrive on the barrier at this offset in every CTA of the mask once the MMAs complete.
 __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
@@ -305,12 +336,12 @@ __device__ __forceinline__ float transpose_reduce32(float* v, int lane) {
 }
 
 // ------------------------------------------------------------ the kernel
-template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
+template <int BN, bool A_MN, bool B_MN, int EPI, int QDT, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmH, const KParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, TWO>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -335,11 +366,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);  // released by the MMAs of both CTAs of the pair
+      // released by the MMAs of both CTAs of the pair (1-SM), or once by the pair's leader (2-SM)
+      mbar_init(empty_bar(s), TWO ? 1 : CL);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps / 2);  // the 8 warps of the group that drains buffer a
+      // the 8 warps of the group that drains buffer a (in both CTAs with the 2-SM MMA)
+      mbar_init(tempty_bar(a), (TWO ? 2 : 1) * (kEpiWarps / 2));
     }
     mbar_init(drain_bar, 1);
     for (int a = 0; a < 2; ++a)
@@ -355,10 +388,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
   if (warp == 2) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(C::TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (TWO) {  // one warp of each CTA of the pair allocates collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(C::TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(C::TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -386,24 +426,35 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t b_dst = a_dst + C::A_BYTES;
-          if (!A_MN) tma_load_2d(a_dst, &tmA, kb * BK, m_blk * BM, fb);
-          else       tma_load_2d(a_dst, &tmA, m_blk * BM, kb * BK, fb);
-          // this CTA's half of the B tile, multicast to both CTAs of the pair
-          if (!B_MN) {
-            tma_load_2d_mc(b_dst + rank * (BN / CL) * BK, &tmB, kb * BK, n_blk * BN + rank * (BN / CL), fb, kPair);
-          } else if (BN == 256) {
-            tma_load_2d_mc(b_dst + rank * 128 * BK, &tmB, n_blk * BN + rank * 128, kb * BK, fb, kPair);
+          if constexpr (TWO) {
+            // both CTAs load their A rows and their half of B into their own
+            // shared memory and signal the leader's barrier, which expects both
+            const uint32_t fl = map_to_rank(fb, 0);
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+            if (!A_MN) tma_load_2d_cg2(a_dst, &tmA, kb * BK, m_blk * BM, fl);
+            else       tma_load_2d_cg2(a_dst, &tmA, m_blk * BM, kb * BK, fl);
+            if (!B_MN) tma_load_2d_cg2(b_dst, &tmB, kb * BK, n_blk * BN + rank * (BN / 2), fl);
+            else       tma_load_2d_cg2(b_dst, &tmB, n_blk * BN + rank * (BN / 2), kb * BK, fl);
           } else {
-            tma_load_2d_mc(b_dst + rank * (BK / CL) * 128, &tmB, n_blk * BN, kb * BK + rank * (BK / CL), fb, kPair);
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            if (!A_MN) tma_load_2d(a_dst, &tmA, kb * BK, m_blk * BM, fb);
+            else       tma_load_2d(a_dst, &tmA, m_blk * BM, kb * BK, fb);
+            // this CTA's half of the B tile, multicast to both CTAs of the pair
+            if (!B_MN) {
+              tma_load_2d_mc(b_dst + rank * (BN / CL) * BK, &tmB, kb * BK, n_blk * BN + rank * (BN / CL), fb, kPair);
+            } else if (BN == 256) {
+              tma_load_2d_mc(b_dst + rank * 128 * BK, &tmB, n_blk * BN + rank * 128, kb * BK, fb, kPair);
+            } else {
+              tma_load_2d_mc(b_dst + rank * (BK / CL) * 128, &tmB, n_blk * BN, kb * BK + rank * (BK / CL), fb, kPair);
+            }
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
+      if (!ok && (!TWO || rank == 0)) {
         // drain: wait (bounded) for the copies of the last armed stages to land
         const int64_t pending = issued < STAGES ? issued : STAGES;
         int s = stage;
@@ -417,7 +468,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (with the 2-SM MMA only the pair's leader issues, for both CTAs)
+    if (lane == 0 && (!TWO || rank == 0)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -436,7 +488,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint32_t accum = (kb | kk) != 0;
             const uint64_t ad = A_MN ? make_desc(a_base + kk * 32 * 128, 1024, 1024) : make_desc(a_base + kk * 32, 16, 1024);
-            if (!B_MN) {
+            if constexpr (TWO) {
+              // 256 x BN x 32 over the pair: A rows and B halves from both CTAs
+              const uint64_t bd = B_MN ? make_desc(b_base + kk * 32 * 128, 1024, 1024) : make_desc(b_base + kk * 32, 16, 1024);
+              mma_f8_cg2(d_tmem, ad, bd, p.idesc, accum);
+            } else if (!B_MN) {
               mma_f8(d_tmem, ad, make_desc(b_base + kk * 32, 16, 1024), p.idesc, accum);
             } else {
 #pragma unroll
@@ -444,16 +500,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 mma_f8(d_tmem + j * 128, ad, make_desc(b_base + j * 128 * BK + kk * 32 * 128, 1024, 1024), p.idesc, accum);
             }
           }
-          mma_commit_mc(empty_bar(stage), kPair);  // frees the stage in both CTAs
+          if constexpr (TWO) mma_commit_cg2_mc(empty_bar(stage), kPair);  // frees the stage in both CTAs
+          else mma_commit_mc(empty_bar(stage), kPair);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        if constexpr (TWO) mma_commit_cg2_mc(tfull_bar(acc), kPair);  // both CTAs' accumulators are ready
+        else mma_commit(tfull_bar(acc));
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
       if (!ok) {
         // make sure no MMA still writes tensor memory before it is freed
-        mma_commit(drain_bar);
+        if constexpr (TWO) mma_commit_cg2_mc(drain_bar, 1);
+        else mma_commit(drain_bar);
         uint32_t dummy_flag = 0;
         mbar_wait(drain_bar, 0, &dummy_flag, 100000000ull);
       }
@@ -492,6 +551,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       }
       h_pending = true;
     };
+    // the accumulator is released to the CTA whose MMA reuses it (the leader with the 2-SM MMA)
+    const uint32_t tempty_target = TWO ? map_to_rank(tempty_bar(acc), 0) : tempty_bar(acc);
+    auto release_acc = [&]() {
+      if constexpr (TWO) mbar_arrive_remote(tempty_target);
+      else mbar_arrive(tempty_target);
+    };
     const int u0 = cid + grp * ncl;  // this group's first unit; then every second one
     if constexpr (EPI == EPI_DGELU) {
       if (u0 < num_units) issue_h(u0, 0);
@@ -517,7 +582,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (ch == CHUNKS - 1 && !combiner) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) release_acc();
         }
         uint4 hin[4];
         if constexpr (EPI == EPI_DGELU) {
@@ -668,7 +733,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) release_acc();
           }
         }
       }
@@ -691,9 +756,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
   tc_fence_before();
   __syncthreads();
+  // both CTAs are done with the pair's tensor memory before it is freed
+  cluster_sync();
   if (warp == 2) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
+    if constexpr (TWO)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
   }
   // neither CTA leaves while its peer may still multicast into it or arrive on its barriers
   cluster_sync();
@@ -751,23 +821,24 @@ struct EpiMaps {
   CUtensorMap o, q, h;
 };
 
-uint32_t make_idesc(int n_mma, int a_dt, int b_dt, bool a_mn, bool b_mn) {
+uint32_t make_idesc(int m_mma, int n_mma, int a_dt, int b_dt, bool a_mn, bool b_mn) {
   return (1u << 4) |                       // accumulator fp32
          ((uint32_t)a_dt << 7) |           // A: 0 E4M3, 1 E5M2
          ((uint32_t)b_dt << 10) |          // B
          ((a_mn ? 1u : 0u) << 15) |        // A major (1 = MN)
          ((b_mn ? 1u : 0u) << 16) |        // B major
          ((uint32_t)(n_mma >> 3) << 17) |  // N / 8
-         ((uint32_t)(BM >> 4) << 24);      // M / 16
+         ((uint32_t)(m_mma >> 4) << 24);   // M / 16
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, int QDT>
+template <int BN, bool A_MN, bool B_MN, int EPI, int QDT, bool TWO = (BN == 256)>
 lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em, const KParams& kp,
                       cudaStream_t st) {
-  auto k = gemm_kernel<BN, A_MN, B_MN, EPI, QDT>;
+  auto k = gemm_kernel<BN, A_MN, B_MN, EPI, QDT, TWO>;
+  using C = Cfg<BN, TWO>;
   static bool smem_set = false;
   if (!smem_set) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return check_launch("fp8 gemm: shared memory attribute");
     smem_set = true;
   }
@@ -778,7 +849,7 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -852,7 +923,10 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.num_m = (int)num_m;
   kp.num_n = (int)num_n;
   kp.num_kb = (int)((g.K + BK - 1) / BK);
-  kp.idesc = make_idesc(b_mn ? 128 : bn, g.a_dtype, g.b_dtype, a_mn, b_mn);
+  // 256-wide tiles run the 2-SM MMA (M = 256 over the CTA pair, N = 256);
+  // 128-wide tiles the 1-SM MMA (M = 128; N = 128 per instruction for MN-major B)
+  kp.idesc = bn == 256 ? make_idesc(256, 256, g.a_dtype, g.b_dtype, a_mn, b_mn)
+                       : make_idesc(128, b_mn ? 128 : bn, g.a_dtype, g.b_dtype, a_mn, b_mn);
   kp.sinv_a = g.sinv_a;
   kp.sinv_b = g.sinv_b;
   kp.bias = g.bias;

@@ -10,6 +10,7 @@ import pytest
 
 from fp8_delayed_scaling_row_gb300 import synth
 from oracle import fp8 as ofp8
+from oracle import fp8
 from oracle import gemm as ogemm
 from oracle import layernorm as oln
 from oracle.delayed_scaling import ScalingState
@@ -199,6 +200,21 @@ def test_gemm_exact_integer_problems(L, a_layout, b_layout, M, N, K, adt, bdt):
     bt = torch.from_numpy(np.ascontiguousarray(b if b_layout == 0 else b.T)).cuda()
     out = L.fp8_gemm(at, a_layout, adt, bt, b_layout, bdt, M, N, K, _scalar(float(sa)), _scalar(float(sb)), bias=bf16_dev(bias))
     ref = ogemm.fp8_gemm(a, FMT[adt], b, FMT[bdt], sa, sb, synth.bf16_bits_to_f32(bias))
+    assert np.array_equal(host(out), ogemm.bf16_to_f32(ogemm.to_bf16_bits(ref)).astype(np.float64))
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("M,N,K", [(4864, 1024, 1024), (4880, 1040, 1104)])
+def test_gemm_exact_integer_problems_on_the_pair_tiles(L, a_layout, b_layout, M, N, K):
+    """Enough tiles for the 256-wide CTA-pair tiles (2-SM MMA) and more K blocks
+    than pipeline stages, with ragged M, N and K tails."""
+    rng = np.random.default_rng(M + N + K + a_layout)
+    a = _int_codes((M, K), fp8.E4M3, rng)
+    b = _int_codes((N, K), fp8.E5M2, rng)
+    at = torch.from_numpy(np.ascontiguousarray(a if a_layout == 0 else a.T)).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(b if b_layout == 0 else b.T)).cuda()
+    out = L.fp8_gemm(at, a_layout, 0, bt, b_layout, 1, M, N, K, _scalar(0.25), _scalar(0.5))
+    ref = ogemm.fp8_gemm(a, fp8.E4M3, b, fp8.E5M2, 0.25, 0.5)
     assert np.array_equal(host(out), ogemm.bf16_to_f32(ogemm.to_bf16_bits(ref)).astype(np.float64))
 
 
