@@ -15,6 +15,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -41,6 +42,11 @@ lnfp8_status check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return LNFP8_OK;
+}
+
+bool pdl_enabled() {
+  static const bool on = getenv("LNFP8_NO_PDL") == nullptr;
+  return on;
 }
 
 int num_sms() {
@@ -165,6 +171,11 @@ lnfp8_status finish_state(const lnfp8_meta* m, const lnfp8_recipe* r, int dt, fl
   if (!defer) return update_launch(m, mask_all(m->n, dt), r->margin, sinv_saved, st);
   if (sinv_saved && cudaMemcpyAsync(sinv_saved, m->scale_inv, m->n * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return check_launch("saving scale_inv");
+  return LNFP8_OK;
+}
+
+lnfp8_status clear_f32(float* p, int64_t n, cudaStream_t st) {
+  if (p && n > 0 && cudaMemsetAsync(p, 0, n * sizeof(float), st) != cudaSuccess) return check_launch("clearing an output");
   return LNFP8_OK;
 }
 
@@ -448,7 +459,13 @@ lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream strea
   }
   const int fdt = fwd_dtype(&a->recipe), bdt = bwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
-  TRY(cast_launch(a->dy, false, a->M, a->N, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->dbias, st));
+  // the accumulated outputs are cleared first, so the kernels below run back to back
+  TRY(clear_f32(a->dbias, a->N, st));
+  if (ln) {
+    TRY(clear_f32(a->dgamma, a->K, st));
+    TRY(clear_f32(a->dbeta, a->K, st));
+  }
+  TRY(cast_launch(a->dy, false, a->M, a->N, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->dbias, st, false));
   uint16_t* dln = ln ? a->dln : a->dx;
   GemmArgs dg = gemm_args(a->dyq, 0, bdt, a->wq, 1, fdt, a->M, a->K, a->N, m.scale_inv + 0, a->sinv_saved + 1);
   dg.out = dln;
@@ -456,7 +473,7 @@ lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream strea
   GemmArgs wg = gemm_args(a->dyq, 1, bdt, a->xq, 1, fdt, a->N, a->K, a->M, m.scale_inv + 0, a->sinv_saved + 0);
   wg.out = a->dw;
   TRY(wgrad(wg, a->dw, st));
-  if (ln) TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st));
+  if (ln) TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st, false));
   return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
 }
 
@@ -551,8 +568,12 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   }
   const int fdt = fwd_dtype(&a->recipe), bdt = bwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
-  TRY(cast_launch(a->dy, false, a->M, a->D, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->db2, st));
-  if (a->db1 && cudaMemsetAsync(a->db1, 0, a->F * sizeof(float), st) != cudaSuccess) return check_launch("clearing db1");
+  // the accumulated outputs are cleared first, so the kernels below run back to back
+  TRY(clear_f32(a->db2, a->D, st));
+  TRY(clear_f32(a->db1, a->F, st));
+  TRY(clear_f32(a->dgamma, a->D, st));
+  TRY(clear_f32(a->dbeta, a->D, st));
+  TRY(cast_launch(a->dy, false, a->M, a->D, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->db2, st, false));
   // FC2 dgrad with the GELU derivative and the dH cast fused: dH = (dYq . W2q) * s * gelu'(H)
   GemmArgs d2 = gemm_args(a->dyq, 0, bdt, a->w2q, 1, fdt, a->M, a->F, a->D, m.scale_inv + 0, a->sinv_saved + 3);
   d2.epi = EPI_DGELU;
@@ -576,7 +597,7 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   GemmArgs w1 = gemm_args(a->dhq, 1, bdt, a->lnq, 1, fdt, a->F, a->D, a->M, m.scale_inv + 1, a->sinv_saved + 0);
   w1.out = a->dw1;
   TRY(wgrad(w1, a->dw1, st));
-  TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st));
+  TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st, false));
   return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
 }
 

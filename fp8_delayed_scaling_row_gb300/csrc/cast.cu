@@ -62,6 +62,8 @@ struct CastT {
 template <typename T, int DT, int TR>
 __global__ void __launch_bounds__(kThreads)
 cast_kernel(const CastT t0, const CastT t1) {
+  pdl_wait();
+  pdl_launch_dependents();
   const CastT& ct = blockIdx.z ? t1 : t0;
   const T* __restrict__ in = static_cast<const T*>(ct.in);
   const int64_t rows = ct.rows, cols = ct.cols, rows_per_cta = ct.rows_per_cta;
@@ -181,10 +183,9 @@ Grid2 cast_grid(int64_t rows, int64_t cols, int64_t want) {
 
 template <typename T>
 lnfp8_status cast_dispatch(dim3 grid, int dtype, const CastT& a, const CastT& b, cudaStream_t st) {
-  if (dtype == LNFP8_E4M3)
-    cast_kernel<T, LNFP8_E4M3, kTR><<<grid, kThreads, 0, st>>>(a, b);
-  else
-    cast_kernel<T, LNFP8_E5M2, kTR><<<grid, kThreads, 0, st>>>(a, b);
+  const cudaError_t e = dtype == LNFP8_E4M3 ? launch_pdl(cast_kernel<T, LNFP8_E4M3, kTR>, grid, dim3(kThreads), 0, st, a, b)
+                                             : launch_pdl(cast_kernel<T, LNFP8_E5M2, kTR>, grid, dim3(kThreads), 0, st, a, b);
+  if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8_quantize launch: %s", cudaGetErrorString(e));
   return check_launch("fp8_quantize");
 }
 
@@ -192,8 +193,8 @@ lnfp8_status cast_dispatch(dim3 grid, int dtype, const CastT& a, const CastT& b,
 
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
-                         float* colsum, cudaStream_t st) {
-  if (colsum && cols > 0 && cudaMemsetAsync(colsum, 0, cols * sizeof(float), st) != cudaSuccess)
+                         float* colsum, cudaStream_t st, bool clear_colsum) {
+  if (clear_colsum && colsum && cols > 0 && cudaMemsetAsync(colsum, 0, cols * sizeof(float), st) != cudaSuccess)
     return check_launch("fp8_quantize: clearing colsum");
   if (rows == 0 || cols == 0) return LNFP8_OK;
   const Grid2 g = cast_grid(rows, cols, 2LL * num_sms());

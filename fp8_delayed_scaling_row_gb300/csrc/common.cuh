@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <utility>
 #include <cuda_fp8.h>
 #include <stdint.h>
 
@@ -31,6 +32,32 @@ struct LaunchScope {
 // gemm.cu): bit 0 = a bounded wait gave up. Read and cleared from the host.
 constexpr unsigned int kStatusTimeout = 1u;
 lnfp8_status status_read_clear(cudaStream_t st, unsigned int* word);
+
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel on the stream finishes; each
+// kernel runs only set-up that reads no data before pdl_wait(), which returns
+// once the previous grid has completed and its writes are visible. Because
+// every kernel waits before it completes, the ordering is transitive.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();  // off when the environment sets LNFP8_NO_PDL
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {

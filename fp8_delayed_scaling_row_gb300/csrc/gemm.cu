@@ -404,6 +404,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up above touches no data; from here on the previous kernel's outputs are read
+  pdl_wait();
+  pdl_launch_dependents();
 
   // Work units: one N tile and CL consecutive M tiles, one per CTA of a cluster.
   const int rank = CL == 2 ? (int)cluster_rank() : 0;
@@ -843,11 +846,13 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
     smem_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
@@ -865,6 +870,7 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
   const int units = ((kp.num_m + CL - 1) / CL) * kp.num_n;
   const int clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3(clusters * CL);
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   static const char* kind = EPI == EPI_GELU ? "gemm_gelu" : EPI == EPI_DGELU ? "gemm_dgelu" :
                             (A_MN ? (B_MN ? "gemm_mn_mn" : "gemm_mn_k") : (B_MN ? "gemm_k_mn" : "gemm_k_k"));
   LaunchScope ls(kind, st);

@@ -15,7 +15,7 @@ lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, 
 
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
-                         float* colsum, cudaStream_t st);
+                         float* colsum, cudaStream_t st, bool clear_colsum = true);
 
 // Two bf16 tensors cast in one launch (the weights of a LayerNormMLP).
 lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
@@ -27,7 +27,7 @@ lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint1
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st);
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
-                           float* dbeta, cudaStream_t st);
+                           float* dbeta, cudaStream_t st, bool clear = true);
 
 // Epilogues of the FP8 GEMM.
 enum GemmEpilogue {

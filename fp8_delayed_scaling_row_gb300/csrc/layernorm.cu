@@ -63,6 +63,8 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
   const int nvec = D >> 3;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int i = threadIdx.x; i < nvec; i += kThreads) {
     sgb[i] = reinterpret_cast<const uint4*>(gamma)[i];
     sgb[nvec + i] = reinterpret_cast<const uint4*>(beta)[i];
@@ -162,6 +164,8 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
   const int gt = threadIdx.x % TPR;
   const float inv_d = 1.0f / (float)D;
   const int nvec = D >> 3;
+  pdl_wait();
+  pdl_launch_dependents();
 
   for (int c = threadIdx.x; c < 2 * D; c += kThreads) colred[c] = 0.f;
   for (int i = threadIdx.x; i < nvec; i += kThreads) sg[i] = reinterpret_cast<const uint4*>(gamma)[i];
@@ -288,7 +292,8 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
     auto k = ln_fwd_kernel<TPR, NV, DT>;                                                                \
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                        \
-    k<<<(unsigned)blocks, kThreads, smem, st>>>(x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg); \
+    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg) != cudaSuccess) \
+      return check_launch("ln_fwd_cast launch");                                                        \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
     case 321: LNF(32, 1); break;
@@ -326,8 +331,8 @@ lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint1
 
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
-                           float* dbeta, cudaStream_t st) {
-  if (D > 0) {
+                           float* dbeta, cudaStream_t st, bool clear) {
+  if (clear && D > 0) {
     if (cudaMemsetAsync(dgamma, 0, D * sizeof(float), st) != cudaSuccess ||
         cudaMemsetAsync(dbeta, 0, D * sizeof(float), st) != cudaSuccess)
       return check_launch("ln_bwd: clearing dgamma/dbeta");
@@ -343,7 +348,8 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
     auto k = ln_bwd_kernel<TPR, NV>;                                                                   \
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                       \
-    k<<<(unsigned)blocks, kThreads, smem, st>>>(dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta); \
+    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta) != cudaSuccess) \
+      return check_launch("ln_bwd launch");                                                            \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
     case 321: LNB(32, 1); break;

@@ -24,6 +24,8 @@ update_kernel(float* __restrict__ scale, float* __restrict__ scale_inv, float* _
   __shared__ uint32_t red[kThreads / 32];
   const int i = blockIdx.x;
   const int t = threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
   const float c = cur[i];
   // read phase: the new row j is the old row j-1, the new row 0 is cur
   uint32_t m = 0;
@@ -96,8 +98,9 @@ lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, 
       return check_launch("amax_history_update: smem attribute");
   }
   LaunchScope ls("state_update", st);
-  update_kernel<<<m->n, kThreads, smem, st>>>(m->scale, m->scale_inv, m->amax_history, m->amax_cur, m->n,
-                                              m->history_len, e5m2_mask, margin, sinv_before);
+  if (launch_pdl(update_kernel, dim3(m->n), dim3(kThreads), smem, st, m->scale, m->scale_inv, m->amax_history,
+                 m->amax_cur, m->n, m->history_len, e5m2_mask, margin, sinv_before) != cudaSuccess)
+    return check_launch("amax_history_update launch");
   return check_launch("amax_history_update");
 }
 
