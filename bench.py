@@ -242,6 +242,19 @@ class MlpRun:
                      ctx=self.ctx)
         L.ln_mlp_bwd(dy, x, p["gamma"], self.ctx, self.bm, self.rec, grads=self.grads)
 
+    def capture_one(self, i):
+        """One CUDA graph of the step on input batch i, the state restored after capture."""
+        torch = self.torch
+        sd_f, sd_b = self.fm.state_dict(), self.bm.state_dict()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._call(self.xs[i], self.dys[i])
+        torch.cuda.synchronize()
+        self.fm.load_state_dict(sd_f)
+        self.bm.load_state_dict(sd_b)
+        return g
+
     def capture(self):
         """Capture one CUDA graph per input batch (the state buffers are shared, so
         replays advance the delayed-scaling state exactly like direct calls)."""
@@ -335,13 +348,28 @@ def run_gpu(args):
     value = flops_per_step() * args.steps * world / (ms / 1e3) / 1e12
 
     # ---- per-kernel times inside the same workload (events on the launching stream)
-    L.profile_enable(True)
     prof_steps = min(args.steps, 50)
-    for i in range(prof_steps):  # direct calls: the library brackets each of its launches with events
-        flush.zero_()
-        run._call(run.xs[i % len(run.xs)], run.dys[i % len(run.dys)])
-    prof = L.profile_collect()
-    L.profile_enable(False)
+    prof, prof_how = {}, "graph"
+    if args.graph:
+        # the step captured once more with the library's event pairs as graph nodes; every
+        # replay re-records them (the event nodes sit between kernels, so no launch overlap)
+        L.profile_enable(True)
+        pg = run.capture_one(0)
+        for i in range(prof_steps):
+            flush.zero_()
+            pg.replay()
+            L.profile_sample()
+        prof = L.profile_collect()
+        L.profile_enable(False)
+        del pg
+    if not prof:
+        prof_how = "direct calls"
+        L.profile_enable(True)
+        for i in range(prof_steps):  # direct calls: the library brackets each of its launches with events
+            flush.zero_()
+            run._call(run.xs[i % len(run.xs)], run.dys[i % len(run.dys)])
+        prof = L.profile_collect()
+        L.profile_enable(False)
     gemm_kinds = {k: v for k, v in prof.items() if k.startswith("gemm")}
     g_ms = sum(v[0] for v in gemm_kinds.values())
     g_n = sum(v[1] for v in gemm_kinds.values())
@@ -354,7 +382,7 @@ def run_gpu(args):
                 "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak if achieved else None, "traffic": gemm_traffic_from_profile(),
                 "peak_source": f"{how} bf16 dense x {FP8_PER_BF16:g} (nominal FP8/BF16 ratio)",
-                "flops_per_launch": g_flops, "launches_timed": g_n,
+                "flops_per_launch": g_flops, "launches_timed": g_n, "timed_from": prof_how,
                 "share_of_step": g_ms / sum(v[0] for v in prof.values()) if prof else None}
     hbm = _num(pk, "hbm_gbs", "hbm_GBs", "hbm_copy_gbs") or FALLBACK["hbm_gbs"]
     per_kernel = {}

@@ -67,6 +67,7 @@ namespace {
 struct ProfRec {
   const char* kind;
   cudaEvent_t a, b;
+  bool sampled;  // its time already went into the rows (a graph replay sample)
 };
 struct ProfRow {
   std::string kind;
@@ -78,8 +79,19 @@ std::atomic<bool> g_prof_on{false};
 std::mutex g_prof_mu;
 std::vector<ProfRec> g_prof_open;      // recorded, not yet collected
 std::vector<cudaEvent_t> g_event_pool;  // reusable events
-std::vector<ProfRow> g_prof_rows;      // the last collection
+std::vector<ProfRow> g_prof_rows;      // totals since profiling was switched on
 thread_local int g_open_idx = -1;
+
+// external records become event nodes when the stream is being captured into a graph;
+// outside a capture the flag is not accepted
+unsigned record_flags(cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return cudaEventRecordDefault;
+  }
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+}
 
 cudaEvent_t pool_event() {
   if (!g_event_pool.empty()) {
@@ -97,8 +109,8 @@ void launch_begin(const char* kind, cudaStream_t st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!g_prof_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  ProfRec r{kind, pool_event(), pool_event()};
-  cudaEventRecord(r.a, st);
+  ProfRec r{kind, pool_event(), pool_event(), false};
+  cudaEventRecordWithFlags(r.a, st, record_flags(st));
   g_prof_open.push_back(r);
   g_open_idx = (int)g_prof_open.size() - 1;
 }
@@ -106,7 +118,7 @@ void launch_begin(const char* kind, cudaStream_t st) {
 void launch_end(cudaStream_t st) {
   if (!g_prof_on.load(std::memory_order_relaxed) || g_open_idx < 0) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  if (g_open_idx < (int)g_prof_open.size()) cudaEventRecord(g_prof_open[g_open_idx].b, st);
+  if (g_open_idx < (int)g_prof_open.size()) cudaEventRecordWithFlags(g_prof_open[g_open_idx].b, st, record_flags(st));
   g_open_idx = -1;
 }
 
@@ -226,23 +238,42 @@ lnfp8_status lnfp8_profile_enable(int on) {
   return LNFP8_OK;
 }
 
+namespace {
+// adds the elapsed time of every open record to the rows; caller holds g_prof_mu
+void prof_add_open(bool only_unsampled) {
+  for (auto& r : g_prof_open) {
+    if (only_unsampled && r.sampled) continue;
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    r.sampled = true;
+    bool found = false;
+    for (auto& row : g_prof_rows)
+      if (row.kind == r.kind) {
+        row.ms += ms;
+        row.launches += 1;
+        found = true;
+        break;
+      }
+    if (!found) g_prof_rows.push_back({r.kind, (double)ms, 1});
+  }
+}
+}  // namespace
+
+lnfp8_status lnfp8_profile_sample(void) {
+  clear_error();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  prof_add_open(false);
+  return LNFP8_OK;
+}
+
 int lnfp8_profile_collect(void) {
   clear_error();
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  g_prof_rows.clear();
+  prof_add_open(true);
   for (auto& r : g_prof_open) {
-    float ms = 0.f;
-    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
-      bool found = false;
-      for (auto& row : g_prof_rows)
-        if (row.kind == r.kind) {
-          row.ms += ms;
-          row.launches += 1;
-          found = true;
-          break;
-        }
-      if (!found) g_prof_rows.push_back({r.kind, (double)ms, 1});
-    }
     g_event_pool.push_back(r.a);
     g_event_pool.push_back(r.b);
   }

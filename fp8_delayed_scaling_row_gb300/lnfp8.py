@@ -29,7 +29,7 @@ _FORMATS = {"e4m3": FORMAT_E4M3, "hybrid": FORMAT_HYBRID, "e5m2": FORMAT_E5M2}
 
 EXPORTED = [
     "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_launch_count",
-    "lnfp8_profile_enable", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
+    "lnfp8_profile_enable", "lnfp8_profile_sample", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
     "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
     "ln_linear_bwd_noalloc", "ln_mlp_fwd",
     "ln_mlp_bwd",
@@ -99,6 +99,7 @@ _c_version = _sig("lnfp8_version", [])
 _c_selftest = _sig("lnfp8_selftest_timeout", [_I64, _P])
 _c_launch_count = _sig("lnfp8_launch_count", [], C.c_longlong)
 _c_prof_enable = _sig("lnfp8_profile_enable", [C.c_int])
+_c_prof_sample = _sig("lnfp8_profile_sample", [])
 _c_prof_collect = _sig("lnfp8_profile_collect", [])
 _c_prof_get = _sig("lnfp8_profile_get", [C.c_int, C.POINTER(C.c_char_p), C.POINTER(C.c_double),
                                          C.POINTER(C.c_longlong)])
@@ -150,6 +151,11 @@ def launch_count() -> int:
 def profile_enable(on: bool = True) -> None:
     """Per-kernel CUDA-event timing on the launching stream (discards old records)."""
     _check(_c_prof_enable(int(on)))
+
+
+def profile_sample() -> None:
+    """After a replay of a graph captured with profiling on: add its kernel times to the totals."""
+    _check(_c_prof_sample())
 
 
 def profile_collect() -> dict:

@@ -117,13 +117,20 @@ lnfp8_status lnfp8_selftest_timeout(int64_t limit_ns, lnfp8_stream stream);
 /* Number of kernels this library has launched in this process. */
 long long lnfp8_launch_count(void);
 
-/* Switches per-kernel timing on (1) or off (0) and discards earlier records.
- * While on, every kernel launch is bracketed by two CUDA events recorded on
- * the launch's own stream (host-side cost only; no device memory). */
+/* Switches per-kernel timing on (1) or off (0) and discards earlier records
+ * and totals. While on, every kernel launch is bracketed by two CUDA events
+ * recorded on the launch's own stream (host-side cost only; no device
+ * memory). Inside a stream capture the two records become event nodes of the
+ * graph, so each replay of the graph re-records them. */
 lnfp8_status lnfp8_profile_enable(int on);
 
-/* Waits for the recorded events, aggregates them by kernel kind and returns
- * the number of kinds; the records are consumed. */
+/* For a captured graph: waits for the open records, adds their times to the
+ * totals and keeps the records, so that it can be called after every replay. */
+lnfp8_status lnfp8_profile_sample(void);
+
+/* Waits for the open records that no sample has counted yet, adds them to the
+ * totals, releases all records and returns the number of kernel kinds in the
+ * totals (which accumulate until the next lnfp8_profile_enable). */
 int lnfp8_profile_collect(void);
 
 /* Kind i (0 <= i < the count lnfp8_profile_collect returned): its name (owned

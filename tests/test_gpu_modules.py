@@ -267,3 +267,56 @@ def test_linear_with_ln_multistep_ragged(L):
 
 def test_linear_without_ln(L):
     run_linear(L, M=250, K=256, N=128, steps=2, ln=False)
+
+
+def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profiled(L):
+    """The step captured into a CUDA graph (as the benchmark replays it) gives the
+    direct call's results; per-kernel timing works for direct calls and for
+    replays of a graph captured with timing on."""
+    M, D, F = 1000, 256, 1024
+    p = {k: bf16_dev(v) for k, v in synth.mlp_params(D, F, bias_std=0.02, seed=5).items()}
+    x = bf16_dev(synth.activations(M, D, dist="outliers", seed=5, step=0))
+    dy = bf16_dev(synth.grad(M, D, seed=5, step=0))
+    rec = L.Recipe("hybrid", 4)
+
+    def make():
+        return L.ScalingMeta(4, 4), L.ScalingMeta(2, 4), L.mlp_ctx(M, D, F), L.mlp_grads(M, D, F)
+
+    def call(fm, bm, ctx, g, y):
+        L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], fm, rec, y=y, ctx=ctx)
+        L.ln_mlp_bwd(dy, x, p["gamma"], ctx, bm, rec, grads=g)
+
+    fm0, bm0, ctx0, g0 = make()
+    y0 = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
+    L.profile_enable(True)
+    call(fm0, bm0, ctx0, g0, y0)
+    direct = L.profile_collect()
+    L.profile_enable(False)
+    L.sync_status()
+    assert sum(n for _, n in direct.values()) == 12 and all(ms > 0 for ms, _ in direct.values())
+
+    fm1, bm1, ctx1, g1 = make()
+    y1 = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    L.profile_enable(True)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call(fm1, bm1, ctx1, g1, y1)
+    graph.replay()
+    torch.cuda.synchronize()
+    L.profile_sample()
+    replayed = L.profile_collect()
+    L.profile_enable(False)
+    L.sync_status()
+    assert set(replayed) == set(direct)
+    assert all(replayed[k][1] == direct[k][1] and replayed[k][0] > 0 for k in direct)
+
+    for a, b in [(y0, y1), (g0.dx, g1.dx), (g0.dw1, g1.dw1), (g0.dw2, g1.dw2)]:
+        assert torch.equal(a, b)
+    for a, b in [(g0.db1, g1.db1), (g0.db2, g1.db2), (g0.dgamma, g1.dgamma), (g0.dbeta, g1.dbeta)]:
+        assert rel_fro(host(a), host(b)) < 1e-5  # column sums use float atomics (order may differ)
+    for m0, m1 in [(fm0, fm1), (bm0, bm1)]:
+        for name in ("scale", "scale_inv", "amax_history"):
+            assert torch.equal(getattr(m0, name), getattr(m1, name)), name
