@@ -186,9 +186,33 @@ lnfp8_status finish_state(const lnfp8_meta* m, const lnfp8_recipe* r, int dt, fl
   return LNFP8_OK;
 }
 
-lnfp8_status clear_f32(float* p, int64_t n, cudaStream_t st) {
-  if (p && n > 0 && cudaMemsetAsync(p, 0, n * sizeof(float), st) != cudaSuccess) return check_launch("clearing an output");
-  return LNFP8_OK;
+// The split-K workspace shared by the GEMMs of one call (they run one after
+// another): one flag area, as large as the largest any of them needs, then one
+// slot area. Each GEMM takes it only if its own plan fits. Returns the flag
+// span the call zeroes before its first kernel.
+std::pair<void*, int64_t> share_split_ws(std::initializer_list<GemmArgs*> gs, void* ws, int64_t bytes) {
+  if (!ws || bytes <= 0) return {nullptr, 0};
+  int64_t flags = 0;
+  for (const GemmArgs* g : gs) {
+    const GemmPlan pl = gemm_plan(g->M, g->N, g->K, g->epi, true);
+    if (pl.splits > 1 && pl.flag_bytes > flags) flags = pl.flag_bytes;
+  }
+  for (GemmArgs* g : gs) {
+    g->ws = ws;
+    g->ws_bytes = bytes;
+    g->ws_flag_bytes = flags;
+  }
+  return {ws, flags < bytes ? flags : bytes};
+}
+
+// Workspace bytes that let every GEMM of a call split as planned.
+int64_t shared_split_bytes(std::initializer_list<GemmPlan> pls) {
+  int64_t flags = 0, slots = 0;
+  for (const GemmPlan& pl : pls) {
+    flags = pl.flag_bytes > flags ? pl.flag_bytes : flags;
+    slots = pl.slot_bytes > slots ? pl.slot_bytes : slots;
+  }
+  return slots ? flags + slots : 0;
 }
 
 GemmArgs gemm_args(const uint8_t* a, int al, int adt, const uint8_t* b, int bl, int bdt, int64_t M, int64_t N,
@@ -387,7 +411,7 @@ lnfp8_status ln_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma
 
 lnfp8_status fp8_gemm(const uint8_t* A, int a_layout, int a_dtype, const uint8_t* B, int b_layout, int b_dtype, int64_t M,
                       int64_t N, int64_t K, const float* sinv_a, const float* sinv_b, const uint16_t* bias,
-                      uint16_t* out, lnfp8_stream stream) {
+                      uint16_t* out, void* workspace, int64_t workspace_bytes, lnfp8_stream stream) {
   const char* who = "fp8_gemm";
   clear_error();
   TRY(tokens(M, who));
@@ -406,10 +430,29 @@ lnfp8_status fp8_gemm(const uint8_t* A, int a_layout, int a_dtype, const uint8_t
     REQ(out, who);
   }
   REQ(B, who);
+  OPT(workspace, who);
+  if (workspace && workspace_bytes < 0) return set_error(LNFP8_ERR_INVALID_ARG, "%s: workspace_bytes < 0", who);
   GemmArgs g = gemm_args(A, a_layout, a_dtype, B, b_layout, b_dtype, M, N, K, sinv_a, sinv_b);
   g.bias = bias;
   g.out = out;
+  TRY(zero_launch({share_split_ws({&g}, workspace, workspace_bytes)}, (cudaStream_t)stream));
   return gemm_launch(g, (cudaStream_t)stream);
+}
+
+int64_t lnfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  return gemm_plan(M, N, K, EPI_STORE, true).ws_bytes;
+}
+
+int64_t lnfp8_ln_linear_bwd_workspace_size(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  return shared_split_bytes({gemm_plan(M, K, N, EPI_STORE, true), gemm_plan(N, K, M, EPI_STORE, true)});
+}
+
+int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F) {
+  if (M < 0 || D < 0 || F < 0) return -1;
+  return shared_split_bytes({gemm_plan(D, F, M, EPI_STORE, true), gemm_plan(M, D, F, EPI_STORE, true),
+                             gemm_plan(F, D, M, EPI_STORE, true)});
 }
 
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream stream) {
@@ -490,19 +533,20 @@ lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream strea
   }
   const int fdt = fwd_dtype(&a->recipe), bdt = bwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
-  // the accumulated outputs are cleared first, so the kernels below run back to back
-  TRY(clear_f32(a->dbias, a->N, st));
-  if (ln) {
-    TRY(clear_f32(a->dgamma, a->K, st));
-    TRY(clear_f32(a->dbeta, a->K, st));
-  }
-  TRY(cast_launch(a->dy, false, a->M, a->N, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->dbias, st, false));
+  OPT(a->gemm_ws, who);
   uint16_t* dln = ln ? a->dln : a->dx;
+  if (a->gemm_ws && a->gemm_ws_bytes < 0) return set_error(LNFP8_ERR_INVALID_ARG, "%s: gemm_ws_bytes < 0", who);
   GemmArgs dg = gemm_args(a->dyq, 0, bdt, a->wq, 1, fdt, a->M, a->K, a->N, m.scale_inv + 0, a->sinv_saved + 1);
   dg.out = dln;
-  TRY(gemm_launch(dg, st));
   GemmArgs wg = gemm_args(a->dyq, 1, bdt, a->xq, 1, fdt, a->N, a->K, a->M, m.scale_inv + 0, a->sinv_saved + 0);
   wg.out = a->dw;
+  const auto flags = share_split_ws({&dg, &wg}, a->gemm_ws, a->gemm_ws_bytes);
+  // the accumulated outputs and the split-K flags are cleared first (one launch)
+  TRY(zero_launch({{a->dbias, a->N * 4}, {ln ? a->dgamma : nullptr, a->K * 4}, {ln ? a->dbeta : nullptr, a->K * 4},
+                   flags},
+                  st));
+  TRY(cast_launch(a->dy, false, a->M, a->N, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->dbias, st, false));
+  TRY(gemm_launch(dg, st));
   TRY(wgrad(wg, a->dw, st));
   if (ln) TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st, false));
   return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
@@ -599,11 +643,20 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   }
   const int fdt = fwd_dtype(&a->recipe), bdt = bwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
-  // the accumulated outputs are cleared first, so the kernels below run back to back
-  TRY(clear_f32(a->db2, a->D, st));
-  TRY(clear_f32(a->db1, a->F, st));
-  TRY(clear_f32(a->dgamma, a->D, st));
-  TRY(clear_f32(a->dbeta, a->D, st));
+  OPT(a->gemm_ws, who);
+  if (a->gemm_ws && a->gemm_ws_bytes < 0) return set_error(LNFP8_ERR_INVALID_ARG, "%s: gemm_ws_bytes < 0", who);
+  // FC2 wgrad: dW2 = dYq^T . Aq
+  GemmArgs w2 = gemm_args(a->dyq, 1, bdt, a->aq, 1, fdt, a->D, a->F, a->M, m.scale_inv + 0, a->sinv_saved + 2);
+  w2.out = a->dw2;
+  // FC1 dgrad: dLN = dHq . W1q
+  GemmArgs d1 = gemm_args(a->dhq, 0, bdt, a->w1q, 1, fdt, a->M, a->D, a->F, m.scale_inv + 1, a->sinv_saved + 1);
+  d1.out = a->dln;
+  // FC1 wgrad: dW1 = dHq^T . LNq
+  GemmArgs w1 = gemm_args(a->dhq, 1, bdt, a->lnq, 1, fdt, a->F, a->D, a->M, m.scale_inv + 1, a->sinv_saved + 0);
+  w1.out = a->dw1;
+  const auto flags = share_split_ws({&w2, &d1, &w1}, a->gemm_ws, a->gemm_ws_bytes);
+  // the accumulated outputs and the split-K flags are cleared first (one launch)
+  TRY(zero_launch({{a->db2, a->D * 4}, {a->db1, a->F * 4}, {a->dgamma, a->D * 4}, {a->dbeta, a->D * 4}, flags}, st));
   TRY(cast_launch(a->dy, false, a->M, a->D, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->db2, st, false));
   // FC2 dgrad with the GELU derivative and the dH cast fused: dH = (dYq . W2q) * s * gelu'(H)
   GemmArgs d2 = gemm_args(a->dyq, 0, bdt, a->w2q, 1, fdt, a->M, a->F, a->D, m.scale_inv + 0, a->sinv_saved + 3);
@@ -616,17 +669,8 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   d2.colsum = a->db1;
   d2.dbg = a->dh_debug;
   TRY(gemm_launch(d2, st));
-  // FC2 wgrad: dW2 = dYq^T . Aq
-  GemmArgs w2 = gemm_args(a->dyq, 1, bdt, a->aq, 1, fdt, a->D, a->F, a->M, m.scale_inv + 0, a->sinv_saved + 2);
-  w2.out = a->dw2;
   TRY(wgrad(w2, a->dw2, st));
-  // FC1 dgrad: dLN = dHq . W1q
-  GemmArgs d1 = gemm_args(a->dhq, 0, bdt, a->w1q, 1, fdt, a->M, a->D, a->F, m.scale_inv + 1, a->sinv_saved + 1);
-  d1.out = a->dln;
   TRY(gemm_launch(d1, st));
-  // FC1 wgrad: dW1 = dHq^T . LNq
-  GemmArgs w1 = gemm_args(a->dhq, 1, bdt, a->lnq, 1, fdt, a->F, a->D, a->M, m.scale_inv + 1, a->sinv_saved + 0);
-  w1.out = a->dw1;
   TRY(wgrad(w1, a->dw1, st));
   TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st, false));
   return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);

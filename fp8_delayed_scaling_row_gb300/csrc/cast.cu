@@ -223,4 +223,44 @@ lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, con
   return cast_dispatch<uint16_t>(grid, dtype, a, b, st);
 }
 
+namespace {
+// Zeroes up to kZeroSpans word ranges in one launch (the accumulated outputs
+// and split-K flags a backward call starts from).
+constexpr int kZeroSpans = 6;
+struct ZeroSpans {
+  uint32_t* p[kZeroSpans];
+  int64_t n[kZeroSpans];  // 32-bit words
+};
+
+__global__ void __launch_bounds__(256) zero_kernel(ZeroSpans z) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = 0; i < kZeroSpans; ++i) {
+    uint32_t* p = z.p[i];
+    const int64_t n = z.n[i];
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += (int64_t)gridDim.x * blockDim.x) p[j] = 0u;
+  }
+}
+}  // namespace
+
+lnfp8_status zero_launch(std::initializer_list<std::pair<void*, int64_t>> spans, cudaStream_t st) {
+  ZeroSpans z = {};
+  int k = 0;
+  int64_t most = 0;
+  for (const auto& sp : spans) {
+    if (!sp.first || sp.second <= 0) continue;
+    if (k == kZeroSpans) return set_error(LNFP8_ERR_INVALID_ARG, "zero_launch: more than %d spans", kZeroSpans);
+    z.p[k] = static_cast<uint32_t*>(sp.first);
+    z.n[k] = (sp.second + 3) / 4;
+    most = z.n[k] > most ? z.n[k] : most;
+    ++k;
+  }
+  if (!k) return LNFP8_OK;
+  const int64_t blocks = (most + 255) / 256 < 152 ? (most + 255) / 256 : 152;
+  LaunchScope ls("zero", st);
+  if (launch_pdl(zero_kernel, dim3((unsigned)blocks), dim3(256), 0, st, z) != cudaSuccess)
+    return check_launch("zero launch");
+  return check_launch("zero");
+}
+
 }  // namespace lnfp8

@@ -25,6 +25,13 @@
 // Operands may be K-major ([rows, K]) or MN-major ([K, rows]); FP8 MN-major
 // operands are native to tcgen05, so the backward GEMMs read dY, A, dH and the
 // LN output in the layout the forward wrote them, with no transposed copies.
+// Split K (bf16-store epilogue only, when the caller provides a workspace):
+// a tile's K range is cut into two halves run as separate work units. Each
+// half owns half of the tile's 32-column chunks: it writes its raw fp32
+// accumulators of the other half's chunks to the workspace and raises a flag,
+// waits (bounded) for the other half's flag, and finishes its own chunks as
+// part_0 + part_1. The result does not depend on which unit finishes first,
+// and both halves share the epilogue work.
 // Every mbarrier wait is bounded: on a timeout the CTA records it in the
 // library's status word, drains its in-flight copies and MMAs, frees its
 // tensor memory and exits.
@@ -94,6 +101,12 @@ struct KParams {
   float* amax_q;
   float* colsum;
   float* dbg;
+  // split K: S (1 or 2) units per tile, kb_per_split K blocks each; ws holds
+  // [num_m2 * 2][num_n] tiles of 128 x BN fp32 (the exchanged chunks); flags
+  // one word per (piece, tile, epilogue warp of a group), zero at launch
+  int splits, kb_per_split;
+  float* ws;
+  unsigned* flags;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -412,9 +425,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const int rank = CL == 2 ? (int)cluster_rank() : 0;
   const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
   const int num_m2 = (p.num_m + CL - 1) / CL;
-  const int num_units = num_m2 * p.num_n;
-  auto unit_m = [&](int u) { return (u % num_m2) * CL + rank; };
-  auto unit_n = [&](int u) { return u / num_m2; };
+  const int S = p.splits;
+  const int num_units = num_m2 * p.num_n * S;
+  // unit u: tile u / S (M pair fastest), K piece u % S
+  auto unit_m = [&](int u) { return ((u / S) % num_m2) * CL + rank; };
+  auto unit_n = [&](int u) { return (u / S) / num_m2; };
+  auto unit_kb0 = [&](int u) { return (u % S) * p.kb_per_split; };
+  auto unit_kb1 = [&](int u) { return min(p.num_kb, (u % S + 1) * p.kb_per_split); };
   constexpr uint16_t kPair = (1u << CL) - 1u;
 
   if (warp == 0) {
@@ -426,7 +443,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       bool ok = true;
       for (int u = cid; u < num_units && ok; u += ncl) {
         const int m_blk = unit_m(u), n_blk = unit_n(u);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int kb_end = unit_kb1(u);
+        for (int kb = unit_kb0(u); kb < kb_end; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
           const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
@@ -482,14 +500,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int kb_beg = unit_kb0(u), kb_end = unit_kb1(u);
+        for (int kb = kb_beg; kb < kb_end; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t b_base = a_base + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
-            const uint32_t accum = (kb | kk) != 0;
+            const uint32_t accum = (kb != kb_beg) || kk != 0;
             const uint64_t ad = A_MN ? make_desc(a_base + kk * 32 * 128, 1024, 1024) : make_desc(a_base + kk * 32, 16, 1024);
             if constexpr (TWO) {
               // 256 x BN x 32 over the pair: A rows and B halves from both CTAs
@@ -564,15 +583,78 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if constexpr (EPI == EPI_DGELU) {
       if (u0 < num_units) issue_h(u0, 0);
     }
+    // Split K (two pieces): piece q of a tile owns the chunks ch with ch % 2 == q.
+    // Each piece spills the chunks the other owns to the workspace and raises
+    // its flag, then waits for the other's flag and finishes its own chunks as
+    // part_0 + part_1. A chunk is one warp's 32 x 32 fp32 block, stored
+    // lane-contiguous (coalesced); each (tile, chunk) is written once.
+    const int gw = ew & 7;  // warp within its group
+    auto slot_ptr = [&](int m_blk, int n_blk, int ch) {
+      const int64_t t = (int64_t)m_blk * p.num_n + n_blk;
+      return reinterpret_cast<uint4*>(p.ws + t * (int64_t)(BM * BN)) + ((gw * CHUNKS + ch) * 8) * 32 + lane;
+    };
+    // flag of the piece q's spill of this warp's chunks of a tile
+    auto flag_ptr = [&](int q, int m_blk, int n_blk) {
+      return p.flags + (((int64_t)q * (num_m2 * CL) + m_blk) * p.num_n + n_blk) * 8 + gw;
+    };
     for (int u = u0; u < num_units; u += 2 * ncl) {
       const int m_blk = unit_m(u), n_blk = unit_n(u);
+      const int sp = u % S;
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
       const bool row_ok = m < p.M;
       bool aborted = false;
+      if constexpr (EPI == EPI_STORE) {
+        if (S > 1) {
 #pragma unroll 1
-      for (int ch = 0; ch < CHUNKS; ++ch) {
+          for (int ch = 1 - sp; ch < CHUNKS; ch += 2) {
+            uint32_t rr[32];
+            tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * HALF_COLS + ch * 32), rr);
+            uint4* dst = slot_ptr(m_blk, n_blk, ch);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) __stcg(dst + j * 32, make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]));
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicExch(flag_ptr(sp, m_blk, n_blk), 1u);
+          // wait (lane 0, bounded) for the other piece's spill of this warp's chunks
+          const unsigned* f = flag_ptr(1 - sp, m_blk, n_blk);
+          int ready = 1;
+          if (lane == 0) {
+            const uint64_t t0 = globaltimer();
+            for (uint32_t it = 0;; ++it) {
+              unsigned v;
+              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+              if (v) break;
+              if ((it & 15) == 15) {
+                if (*abort_flag) { ready = 0; break; }
+                if (globaltimer() - t0 > 1000000000ull) {
+                  *abort_flag = 1;
+                  atomicOr(&g_status, kStatusTimeout);
+                  ready = 0;
+                  break;
+                }
+              }
+            }
+          }
+          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+          if (!ready) break;
+          // every lane acquires the flag (already set); lane 0 then leaves it
+          // zero for the next GEMM that uses this workspace
+          {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+          }
+          __syncwarp();
+          if (lane == 0) *const_cast<unsigned*>(f) = 0u;
+        }
+      }
+      // with two K pieces this unit finishes the chunks it owns, the last of them being CHUNKS - 2 + sp
+      const int ch_step = S > 1 ? 2 : 1;
+      const int ch_last = S > 1 ? CHUNKS - 2 + sp : CHUNKS - 1;
+#pragma unroll 1
+      for (int ch = S > 1 ? sp : 0; ch < CHUNKS; ch += ch_step) {
         const int col0 = half * HALF_COLS + ch * 32;
         const int64_t n0 = (int64_t)n_blk * BN + col0;
         uint32_t rr[32];
@@ -582,10 +664,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (ch == CHUNKS - 1 && !combiner) {
+        if (ch == ch_last && !combiner) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) release_acc();
+        }
+        if constexpr (EPI == EPI_STORE) {
+          if (S > 1) {  // part_0 + part_1 (fp32 addition commutes: either piece gets the same bits)
+            const uint4* src = slot_ptr(m_blk, n_blk, ch);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 w = __ldcg(src + j * 32);
+              rr[4 * j] = __float_as_uint(__uint_as_float(rr[4 * j]) + __uint_as_float(w.x));
+              rr[4 * j + 1] = __float_as_uint(__uint_as_float(rr[4 * j + 1]) + __uint_as_float(w.y));
+              rr[4 * j + 2] = __float_as_uint(__uint_as_float(rr[4 * j + 2]) + __uint_as_float(w.z));
+              rr[4 * j + 3] = __float_as_uint(__uint_as_float(rr[4 * j + 3]) + __uint_as_float(w.w));
+            }
+          }
         }
         uint4 hin[4];
         if constexpr (EPI == EPI_DGELU) {
@@ -867,8 +962,10 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
       max_clusters = num_sms() / CL;
     }
   }
-  const int units = ((kp.num_m + CL - 1) / CL) * kp.num_n;
+  const int units = ((kp.num_m + CL - 1) / CL) * kp.num_n * kp.splits;
   const int clusters = units < max_clusters ? units : max_clusters;
+  // a split-K reducer waits for the tile's later pieces, which must not queue behind it
+  if (kp.splits > clusters) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: %d K splits on %d clusters", kp.splits, clusters);
   cfg.gridDim = dim3(clusters * CL);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   static const char* kind = EPI == EPI_GELU ? "gemm_gelu" : EPI == EPI_DGELU ? "gemm_dgelu" :
@@ -896,15 +993,56 @@ lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st) {
   return check_launch("lnfp8_selftest_timeout");
 }
 
+// Tile width and K splits for one GEMM. Costs are counted in K blocks of one
+// 2-SM tile: ceil(units / clusters) rounds of K/S blocks each, plus for S > 1
+// about four blocks' time for the exchange of the halves' partial products.
+// Splitting is considered for the bf16-store epilogue with a workspace only,
+// when all units fit in one round (the exchange then overlaps no other
+// tile's work, so it is paid once), and taken when it saves more than a tenth.
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split) {
+  GemmPlan pl;
+  const int64_t num_m = (M + BM - 1) / BM;
+  const int64_t num_m2 = (num_m + CL - 1) / CL;
+  const int64_t num_kb = (K + BK - 1) / BK;
+  const int64_t clusters = num_sms() / CL > 0 ? num_sms() / CL : 1;
+  const int64_t tiles = num_m2 * ((N + 255) / 256);
+  pl.bn = 256;
+  pl.splits = 1;
+  if (epi == EPI_STORE && may_split && tiles > 0 && num_kb >= 8) {
+    auto cost = [&](int64_t sp) {
+      const int64_t kbs = (num_kb + sp - 1) / sp;
+      return ((tiles * sp + clusters - 1) / clusters) * kbs + 4 * (sp - 1);
+    };
+    int best = 1;
+    for (int sp = 2; sp <= 2; ++sp) {  // the epilogue exchanges chunks between two pieces
+      const int64_t kbs = (num_kb + sp - 1) / sp;
+      if (kbs < 4 || (sp - 1) * kbs >= num_kb || tiles * sp > clusters) continue;  // non-empty pieces, one round
+      if (cost(sp) < cost(best)) best = sp;
+    }
+    if (best > 1 && 10 * cost(best) < 9 * cost(1)) pl.splits = best;
+  }
+  // without a split, 128-wide single-SM tiles when 256-wide ones leave most SMs idle
+  if (pl.splits == 1 && epi == EPI_STORE && num_m * ((N + 255) / 256) < (int64_t)num_sms()) pl.bn = 128;
+  pl.kb_per_split = (int)((num_kb + pl.splits - 1) / pl.splits);
+  const int64_t rows = num_m2 * CL, cols = (N + pl.bn - 1) / pl.bn;
+  pl.flag_bytes = pl.splits > 1 ? ((pl.splits * rows * cols * 8 * 4 + 255) / 256) * 256 : 0;
+  pl.slot_bytes = pl.splits > 1 ? rows * cols * (int64_t)(BM * pl.bn) * 4 : 0;
+  pl.ws_bytes = pl.flag_bytes + pl.slot_bytes;
+  return pl;
+}
+
 lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return LNFP8_OK;
   if (g.M > 0x7FFFFFFF || g.N > 0x7FFFFFFF || g.K > 0x7FFFFFFF)
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm: dimension above 2^31");
   const bool a_mn = g.a_layout == 1, b_mn = g.b_layout == 1;
-  // Tile width: 256 columns unless that leaves most SMs idle.
   const int64_t num_m = (g.M + BM - 1) / BM;
-  int bn = 256;
-  if (g.epi == EPI_STORE && num_m * ((g.N + 255) / 256) < (int64_t)num_sms()) bn = 128;
+  GemmPlan pl = gemm_plan(g.M, g.N, g.K, g.epi, g.ws != nullptr);
+  // the slots start after the flag area, which the caller may size for several GEMMs
+  const int64_t flag_off = g.ws_flag_bytes > 0 ? g.ws_flag_bytes : pl.flag_bytes;
+  if (pl.splits > 1 && (flag_off < pl.flag_bytes || flag_off % 256 || g.ws_bytes < flag_off + pl.slot_bytes))
+    pl = gemm_plan(g.M, g.N, g.K, g.epi, false);
+  const int bn = pl.bn;
   const int64_t num_n = (g.N + bn - 1) / bn;
   if (num_m * num_n > 0x7FFFFFFF) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm: too many tiles");
 
@@ -943,6 +1081,10 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.amax_q = g.amax_q;
   kp.colsum = g.colsum;
   kp.dbg = g.dbg;
+  kp.splits = pl.splits;
+  kp.kb_per_split = pl.kb_per_split;
+  kp.flags = pl.splits > 1 ? reinterpret_cast<unsigned*>(g.ws) : nullptr;
+  kp.ws = pl.splits > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g.ws) + flag_off) : nullptr;
 
   if (g.epi == EPI_STORE) {
     if (bn == 256) return launch_layouts<256, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, em, kp, st);

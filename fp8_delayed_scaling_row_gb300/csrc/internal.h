@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
+#include <utility>
+
 #include "lnfp8.h"
 
 namespace lnfp8 {
@@ -18,6 +21,9 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
                          float* colsum, cudaStream_t st, bool clear_colsum = true);
 
 // Two bf16 tensors cast in one launch (the weights of a LayerNormMLP).
+// Zeroes each (pointer, bytes) span (bytes a multiple of 4; NULL or 0 skipped), one launch.
+lnfp8_status zero_launch(std::initializer_list<std::pair<void*, int64_t>> spans, cudaStream_t st);
+
 lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
                           uint8_t* out0, const uint16_t* in1, int64_t rows1, int64_t cols1, const float* scale1,
                           float* amax1, uint8_t* out1, int dtype, cudaStream_t st);
@@ -56,7 +62,24 @@ struct GemmArgs {
   float* amax_q;
   float* colsum;         // [N] fp32 (DGELU), accumulated: the caller clears it
   float* dbg;            // optional [M, N] fp32 pre-cast value
+  // optional split-K workspace (bf16-store epilogue): a flag area of
+  // ws_flag_bytes (0: the plan's own flag_bytes; a multiple of 256 at least
+  // that large), which must be zero at launch and is left zero, then the
+  // partial-product slots
+  void* ws = nullptr;
+  int64_t ws_bytes = 0;
+  int64_t ws_flag_bytes = 0;
 };
+
+struct GemmPlan {
+  int bn;             // tile width (256: 2-SM pair tiles; 128: single-SM)
+  int splits;         // K pieces per tile
+  int kb_per_split;   // K blocks of 128 per piece
+  int64_t flag_bytes; // flag words this GEMM needs at the start of the workspace
+  int64_t slot_bytes; // partial-product slots after the flag area
+  int64_t ws_bytes;   // flag_bytes + slot_bytes (0 without a split)
+};
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split);
 
 lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st);
 lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st);

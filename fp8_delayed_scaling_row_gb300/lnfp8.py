@@ -31,8 +31,8 @@ EXPORTED = [
     "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_launch_count",
     "lnfp8_profile_enable", "lnfp8_profile_sample", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
     "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
-    "ln_linear_bwd_noalloc", "ln_mlp_fwd",
-    "ln_mlp_bwd",
+    "ln_linear_bwd_noalloc", "ln_mlp_fwd", "ln_mlp_bwd", "lnfp8_gemm_workspace_size",
+    "lnfp8_ln_linear_bwd_workspace_size", "lnfp8_ln_mlp_bwd_workspace_size",
 ]
 
 
@@ -67,7 +67,7 @@ class CLnLinearBwd(C.Structure):
     _fields_ = [("M", _I64), ("K", _I64), ("N", _I64), ("dy", _P), ("x", _P), ("gamma", _P), ("xq", _P),
                 ("wq", _P), ("mu", _P), ("rsigma", _P), ("sinv_saved", _P), ("dx", _P), ("dw", _P), ("dbias", _P),
                 ("dgamma", _P), ("dbeta", _P), ("dyq", _P), ("dln", _P), ("meta", CMeta), ("recipe", CRecipe),
-                ("defer_update", C.c_int)]
+                ("defer_update", C.c_int), ("gemm_ws", _P), ("gemm_ws_bytes", _I64)]
 
 
 class CLnMlpFwd(C.Structure):
@@ -82,7 +82,7 @@ class CLnMlpBwd(C.Structure):
                 ("mu", _P), ("rsigma", _P), ("w1q", _P), ("w2q", _P), ("h", _P), ("aq", _P), ("sinv_saved", _P),
                 ("dx", _P), ("dgamma", _P), ("dbeta", _P), ("dw1", _P), ("db1", _P), ("dw2", _P), ("db2", _P),
                 ("dyq", _P), ("dhq", _P), ("dln", _P), ("meta", CMeta), ("recipe", CRecipe),
-                ("defer_update", C.c_int), ("dh_debug", _P)]
+                ("defer_update", C.c_int), ("dh_debug", _P), ("gemm_ws", _P), ("gemm_ws_bytes", _I64)]
 
 
 def _sig(name, args, res=C.c_int):
@@ -108,7 +108,11 @@ _c_update = _sig("amax_history_update", [C.POINTER(CMeta), C.POINTER(CRecipe), C
 _c_quant = _sig("fp8_quantize", [_P, C.c_int, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P])
 _c_ln_fwd = _sig("ln_fwd_cast", [_P, _P, _P, C.c_float, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P, _P])
 _c_ln_bwd = _sig("ln_bwd", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P])
-_c_gemm = _sig("fp8_gemm", [_P, C.c_int, C.c_int, _P, C.c_int, C.c_int, _I64, _I64, _I64, _P, _P, _P, _P, _P])
+_c_gemm = _sig("fp8_gemm", [_P, C.c_int, C.c_int, _P, C.c_int, C.c_int, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I64,
+                            _P])
+_c_gemm_ws = _sig("lnfp8_gemm_workspace_size", [_I64, _I64, _I64], C.c_int64)
+_c_lin_bwd_ws = _sig("lnfp8_ln_linear_bwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
+_c_mlp_bwd_ws = _sig("lnfp8_ln_mlp_bwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_lin_fwd = _sig("ln_linear_fwd", [C.POINTER(CLnLinearFwd), _P])
 _c_lin_bwd = _sig("ln_linear_bwd", [C.POINTER(CLnLinearBwd), _P])
 _c_lin_bwd_noalloc = _sig("ln_linear_bwd_noalloc", [C.POINTER(CLnLinearBwd), _P])
@@ -266,12 +270,31 @@ def ln_bwd(dy, x, gamma, mu, rsigma, *, dx=None, dgamma=None, dbeta=None, stream
     return dx, dgamma, dbeta
 
 
+def gemm_workspace_size(M, N, K) -> int:
+    """Bytes of workspace with which fp8_gemm splits K for this shape (0: it would not)."""
+    return int(_c_gemm_ws(M, N, K))
+
+
+def ln_linear_bwd_workspace_size(M, K, N) -> int:
+    return int(_c_lin_bwd_ws(M, K, N))
+
+
+def ln_mlp_bwd_workspace_size(M, D, F) -> int:
+    return int(_c_mlp_bwd_ws(M, D, F))
+
+
+def _ws(nbytes, device):
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
+
+
 def fp8_gemm(a, a_layout, a_dtype, b, b_layout, b_dtype, M, N, K, sinv_a, sinv_b, *, bias=None, out=None,
-             stream=None):
-    """out[M, N] bf16 = (A . B^T) * sinv_a * sinv_b + bias; layouts as in the C ABI."""
+             workspace=None, stream=None):
+    """out[M, N] bf16 = (A . B^T) * sinv_a * sinv_b + bias; layouts as in the C ABI. With a
+    uint8 workspace tensor of gemm_workspace_size(M, N, K) bytes the GEMM may split K."""
     out = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=b.device)
     _check(_c_gemm(_ptr(a), a_layout, a_dtype, _ptr(b), b_layout, b_dtype, M, N, K, _ptr(sinv_a), _ptr(sinv_b),
-                   _ptr(bias), _ptr(out), _stream(stream)))
+                   _ptr(bias), _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                   _stream(stream)))
     return out
 
 
@@ -323,14 +346,16 @@ class LinearGrads:
     dbeta: torch.Tensor | None
     dyq: torch.Tensor
     dln: torch.Tensor | None
+    gemm_ws: torch.Tensor | None = None  # split-K workspace of the GEMMs (None: unsplit)
 
 
-def linear_grads(M, K, N, *, ln=True, bias=True, device="cuda") -> LinearGrads:
+def linear_grads(M, K, N, *, ln=True, bias=True, split_k=True, device="cuda") -> LinearGrads:
     return LinearGrads(dx=_e((M, K), torch.bfloat16, device), dw=_e((N, K), torch.bfloat16, device),
                        dbias=_e((N,), torch.float32, device) if bias else None,
                        dgamma=_e((K,), torch.float32, device) if ln else None,
                        dbeta=_e((K,), torch.float32, device) if ln else None,
-                       dyq=_e((M, N), torch.uint8, device), dln=_e((M, K), torch.bfloat16, device) if ln else None)
+                       dyq=_e((M, N), torch.uint8, device), dln=_e((M, K), torch.bfloat16, device) if ln else None,
+                       gemm_ws=_ws(ln_linear_bwd_workspace_size(M, K, N), device) if split_k else None)
 
 
 def ln_linear_bwd(dy, x, gamma, ctx: LinearCtx, meta: ScalingMeta, recipe: Recipe, *, grads: LinearGrads | None = None,
@@ -342,7 +367,8 @@ def ln_linear_bwd(dy, x, gamma, ctx: LinearCtx, meta: ScalingMeta, recipe: Recip
                      mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma), sinv_saved=_ptr(ctx.sinv_saved), dx=_ptr(g.dx),
                      dw=_ptr(g.dw), dbias=_ptr(g.dbias), dgamma=_ptr(g.dgamma), dbeta=_ptr(g.dbeta),
                      dyq=_ptr(g.dyq), dln=_ptr(g.dln), meta=meta.c(), recipe=recipe.c(),
-                     defer_update=int(defer_update))
+                     defer_update=int(defer_update), gemm_ws=_ptr(g.gemm_ws),
+                     gemm_ws_bytes=g.gemm_ws.numel() if g.gemm_ws is not None else 0)
     _check(_c_lin_bwd(C.byref(a), _stream(stream)))
     return g
 
@@ -415,15 +441,17 @@ class MlpGrads:
     dhq: torch.Tensor
     dln: torch.Tensor
     dh_debug: torch.Tensor | None = None
+    gemm_ws: torch.Tensor | None = None  # split-K workspace of the GEMMs (None: unsplit)
 
 
-def mlp_grads(M, D, F, *, bias=True, device="cuda", debug=False) -> MlpGrads:
+def mlp_grads(M, D, F, *, bias=True, split_k=True, device="cuda", debug=False) -> MlpGrads:
     return MlpGrads(dx=_e((M, D), torch.bfloat16, device), dgamma=_e((D,), torch.float32, device),
                     dbeta=_e((D,), torch.float32, device), dw1=_e((F, D), torch.bfloat16, device),
                     db1=_e((F,), torch.float32, device) if bias else None, dw2=_e((D, F), torch.bfloat16, device),
                     db2=_e((D,), torch.float32, device) if bias else None, dyq=_e((M, D), torch.uint8, device),
                     dhq=_e((M, F), torch.uint8, device), dln=_e((M, D), torch.bfloat16, device),
-                    dh_debug=_e((M, F), torch.float32, device) if debug else None)
+                    dh_debug=_e((M, F), torch.float32, device) if debug else None,
+                    gemm_ws=_ws(ln_mlp_bwd_workspace_size(M, D, F), device) if split_k else None)
 
 
 def ln_mlp_bwd(dy, x, gamma, ctx: MlpCtx, meta: ScalingMeta, recipe: Recipe, *, grads: MlpGrads | None = None,
@@ -436,6 +464,7 @@ def ln_mlp_bwd(dy, x, gamma, ctx: MlpCtx, meta: ScalingMeta, recipe: Recipe, *, 
                   sinv_saved=_ptr(ctx.sinv_saved), dx=_ptr(g.dx), dgamma=_ptr(g.dgamma), dbeta=_ptr(g.dbeta),
                   dw1=_ptr(g.dw1), db1=_ptr(g.db1), dw2=_ptr(g.dw2), db2=_ptr(g.db2), dyq=_ptr(g.dyq),
                   dhq=_ptr(g.dhq), dln=_ptr(g.dln), meta=meta.c(), recipe=recipe.c(),
-                  defer_update=int(defer_update), dh_debug=_ptr(g.dh_debug))
+                  defer_update=int(defer_update), dh_debug=_ptr(g.dh_debug), gemm_ws=_ptr(g.gemm_ws),
+                  gemm_ws_bytes=g.gemm_ws.numel() if g.gemm_ws is not None else 0)
     _check(_c_mlp_bwd(C.byref(a), _stream(stream)))
     return g

@@ -201,10 +201,23 @@ lnfp8_status ln_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma
  *   a_layout 0: A stored [M, K] (K contiguous); 1: A stored [K, M].
  *   b_layout 0: B stored [N, K] (K contiguous); 1: B stored [K, N].
  *   a_dtype, b_dtype: lnfp8_dtype. bias: [N] bf16 or NULL.
- * N and K must be multiples of 16, and M too when a_layout = 1. */
+ * N and K must be multiples of 16, and M too when a_layout = 1.
+ * workspace: optional device buffer of workspace_bytes (16-byte aligned), or
+ * NULL. When it holds at least lnfp8_gemm_workspace_size(M, N, K) bytes and
+ * that size is not 0, the GEMM cuts K into pieces that run on separate SMs
+ * (split K) and adds the pieces' fp32 partial products in a fixed order, so
+ * the result is deterministic. The library zeroes the part it needs at the
+ * start of the call; the buffer is the caller's and must not be used by
+ * anything else until the call has completed on the stream. */
 lnfp8_status fp8_gemm(const uint8_t* A, int a_layout, int a_dtype, const uint8_t* B, int b_layout,
                       int b_dtype, int64_t M, int64_t N, int64_t K, const float* sinv_a,
-                      const float* sinv_b, const uint16_t* bias, uint16_t* out, lnfp8_stream stream);
+                      const float* sinv_b, const uint16_t* bias, uint16_t* out, void* workspace,
+                      int64_t workspace_bytes, lnfp8_stream stream);
+
+/* Bytes of workspace with which fp8_gemm would split K for this shape on the
+ * current device; 0 when it would not split (then no workspace is used), -1
+ * for negative sizes. */
+int64_t lnfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* LayerNormLinear / Linear ---------------------------------------------- */
 
@@ -249,6 +262,8 @@ typedef struct {
   lnfp8_meta meta;            /* backward state, n = 1 */
   lnfp8_recipe recipe;
   int defer_update;
+  void* gemm_ws;              /* optional split-K workspace (see lnfp8_ln_linear_bwd_workspace_size), or NULL */
+  int64_t gemm_ws_bytes;
 } lnfp8_ln_linear_bwd_args;
 
 /* LayerNormLinear forward (TE tutorial code block 1: te.LayerNormLinear(H, 3H);
@@ -263,6 +278,14 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* args, lnfp8_stream st
  * dw = (dyq^T . xq) * (gscale_inv[0] * sinv_saved[0]); dx = LN backward of dln
  * (dx = dln without LayerNorm); then the backward state update. */
 lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* args, lnfp8_stream stream);
+
+/* Bytes of args->gemm_ws with which ln_linear_bwd splits K in its GEMMs
+ * (the dgrad [M, K] and the wgrad [N, K] over M tokens); 0 when neither
+ * would split, -1 for negative sizes. A smaller or NULL workspace is valid
+ * and runs the GEMMs unsplit. The library zeroes what it uses at the start
+ * of each call; the results are the same with and without it up to fp32
+ * summation order. */
+int64_t lnfp8_ln_linear_bwd_workspace_size(int64_t M, int64_t K, int64_t N);
 
 /* LayerNormLinear backward without caller-provided scratch. The pages have no
  * counterpart of this entry point. It is for callers that cannot allocate
@@ -341,6 +364,8 @@ typedef struct {
   lnfp8_recipe recipe;
   int defer_update;
   float* dh_debug;        /* optional [M, F] fp32 pre-cast dH */
+  void* gemm_ws;          /* optional split-K workspace (see lnfp8_ln_mlp_bwd_workspace_size), or NULL */
+  int64_t gemm_ws_bytes;
 } lnfp8_ln_mlp_bwd_args;
 
 /* LayerNormMLP forward (TE tutorial code block 1: te.LayerNormMLP(H, 4H);
@@ -358,6 +383,12 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* args, lnfp8_stream stream);
  *   dln = (dhq . w1q) * gsinv[1]*sinv[1]; dw1 = (dhq^T . lnq) * gsinv[1]*sinv[0];
  *   dx, dgamma, dbeta = LN backward of dln; then the backward state update. */
 lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* args, lnfp8_stream stream);
+
+/* Bytes of args->gemm_ws with which ln_mlp_bwd splits K in its plain-store
+ * GEMMs (dW2 [D, F] and dW1 [F, D] over M tokens, dLN [M, D] over F); 0 when
+ * none would split, -1 for negative sizes. As for ln_linear_bwd, a smaller or
+ * NULL workspace runs them unsplit. */
+int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F);
 
 #ifdef __cplusplus
 }

@@ -95,9 +95,23 @@ def test_quantize_and_gemm_reject_bad_shapes(lib):
     assert lib._c_quant(FAKE, 0, 10, 32, 3, FAKE, FAKE, FAKE, None, None, None) == 1
     assert lib._c_quant(FAKE, 0, 10, 32, 0, None, FAKE, FAKE, None, None, None) == 1
     # A stored [K, M] needs M % 16 == 0
-    assert lib._c_gemm(FAKE, 1, 0, FAKE, 0, 0, 100, 32, 32, FAKE, FAKE, None, FAKE, None) == 2
-    assert lib._c_gemm(FAKE, 0, 0, FAKE, 2, 0, 100, 32, 32, FAKE, FAKE, None, FAKE, None) == 1
-    assert lib._c_gemm(FAKE, 0, 0, FAKE, 0, 0, 100, 32, 0, FAKE, FAKE, None, FAKE, None) == 2
+    assert lib._c_gemm(FAKE, 1, 0, FAKE, 0, 0, 100, 32, 32, FAKE, FAKE, None, FAKE, None, 0, None) == 2
+    assert lib._c_gemm(FAKE, 0, 0, FAKE, 2, 0, 100, 32, 32, FAKE, FAKE, None, FAKE, None, 0, None) == 1
+    assert lib._c_gemm(FAKE, 0, 0, FAKE, 0, 0, 100, 32, 0, FAKE, FAKE, None, FAKE, None, 0, None) == 2
+    # a misaligned workspace and a negative workspace size are rejected before anything runs
+    assert lib._c_gemm(FAKE, 0, 0, FAKE, 0, 0, 100, 32, 32, FAKE, FAKE, None, FAKE, FAKE + 4, 1 << 20, None) == 1
+    assert lib._c_gemm(FAKE, 0, 0, FAKE, 0, 0, 100, 32, 32, FAKE, FAKE, None, FAKE, FAKE, -1, None) == 1
+
+
+def test_workspace_size_queries(lib):
+    """The size queries need no GPU; negative sizes give -1 and an empty problem needs none."""
+    assert lib.gemm_workspace_size(-1, 32, 32) == -1
+    assert lib.ln_linear_bwd_workspace_size(16, -1, 32) == -1
+    assert lib.ln_mlp_bwd_workspace_size(16, 32, -5) == -1
+    assert lib.gemm_workspace_size(0, 0, 0) == 0
+    for f in (lib.gemm_workspace_size, lib.ln_linear_bwd_workspace_size, lib.ln_mlp_bwd_workspace_size):
+        n = f(8192, 768, 3072)
+        assert n >= 0 and n % 256 == 0
 
 
 def test_state_update_rejects_bad_arguments(lib):

@@ -218,6 +218,64 @@ def test_gemm_exact_integer_problems_on_the_pair_tiles(L, a_layout, b_layout, M,
     assert np.array_equal(host(out), ogemm.bf16_to_f32(ogemm.to_bf16_bits(ref)).astype(np.float64))
 
 
+@pytest.mark.parametrize("a_layout,b_layout", [(1, 1), (0, 1), (0, 0), (1, 0)])
+@pytest.mark.parametrize("M,N,K", [
+    (768, 3072, 8192),   # the FC2 weight gradient of the 768 -> 3072 MLP over 8192 tokens
+    (520, 2832, 8208),   # ragged M (odd tile count: the pair's spare tile), N and K
+    (256, 256, 8192),    # one tile
+    (208, 240, 4112),    # one ragged tile, the second piece with the ragged K block
+    (3072, 768, 8192),   # the FC1 weight gradient
+])
+def test_gemm_split_k_exact_integer_problems(L, a_layout, b_layout, M, N, K):
+    """With a workspace the GEMM cuts K into pieces on separate SMs and adds the
+    pieces' fp32 partials in order: integer problems stay exact, and the result
+    equals the unsplit GEMM's bit for bit. The workspace's flags are left zero."""
+    if a_layout == 1 and M % 16:
+        pytest.skip("A stored [K, M] needs M % 16 == 0")
+    nbytes = L.gemm_workspace_size(M, N, K)
+    assert nbytes > 0, "this shape is meant to split"
+    rng = np.random.default_rng(M + N + K + 3 * a_layout + b_layout)
+    a = _int_codes((M, K), ofp8.E4M3, rng)
+    b = _int_codes((N, K), ofp8.E5M2, rng)
+    bias = synth.f32_to_bf16_bits(rng.integers(-8, 8, N).astype(np.float32))
+    at = torch.from_numpy(np.ascontiguousarray(a if a_layout == 0 else a.T)).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(b if b_layout == 0 else b.T)).cuda()
+    ws = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda")  # the call zeroes what it needs
+    args = (at, a_layout, 0, bt, b_layout, 1, M, N, K, _scalar(0.25), _scalar(0.5))
+    split = L.fp8_gemm(*args, bias=bf16_dev(bias), workspace=ws)
+    whole = L.fp8_gemm(*args, bias=bf16_dev(bias))
+    small = L.fp8_gemm(*args, bias=bf16_dev(bias), workspace=ws[: nbytes - 16])  # too small: runs unsplit
+    L.sync_status()
+    ref = ogemm.fp8_gemm(a, ofp8.E4M3, b, ofp8.E5M2, 0.25, 0.5, synth.bf16_bits_to_f32(bias))
+    assert np.array_equal(host(split), ogemm.bf16_to_f32(ogemm.to_bf16_bits(ref)).astype(np.float64))
+    assert torch.equal(split, whole) and torch.equal(small, whole)
+    # layout: flag words, then one 128 x 256 fp32 tile per (128-row tile pair slot, 256-column tile)
+    rows = -(-(-(-M // 128)) // 2) * 2
+    slot_bytes = rows * (-(-N // 256)) * 128 * 256 * 4
+    flag_bytes = nbytes - slot_bytes
+    w = ws.cpu().numpy()
+    assert 0 < flag_bytes and flag_bytes % 256 == 0
+    assert not w[:flag_bytes].any(), "the flags are left zero"
+    assert (w[flag_bytes:] != 0xAB).mean() > 0.5, "the exchanged partials went to the slots"
+
+
+def test_gemm_split_k_random_codes_within_tolerance(L):
+    M, N, K = 768, 3072, 8192
+    rng = np.random.default_rng(7)
+    a = ofp8.encode(rng.standard_normal((M, K)).astype(np.float32) * 30, ofp8.E5M2)
+    b = ofp8.encode(rng.standard_normal((N, K)).astype(np.float32) * 40, ofp8.E4M3)
+    sa, sb = np.float32(1 / 30.0), np.float32(1 / 40.0)
+    at = torch.from_numpy(np.ascontiguousarray(a.T)).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(b.T)).cuda()
+    ws = torch.zeros(L.gemm_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+    out = L.fp8_gemm(at, 1, 1, bt, 1, 0, M, N, K, _scalar(float(sa)), _scalar(float(sb)), workspace=ws)
+    L.sync_status()
+    ref = ogemm.fp8_gemm(a, ofp8.E5M2, b, ofp8.E4M3, sa, sb)
+    got = host(out)
+    assert rel_fro(got, ref) < 1e-2
+    assert np.abs(got - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+
+
 @pytest.mark.parametrize("a_layout,b_layout", [(0, 0), (0, 1), (1, 1)])
 def test_gemm_random_codes_within_tolerance(L, a_layout, b_layout):
     M, N, K = 384, 512, 3072

@@ -293,7 +293,8 @@ def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profile
     direct = L.profile_collect()
     L.profile_enable(False)
     L.sync_status()
-    assert sum(n for _, n in direct.values()) == 12 and all(ms > 0 for ms, _ in direct.values())
+    # forward: weight casts, LayerNorm, FC1, FC2, state; backward: clears, dY cast, four GEMMs, LayerNorm, state
+    assert sum(n for _, n in direct.values()) == 13 and all(ms > 0 for ms, _ in direct.values())
 
     fm1, bm1, ctx1, g1 = make()
     y1 = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
@@ -320,3 +321,32 @@ def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profile
     for m0, m1 in [(fm0, fm1), (bm0, bm1)]:
         for name in ("scale", "scale_inv", "amax_history"):
             assert torch.equal(getattr(m0, name), getattr(m1, name)), name
+
+
+@pytest.mark.parametrize("M,D,F", [(8192, 768, 3072), (1000, 256, 1024)])
+def test_mlp_backward_split_k_is_deterministic_and_matches_unsplit(L, M, D, F):
+    """The backward GEMMs share one split-K workspace, one after another. Two runs
+    with it give identical bits, and the same results as the unsplit GEMMs up to
+    fp32 summation order (a bf16 ulp on a few elements)."""
+    p = {k: bf16_dev(v) for k, v in synth.mlp_params(D, F, bias_std=0.02, seed=3).items()}
+    x = bf16_dev(synth.activations(M, D, dist="outliers", seed=3, step=0))
+    dy = bf16_dev(synth.grad(M, D, seed=3, step=0))
+    rec = L.Recipe("hybrid", 4)
+    ctx = L.mlp_ctx(M, D, F)
+    L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], L.ScalingMeta(4, 4), rec, ctx=ctx)
+    runs = []
+    for split in (True, True, False):
+        g = L.mlp_grads(M, D, F, split_k=split)
+        assert (g.gemm_ws is not None) == (split and L.ln_mlp_bwd_workspace_size(M, D, F) > 0)
+        L.ln_mlp_bwd(dy, x, p["gamma"], ctx, L.ScalingMeta(2, 4), rec, grads=g)
+        L.sync_status()
+        runs.append(g)
+    names = ("dx", "dw1", "dw2", "dln", "dgamma", "dbeta", "db1", "db2")
+    for k in ("dx", "dw1", "dw2", "dln"):
+        assert torch.equal(getattr(runs[0], k), getattr(runs[1], k)), k
+    for k in names:
+        a, b = host(getattr(runs[0], k)), host(getattr(runs[2], k))
+        assert rel_fro(a, b) < 1e-4, (k, rel_fro(a, b))
+    for k in ("dw1", "dw2", "dln"):
+        a, b = host(getattr(runs[0], k)), host(getattr(runs[2], k))
+        assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(b).max(), k
