@@ -658,6 +658,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int col0 = half * HALF_COLS + ch * 32;
         const int64_t n0 = (int64_t)n_blk * BN + col0;
         uint32_t rr[32];
+        uint4 bias8[4];  // this chunk's bias, requested before the tensor-memory load
+        if constexpr (EPI != EPI_DGELU) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            bias8[g] = p.bias && n0 + g * 8 < p.N ? __ldg(reinterpret_cast<const uint4*>(p.bias + n0 + g * 8))
+                                                   : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (p.num_kb > 0) {
           tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + col0), rr);
         } else {
@@ -709,8 +716,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           for (int i = 0; i < 4; ++i) e2[i] = f2(__uint_as_float(rr[g * 8 + 2 * i]), __uint_as_float(rr[g * 8 + 2 * i + 1]));
           uint64_t b2[4] = {0ull, 0ull, 0ull, 0ull};
           if constexpr (EPI != EPI_DGELU) {
-            if (p.bias && n < p.N) {
-              const uint4 bu = *reinterpret_cast<const uint4*>(p.bias + n);
+            {
+              const uint4 bu = bias8[g];
               b2[0] = bf2_to_f2(bu.x);
               b2[1] = bf2_to_f2(bu.y);
               b2[2] = bf2_to_f2(bu.z);
