@@ -49,6 +49,12 @@ bool pdl_enabled() {
   return on;
 }
 
+// LNFP8_NO_PAIR=1 runs the FC2 data and weight gradients as two launches (for comparison)
+bool pair_disabled() {
+  static const bool off = getenv("LNFP8_NO_PAIR") != nullptr;
+  return off;
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -190,9 +196,10 @@ lnfp8_status finish_state(const lnfp8_meta* m, const lnfp8_recipe* r, int dt, fl
 // another): one flag area, as large as the largest any of them needs, then one
 // slot area. Each GEMM takes it only if its own plan fits. Returns the flag
 // span the call zeroes before its first kernel.
-std::pair<void*, int64_t> share_split_ws(std::initializer_list<GemmArgs*> gs, void* ws, int64_t bytes) {
+std::pair<void*, int64_t> share_split_ws(std::initializer_list<GemmArgs*> gs, void* ws, int64_t bytes,
+                                         int64_t extra_flag_bytes = 0) {
   if (!ws || bytes <= 0) return {nullptr, 0};
-  int64_t flags = 0;
+  int64_t flags = extra_flag_bytes;
   for (const GemmArgs* g : gs) {
     const GemmPlan pl = gemm_plan(g->M, g->N, g->K, g->epi, true);
     if (pl.splits > 1 && pl.flag_bytes > flags) flags = pl.flag_bytes;
@@ -451,8 +458,13 @@ int64_t lnfp8_ln_linear_bwd_workspace_size(int64_t M, int64_t K, int64_t N) {
 
 int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F) {
   if (M < 0 || D < 0 || F < 0) return -1;
-  return shared_split_bytes({gemm_plan(D, F, M, EPI_STORE, true), gemm_plan(M, D, F, EPI_STORE, true),
-                             gemm_plan(F, D, M, EPI_STORE, true)});
+  GemmArgs w2;
+  memset(&w2, 0, sizeof(w2));
+  w2.M = D;
+  w2.N = F;
+  w2.K = M;
+  // dW2 runs in one launch with the FC2 data gradient (its own exchange plan), dLN and dW1 alone
+  return shared_split_bytes({pair_plan(w2), gemm_plan(M, D, F, EPI_STORE, true), gemm_plan(F, D, M, EPI_STORE, true)});
 }
 
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream stream) {
@@ -654,7 +666,9 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   // FC1 wgrad: dW1 = dHq^T . LNq
   GemmArgs w1 = gemm_args(a->dhq, 1, bdt, a->lnq, 1, fdt, a->F, a->D, a->M, m.scale_inv + 1, a->sinv_saved + 0);
   w1.out = a->dw1;
-  const auto flags = share_split_ws({&w2, &d1, &w1}, a->gemm_ws, a->gemm_ws_bytes);
+  // dW2 shares one launch with the FC2 data gradient when both are non-empty
+  const bool paired = a->M > 0 && a->F > 0 && a->D > 0 && !pair_disabled();
+  const auto flags = share_split_ws({&w2, &d1, &w1}, a->gemm_ws, a->gemm_ws_bytes, paired ? pair_plan(w2).flag_bytes : 0);
   // the accumulated outputs and the split-K flags are cleared first (one launch)
   TRY(zero_launch({{a->db2, a->D * 4}, {a->db1, a->F * 4}, {a->dgamma, a->D * 4}, {a->dbeta, a->D * 4}, flags}, st));
   TRY(cast_launch(a->dy, false, a->M, a->D, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->db2, st, false));
@@ -668,8 +682,12 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   d2.amax_q = m.amax_cur + 1;
   d2.colsum = a->db1;
   d2.dbg = a->dh_debug;
-  TRY(gemm_launch(d2, st));
-  TRY(wgrad(w2, a->dw2, st));
+  if (paired) {
+    TRY(gemm_pair_launch(d2, w2, st));
+  } else {
+    TRY(gemm_launch(d2, st));
+    TRY(wgrad(w2, a->dw2, st));
+  }
   TRY(gemm_launch(d1, st));
   TRY(wgrad(w1, a->dw1, st));
   TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st, false));

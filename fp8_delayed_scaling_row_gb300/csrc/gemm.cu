@@ -13,11 +13,14 @@
 //              dhq = fp8(dh * scale_dh); db1 += column sums     (FC2 dgrad)
 // so the GELU output and the gradient dH are written only as FP8 codes.
 //
-// Kernel shape (persistent, one CTA per SM, 640 threads):
+// Kernel shape (persistent, one CTA per SM, 640 threads, 96 registers each):
 //   warp 0      TMA producer (one elected thread), STAGES-deep smem ring
-//   warp 1      MMA issuer (one thread): 128 x BN x 32 tcgen05.mma per K step
-//   warp 2      tensor-memory allocator (2 x BN fp32 columns: double-buffered
-//               accumulator so the epilogue of tile i overlaps the MMAs of i+1)
+//   warp 1      tensor-memory allocator (2 x BN fp32 columns: double-buffered
+//               accumulator so the epilogue of tile i overlaps the MMAs of
+//               i+1), then MMA issuer (one thread): 128 x BN x 32
+//               tcgen05.mma per K step
+//   warps 2-3   idle (registers are handed out per four warps, so a
+//               smaller block would not give the epilogue more of them)
 //   warps 4-19  epilogue, two groups of 8: group g drains accumulator buffer g
 //               (every other tile), so two tiles' epilogues run at once; warp
 //               w reads TMEM lanes 32*(w%4).. (its 32 rows) and one half of
@@ -64,7 +67,7 @@ constexpr int kEpiWarps = 16;  // two groups of 8, one per accumulator buffer
 // CTAs per cluster: a pair of CTAs works on two M tiles of the same N tile and
 // each loads half of the shared B tile, multicast to both.
 constexpr int CL = 2;
-constexpr int kThreads = 128 + 32 * kEpiWarps;
+constexpr int kThreads = 128 + 32 * kEpiWarps;  // warpgroup 0 (producer, MMA, two idle warps), 16 epilogue warps
 
 template <int BN, bool TWO>
 struct Cfg {
@@ -400,7 +403,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
-  if (warp == 2) {
+  if (warp == 1) {
     if constexpr (TWO) {  // one warp of each CTA of the pair allocates collectively
       asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                    "r"(C::TMEM_COLS)
@@ -863,7 +866,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   __syncthreads();
   // both CTAs are done with the pair's tensor memory before it is freed
   cluster_sync();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     if constexpr (TWO)
       asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
@@ -982,6 +985,8 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
   if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8 gemm launch: %s", cudaGetErrorString(e));
   return check_launch("fp8 gemm");
 }
+
+#include "gemm_pair.cuh"
 
 template <int BN, int EPI, int QDT>
 lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
@@ -1107,6 +1112,84 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   }
   return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: epilogue %d with layouts (%d, %d) is not built", g.epi,
                    g.a_layout, g.b_layout);
+}
+
+// The split exchange area a paired launch needs for its secondary GEMM
+// (flag words and partial-product slots), zero when it would not split.
+GemmPlan pair_plan(const GemmArgs& sec) {
+  GemmPlan pl;
+  pl.bn = 256;
+  const int64_t num_m2 = ((sec.M + BM - 1) / BM + CL - 1) / CL;
+  const int64_t num_n = (sec.N + 255) / 256;
+  const int64_t num_kb = (sec.K + BK - 1) / BK;
+  pl.splits = num_kb >= 8 ? 2 : 1;
+  pl.kb_per_split = (int)((num_kb + pl.splits - 1) / pl.splits);
+  const int64_t tiles = num_m2 * CL * num_n;
+  pl.flag_bytes = pl.splits > 1 ? ((tiles * 2 * kEpiWarps * 4 + 255) / 256) * 256 : 0;
+  pl.slot_bytes = pl.splits > 1 ? tiles * (int64_t)(BM * 256) * 4 : 0;
+  pl.ws_bytes = pl.flag_bytes + pl.slot_bytes;
+  return pl;
+}
+
+lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t st) {
+  if (g0.epi != EPI_DGELU || g0.a_layout != 0 || g0.b_layout != 1 || g1.epi != EPI_STORE)
+    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: only dGELU (A [M, K], B [K, N]) with a bf16-store GEMM");
+  for (const GemmArgs* g : {&g0, &g1})
+    if (g->M > 0x7FFFFFFF || g->N > 0x7FFFFFFF || g->K > 0x7FFFFFFF)
+      return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: dimension above 2^31");
+  if (g0.M == 0 || g0.N == 0 || g0.K == 0 || g1.M == 0 || g1.N == 0 || g1.K == 0)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: empty operand (run the GEMMs separately)");
+  const bool a1_mn = g1.a_layout == 1, b1_mn = g1.b_layout == 1;
+  GemmPlan pl = pair_plan(g1);
+  const int64_t flag_off = g1.ws_flag_bytes > 0 ? g1.ws_flag_bytes : pl.flag_bytes;
+  if (pl.splits > 1 && (!g1.ws || flag_off < pl.flag_bytes || flag_off % 256 || g1.ws_bytes < flag_off + pl.slot_bytes)) {
+    pl.splits = 1;
+    pl.kb_per_split = (int)((g1.K + BK - 1) / BK);
+  }
+
+  CUtensorMap maps[7];
+  bool ok = make_operand_map(&maps[0], g0.a, g0.K, g0.M, BM);
+  ok = ok && make_operand_map(&maps[1], g0.b, g0.N, g0.K, BK);
+  ok = ok && make_map(&maps[2], g0.out_q, 1, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+  ok = ok && make_map(&maps[3], g0.h_in, 2, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && (a1_mn ? make_operand_map(&maps[4], g1.a, g1.M, g1.K, BK) : make_operand_map(&maps[4], g1.a, g1.K, g1.M, BM));
+  ok = ok && (b1_mn ? make_operand_map(&maps[5], g1.b, g1.N, g1.K, BK) : make_operand_map(&maps[5], g1.b, g1.K, g1.N, 128));
+  ok = ok && make_map(&maps[6], g1.out, 2, g1.N, g1.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) return set_error(LNFP8_ERR_CUDA, "fp8 gemm pair: cuTensorMapEncodeTiled failed");
+
+  PairParams pp;
+  auto prob = [&](const GemmArgs& g, bool a_mn, bool b_mn, int splits) {
+    PairProb pr;
+    pr.M = (int)g.M;
+    pr.N = (int)g.N;
+    pr.num_m2 = (int)(((g.M + BM - 1) / BM + CL - 1) / CL);
+    pr.num_n = (int)((g.N + 255) / 256);
+    pr.num_kb = (int)((g.K + BK - 1) / BK);
+    pr.units = pr.num_m2 * pr.num_n * splits;
+    pr.idesc = make_idesc(256, 256, g.a_dtype, g.b_dtype, a_mn, b_mn);
+    pr.sinv_a = g.sinv_a;
+    pr.sinv_b = g.sinv_b;
+    return pr;
+  };
+  pp.p0 = prob(g0, false, true, 1);
+  pp.p1 = prob(g1, a1_mn, b1_mn, pl.splits);
+  pp.scale_q = g0.scale_q;
+  pp.amax_q = g0.amax_q;
+  pp.colsum = g0.colsum;
+  pp.dbg = g0.dbg;
+  pp.bias1 = g1.bias;
+  pp.splits1 = pl.splits;
+  pp.kbs1 = pl.kb_per_split;
+  pp.flags = pl.splits > 1 ? reinterpret_cast<unsigned*>(g1.ws) : nullptr;
+  pp.ws = pl.splits > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g1.ws) + flag_off) : nullptr;
+  if ((int64_t)pp.p0.units + pp.p1.units > 0x7FFFFFFF) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: too many tiles");
+  if (g0.q_dtype == LNFP8_E4M3) {
+    if (a1_mn && b1_mn) return pair_launch_t<true, true, LNFP8_E4M3>(maps, pp, st);
+  } else {
+    if (a1_mn && b1_mn) return pair_launch_t<true, true, LNFP8_E5M2>(maps, pp, st);
+  }
+  return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: secondary layouts (%d, %d) are not built", g1.a_layout,
+                   g1.b_layout);
 }
 
 }  // namespace lnfp8

@@ -1,0 +1,615 @@
+// Paired persistent GEMM: the FC2 data gradient with the fused dGELU epilogue
+// (the "primary") and one plain bf16-store GEMM (the "secondary", the FC2
+// weight gradient) share every CTA pair of one launch.
+//
+// The dGELU epilogue (GELU derivative, E5M2 cast, amax, column sums, the
+// read of H) takes several times longer per 256 x 256 tile than the tile's
+// MMAs (K = d_model), so alone its tensor cores idle most of the time. The
+// weight gradient is the opposite: long MMAs (K = tokens) and a short
+// epilogue. Here each CTA pair walks one schedule: a primary tile, then a
+// slice of its secondary tiles' K blocks, then the next primary tile, ... so
+// the MMAs of the secondary run while the epilogue warps work on the primary.
+// Tensor memory holds one primary accumulator (columns 0-255) and one
+// secondary accumulator (256-511); all 16 epilogue warps drain each tile
+// (warp quarter q reads TMEM lanes 32q.., warp slice s the tile's columns
+// 64s..64s+63, two 32-column chunks).
+//
+// This file is part of gemm.cu's translation unit (it uses its PTX wrappers,
+// tile constants and status word).
+
+constexpr int kPairStages = 4;
+
+struct PairCfg {
+  static constexpr int STAGES = kPairStages;
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = 128 * BK;  // this CTA's half of the 256-wide B tile
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int OUT_OFF = STAGES * STAGE_BYTES;      // bf16 staging box per warp (secondary stores)
+  static constexpr int H_OFF = OUT_OFF + kEpiWarps * 2048;  // bf16 H box per warp (primary loads)
+  static constexpr int Q_OFF = H_OFF + kEpiWarps * 2048;    // FP8 staging box per warp (primary stores)
+  static constexpr int CSUM_OFF = Q_OFF + kEpiWarps * 1024; // [tile parity][row quarter][256] fp32 column-sum partials
+  static constexpr int BAR_OFF = CSUM_OFF + 2 * 4 * 256 * 4;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(2 * STAGES + 5 + 4 + kEpiWarps + 1 <= BAR_BYTES / 8, "barrier area");
+};
+
+struct PairProb {
+  int M, N, num_m2, num_n, num_kb, units;
+  uint32_t idesc;
+  const float* sinv_a;
+  const float* sinv_b;
+};
+
+struct PairParams {
+  PairProb p0, p1;  // primary (dGELU), secondary (bf16 store)
+  // primary epilogue
+  const float* scale_q;
+  float* amax_q;
+  float* colsum;
+  float* dbg;
+  // secondary epilogue
+  const uint16_t* bias1;
+  int splits1, kbs1;  // K pieces per secondary tile (1 or 2) and K blocks per piece
+  float* ws;          // split exchange: [tile][warp][chunk][8][32] x 16 B
+  unsigned* flags;    // [tile][piece][warp]
+};
+
+// The schedule of one cluster. Its work units are the global units c, c + ncl,
+// ... where global units 0..U0-1 are the primary tiles and the rest the
+// secondary units (tile, K piece). The cluster runs its primary units in
+// order and spreads the K blocks of its secondary units evenly over the gaps
+// after them.
+struct PairSched {
+  int c, ncl, U0, U1, nP;
+  int64_t KS;
+  __device__ void init(const PairParams& p, int cid, int ncl_) {
+    c = cid;
+    ncl = ncl_;
+    U0 = p.p0.units;
+    U1 = p.p1.units;
+    nP = U0 > c ? (U0 - c + ncl - 1) / ncl : 0;
+    KS = 0;
+    for (int g = c + nP * ncl; g < U0 + U1; g += ncl) KS += s_len(p, g - U0);
+  }
+  __device__ int p_unit(int i) const { return c + i * ncl; }
+  __device__ int s_unit(int j) const { return c + (nP + j) * ncl - U0; }  // j-th secondary unit of the cluster
+  __device__ static int s_kb0(const PairParams& p, int v) { return (v % p.splits1) * p.kbs1; }
+  __device__ static int s_len(const PairParams& p, int v) {
+    const int k0 = s_kb0(p, v);
+    const int k1 = min(p.p1.num_kb, k0 + p.kbs1);
+    return k1 - k0;
+  }
+  __device__ int gaps() const { return nP > 0 ? nP : 1; }
+  __device__ int64_t gap_end(int i) const { return nP > 0 ? KS * (i + 1) / nP : KS; }
+};
+
+// Walks the secondary K blocks of a cluster's schedule: segment = one unit's
+// consecutive K blocks inside one gap.
+struct SecCursor {
+  int j = 0;         // local index of the current secondary unit
+  int64_t jo = 0;    // schedule offset where it starts
+  int64_t off = 0;   // next offset to run
+  template <class F>
+  __device__ bool run_gap(const PairSched& sc, const PairParams& p, int64_t end, F&& seg) {
+    while (off < end) {
+      const int v = sc.s_unit(j);
+      const int len = PairSched::s_len(p, v);
+      const int64_t seg_end = min(end, jo + len);
+      const int k0 = PairSched::s_kb0(p, v);
+      const bool first = off == jo, last = seg_end == jo + len;
+      if (!seg(v, k0 + (int)(off - jo), k0 + (int)(seg_end - jo), first, last)) return false;
+      off = seg_end;
+      if (last) {
+        jo += len;
+        ++j;
+      }
+    }
+    return true;
+  }
+};
+
+template <bool A1_MN, bool B1_MN, int QDT>
+__global__ void __launch_bounds__(kThreads, 1)
+pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+            const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmH0,
+            const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+            const __grid_constant__ CUtensorMap tmO1, const PairParams p) {
+  using C = PairCfg;
+  constexpr int STAGES = C::STAGES;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, csum[4 slices], hload[kEpiWarps]
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 4 + kEpiWarps);
+  uint32_t* tmem_slot = misc;
+  volatile uint32_t* abort_flag = misc + 1;
+  float* csred2 = reinterpret_cast<float*>(smem + C::CSUM_OFF);  // [2 tile parities][4 quarters][256]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto csum_bar = [&](int sl) { return bar0 + 8u * (2 * STAGES + 5 + sl); };
+  auto hload_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 9 + w); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);  // released once by the pair's leader MMA
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * kEpiWarps);  // every epilogue warp of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    for (int sl = 0; sl < 4; ++sl) mbar_init(csum_bar(sl), 4);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(hload_bar(w), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  cluster_sync();
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA1)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)), "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int rank = (int)cluster_rank();
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  constexpr uint16_t kPair = 3;
+  PairSched sc;
+  sc.init(p, cid, ncl);
+  // tile coordinates: primary unit u = tile; secondary unit v = tile * splits1 + piece
+  auto p_m = [&](int u) { return (u % p.p0.num_m2) * CL + rank; };
+  auto p_n = [&](int u) { return u / p.p0.num_m2; };
+  auto s_m = [&](int v) { return ((v / p.splits1) % p.p1.num_m2) * CL + rank; };
+  auto s_n = [&](int v) { return (v / p.splits1) / p.p1.num_m2; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      auto load = [&](bool prim, int m_blk, int n_blk, int kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) return false;
+        const uint32_t fb = full_bar(stage);
+        const uint32_t fl = map_to_rank(fb, 0);
+        const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
+        const uint32_t b_dst = a_dst + C::A_BYTES;
+        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+        if (prim) {  // dY codes [M, D] K-major; W2 codes [D, F] = [K, N] MN-major
+          tma_load_2d_cg2(a_dst, &tmA0, kb * BK, m_blk * BM, fl);
+          tma_load_2d_cg2(b_dst, &tmB0, n_blk * BN + rank * 128, kb * BK, fl);
+        } else {
+          if (!A1_MN) tma_load_2d_cg2(a_dst, &tmA1, kb * BK, m_blk * BM, fl);
+          else        tma_load_2d_cg2(a_dst, &tmA1, m_blk * BM, kb * BK, fl);
+          if (!B1_MN) tma_load_2d_cg2(b_dst, &tmB1, kb * BK, n_blk * BN + rank * 128, fl);
+          else        tma_load_2d_cg2(b_dst, &tmB1, n_blk * BN + rank * 128, kb * BK, fl);
+        }
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        return true;
+      };
+      SecCursor cur;
+      for (int i = 0; i < sc.gaps() && ok; ++i) {
+        if (i < sc.nP) {
+          const int u = sc.p_unit(i);
+          for (int kb = 0; kb < p.p0.num_kb && ok; ++kb) ok = load(true, p_m(u), p_n(u), kb);
+        }
+        if (ok)
+          ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int v, int k0, int k1, bool, bool) {
+            for (int kb = k0; kb < k1; ++kb)
+              if (!load(false, s_m(v), s_n(v), kb)) return false;
+            return true;
+          });
+      }
+      if (!ok && rank == 0) {
+        const int64_t pending = issued < STAGES ? issued : STAGES;
+        int s = stage;
+        uint32_t ph = phase;
+        for (int64_t i = 0; i < pending; ++i) {
+          if (--s < 0) { s = STAGES - 1; ph ^= 1; }
+          uint32_t dummy_flag = 0;
+          mbar_wait(full_bar(s), ph, &dummy_flag, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (pair leader)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase[2] = {0u, 0u};
+      bool ok = true;
+      auto mma_blocks = [&](bool prim, int k0, int k1, bool fresh) {
+        const uint32_t d_tmem = tmem_base + (prim ? 0u : 256u);
+        const uint32_t idesc = prim ? p.p0.idesc : p.p1.idesc;
+        for (int kb = k0; kb < k1; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_base = a_base + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t accum = !(fresh && kb == k0 && kk == 0);
+            const bool a_mn = prim ? false : A1_MN, b_mn = prim ? true : B1_MN;
+            const uint64_t ad = a_mn ? make_desc(a_base + kk * 32 * 128, 1024, 1024) : make_desc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = b_mn ? make_desc(b_base + kk * 32 * 128, 1024, 1024) : make_desc(b_base + kk * 32, 16, 1024);
+            mma_f8_cg2(d_tmem, ad, bd, idesc, accum);
+          }
+          mma_commit_cg2_mc(empty_bar(stage), kPair);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        return true;
+      };
+      SecCursor cur;
+      for (int i = 0; i < sc.gaps() && ok; ++i) {
+        if (i < sc.nP) {
+          if (!mbar_wait(tempty_bar(0), acc_phase[0] ^ 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (!mma_blocks(true, 0, p.p0.num_kb, true)) { ok = false; break; }
+          mma_commit_cg2_mc(tfull_bar(0), kPair);
+          acc_phase[0] ^= 1;
+        }
+        ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int, int k0, int k1, bool first, bool last) {
+          if (first) {
+            if (!mbar_wait(tempty_bar(1), acc_phase[1] ^ 1, abort_flag)) return false;
+            tc_fence_after();
+          }
+          if (!mma_blocks(false, k0, k1, first)) return false;
+          if (last) {
+            mma_commit_cg2_mc(tfull_bar(1), kPair);
+            acc_phase[1] ^= 1;
+          }
+          return true;
+        });
+      }
+      if (!ok) {
+        mma_commit_cg2_mc(drain_bar, 1);
+        uint32_t dummy_flag = 0;
+        mbar_wait(drain_bar, 0, &dummy_flag, 100000000ull);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue (16 warps per tile)
+    const int ew = warp - 4;
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter..
+    const int slice = ew >> 2;     // columns 64*slice .. 64*slice+63 of the tile
+    const int r = lane;
+    uint8_t* so = smem + C::OUT_OFF + ew * 2048;
+    uint8_t* sh = smem + C::H_OFF + ew * 2048;
+    uint8_t* sq = smem + C::Q_OFF + ew * 1024;
+    const uint32_t so_a = smem_u32(so), sh_a = smem_u32(sh), sq_a = smem_u32(sq);
+    const uint32_t hbar = hload_bar(ew);
+    uint32_t hphase = 0;
+    bool h_pending = false;
+    const float s0 = __fmul_rn(*p.p0.sinv_a, *p.p0.sinv_b);
+    const float s1 = __fmul_rn(*p.p1.sinv_a, *p.p1.sinv_b);
+    const float scale_q = *p.scale_q;
+    float am_f = 0.f;
+    uint32_t acc_phase[2] = {0u, 0u};
+    const bool combiner = p.colsum != nullptr && quarter == 0;
+    const uint32_t tempty0 = map_to_rank(tempty_bar(0), 0), tempty1 = map_to_rank(tempty_bar(1), 0);
+    // H prefetch: this warp's two chunks of each of the cluster's primary tiles, one chunk ahead
+    int h_i = 0, h_ch = 0;
+    auto issue_h = [&]() {
+      if (h_i >= sc.nP) return;
+      const int u = sc.p_unit(h_i);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(hbar, 2048);
+        tma_load_2d(sh_a, &tmH0, p_n(u) * BN + slice * 64 + h_ch * 32, p_m(u) * BM + quarter * 32, hbar);
+      }
+      h_pending = true;
+      if (++h_ch == 2) { h_ch = 0; ++h_i; }
+    };
+    issue_h();
+
+    // Every warp releases the primary accumulator after its last tensor-memory
+    // load, so the next primary tile's MMAs overlap the rest of this epilogue.
+    // The column-sum partials alternate between two buffers by tile parity: a
+    // combiner reads this tile's buffer before it touches the next tile, and
+    // the tile after next cannot start before every warp, the combiner too,
+    // has released the next one.
+    auto prim_tile = [&](int u) -> bool {
+      const int m_blk = p_m(u), n_blk = p_n(u);
+      float* csred = csred2 + acc_phase[0] * 4 * BN;
+      if (!mbar_wait(tfull_bar(0), acc_phase[0], abort_flag)) return false;
+      tc_fence_after();
+      const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
+      const bool row_ok = m < p.p0.M;
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col0 = slice * 64 + ch * 32;
+        const int64_t n0 = (int64_t)n_blk * BN + col0;
+        uint32_t rr[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0, rr);
+        if (ch == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(tempty0);
+        }
+        if (!mbar_wait(hbar, hphase, abort_flag)) return false;
+        hphase ^= 1;
+        h_pending = false;
+        uint4 hin[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hin[j] = *reinterpret_cast<const uint4*>(sh + sw64(r, j));
+        fence_async_smem();
+        __syncwarp();
+        issue_h();
+        float v[32];
+        uint2 oq[4];
+        const uint64_t s2 = f2(s0, s0);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int64_t n = n0 + g * 8;
+          const bool ok = row_ok && n < p.p0.N;
+          const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC);
+          const uint64_t KC3 = f2(3.0f * kGeluK * kGeluC, 3.0f * kGeluK * kGeluC), H2 = f2(0.5f, 0.5f), O2 = f2(1.0f, 1.0f);
+          const uint32_t hw[4] = {hin[g].x, hin[g].y, hin[g].z, hin[g].w};
+          uint64_t d2[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint64_t e2 = f2(__uint_as_float(rr[g * 8 + 2 * i]), __uint_as_float(rr[g * 8 + 2 * i + 1]));
+            const uint64_t h = bf2_to_f2(hw[i]);
+            const uint64_t hsq = mul2(h, h);
+            const uint64_t uu = mul2(h, fma2(hsq, KC2, K2));
+            const uint64_t t = f2(tanh_fast(lo(uu)), tanh_fast(hi(uu)));
+            const uint64_t dudh = fma2(hsq, KC3, K2);
+            const uint64_t sech2 = sub2(O2, mul2(t, t));
+            const uint64_t gp = fma2(mul2(mul2(h, H2), sech2), dudh, fma2(t, H2, H2));
+            d2[i] = mul2(mul2(e2, s2), gp);
+          }
+          const uint64_t q2 = f2(scale_q, scale_q);
+          oq[g].x = (uint32_t)cvt_pair<QDT>(mul2(d2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[1], q2)) << 16);
+          oq[g].y = (uint32_t)cvt_pair<QDT>(mul2(d2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[3], q2)) << 16);
+          if (ok) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(d2[i])), hi(d2[i]));
+            if (p.dbg) {
+              float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.p0.N + n);
+              d4[0] = make_float4(lo(d2[0]), hi(d2[0]), lo(d2[1]), hi(d2[1]));
+              d4[1] = make_float4(lo(d2[2]), hi(d2[2]), lo(d2[3]), hi(d2[3]));
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[g * 8 + 2 * i] = ok ? lo(d2[i]) : 0.f;
+            v[g * 8 + 2 * i + 1] = ok ? hi(d2[i]) : 0.f;
+          }
+        }
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        *reinterpret_cast<uint4*>(sq + sw32(r, 0)) = make_uint4(oq[0].x, oq[0].y, oq[1].x, oq[1].y);
+        *reinterpret_cast<uint4*>(sq + sw32(r, 1)) = make_uint4(oq[2].x, oq[2].y, oq[3].x, oq[3].y);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int y = m_blk * BM + quarter * 32;
+          if (y < p.p0.M) tma_store_2d(&tmQ0, sq_a, (int)n0, y);
+          bulk_commit();
+        }
+        if (p.colsum) csred[quarter * BN + col0 + lane] = transpose_reduce32(v, lane);
+      }
+      if (p.colsum) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(csum_bar(slice));
+        if (combiner) {
+          if (!mbar_wait(csum_bar(slice), acc_phase[0], abort_flag)) return false;
+          for (int c = lane; c < 64; c += 32) {
+            const int col = slice * 64 + c;
+            const int64_t n = (int64_t)n_blk * BN + col;
+            const float tot = (csred[col] + csred[BN + col]) + (csred[2 * BN + col] + csred[3 * BN + col]);
+            if (n < p.p0.N) atomicAdd(p.colsum + n, tot);
+          }
+        }
+      }
+      acc_phase[0] ^= 1;
+      return true;
+    };
+
+    // secondary tile (bf16 store); with two K pieces the halves exchange chunks:
+    // piece q finishes chunk q of every warp's pair and spills the other
+    auto slot_ptr = [&](int m_blk, int n_blk, int ch) {
+      const int64_t t = (int64_t)m_blk * p.p1.num_n + n_blk;
+      return reinterpret_cast<uint4*>(p.ws + t * (int64_t)(BM * BN)) + ((ew * 2 + ch) * 8) * 32 + lane;
+    };
+    auto flag_ptr = [&](int m_blk, int n_blk, int q) {
+      return p.flags + (((int64_t)m_blk * p.p1.num_n + n_blk) * 2 + q) * kEpiWarps + ew;
+    };
+    auto sec_tile = [&](int v) -> bool {
+      const int m_blk = s_m(v), n_blk = s_n(v);
+      const int sp = p.splits1 > 1 ? v % p.splits1 : 0;
+      if (!mbar_wait(tfull_bar(1), acc_phase[1], abort_flag)) return false;
+      tc_fence_after();
+      const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
+      (void)m;
+      if (p.splits1 > 1) {
+        const int ch = 1 - sp;
+        uint32_t rr[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(256 + slice * 64 + ch * 32), rr);
+        uint4* dst = slot_ptr(m_blk, n_blk, ch);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) __stcg(dst + j * 32, make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]));
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicExch(flag_ptr(m_blk, n_blk, sp), 1u);
+        const unsigned* f = flag_ptr(m_blk, n_blk, 1 - sp);
+        int ready = 1;
+        if (lane == 0) {
+          const uint64_t t0 = globaltimer();
+          for (uint32_t it = 0;; ++it) {
+            unsigned fv;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(fv) : "l"(f) : "memory");
+            if (fv) break;
+            if ((it & 15) == 15) {
+              if (*abort_flag) { ready = 0; break; }
+              if (globaltimer() - t0 > 1000000000ull) {
+                *abort_flag = 1;
+                atomicOr(&g_status, kStatusTimeout);
+                ready = 0;
+                break;
+              }
+            }
+          }
+        }
+        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+        if (!ready) return false;
+        {
+          unsigned fv;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(fv) : "l"(f) : "memory");
+        }
+        __syncwarp();
+        if (lane == 0) *const_cast<unsigned*>(f) = 0u;
+      }
+      const int ch_first = p.splits1 > 1 ? sp : 0, ch_step = p.splits1 > 1 ? 2 : 1;
+#pragma unroll 1
+      for (int ch = ch_first; ch < 2; ch += ch_step) {
+        const int col0 = slice * 64 + ch * 32;
+        const int64_t n0 = (int64_t)n_blk * BN + col0;
+        uint4 bias8[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          bias8[g] = p.bias1 && n0 + g * 8 < p.p1.N ? __ldg(reinterpret_cast<const uint4*>(p.bias1 + n0 + g * 8))
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t rr[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(256 + col0), rr);
+        if (ch + ch_step >= 2) {  // the last load of this warp: release the accumulator
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(tempty1);
+        }
+        if (p.splits1 > 1) {  // part_0 + part_1 (fp32 addition commutes)
+          const uint4* src = slot_ptr(m_blk, n_blk, ch);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 w = __ldcg(src + j * 32);
+            rr[4 * j] = __float_as_uint(__uint_as_float(rr[4 * j]) + __uint_as_float(w.x));
+            rr[4 * j + 1] = __float_as_uint(__uint_as_float(rr[4 * j + 1]) + __uint_as_float(w.y));
+            rr[4 * j + 2] = __float_as_uint(__uint_as_float(rr[4 * j + 2]) + __uint_as_float(w.z));
+            rr[4 * j + 3] = __float_as_uint(__uint_as_float(rr[4 * j + 3]) + __uint_as_float(w.w));
+          }
+        }
+        uint4 ob[4];
+        const uint64_t s2 = f2(s1, s1);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint4 bu = bias8[g];
+          const uint64_t b2[4] = {bf2_to_f2(bu.x), bf2_to_f2(bu.y), bf2_to_f2(bu.z), bf2_to_f2(bu.w)};
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint64_t e2 = f2(__uint_as_float(rr[g * 8 + 2 * i]), __uint_as_float(rr[g * 8 + 2 * i + 1]));
+            const uint64_t y = fma2(e2, s2, b2[i]);
+            w[i] = pack_bf16x2(lo(y), hi(y));
+          }
+          ob[g] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(so + sw64(r, j)) = ob[j];
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int y = m_blk * BM + quarter * 32;
+          if (y < p.p1.M) tma_store_2d(&tmO1, so_a, (int)n0, y);
+          bulk_commit();
+        }
+      }
+      acc_phase[1] ^= 1;
+      return true;
+    };
+
+    SecCursor cur;
+    bool ok = true;
+    for (int i = 0; i < sc.gaps() && ok; ++i) {
+      if (i < sc.nP) ok = prim_tile(sc.p_unit(i));
+      if (ok)
+        ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int v, int, int, bool, bool last) {
+          return last ? sec_tile(v) : true;
+        });
+    }
+    if (h_pending) {  // a prefetch may be in flight (the last one, or after an abort)
+      uint32_t dummy_flag = 0;
+      if (lane == 0) mbar_wait(hbar, hphase, &dummy_flag, 100000000ull);
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
+    const uint32_t am = warp_max_u32(abs_bits(am_f));
+    if (lane == 0 && am != 0u) atomic_max_amax(p.amax_q, am);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
+  }
+  cluster_sync();
+}
+
+template <bool A1_MN, bool B1_MN, int QDT>
+lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaStream_t st) {
+  auto k = pair_kernel<A1_MN, B1_MN, QDT>;
+  static bool smem_set = false;
+  if (!smem_set) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM) != cudaSuccess)
+      return check_launch("fp8 gemm pair: shared memory attribute");
+    smem_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = PairCfg::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (!max_clusters) {
+    cfg.gridDim = dim3(num_sms());
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg) != cudaSuccess || max_clusters < 1) {
+      cudaGetLastError();
+      max_clusters = num_sms() / CL;
+    }
+  }
+  const int units = pp.p0.units + pp.p1.units;
+  const int clusters = units < max_clusters ? units : max_clusters;
+  // the two K pieces of a secondary tile exchange partials: they must run on different clusters
+  if (pp.splits1 > 1 && clusters < 2) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: split on one cluster");
+  cfg.gridDim = dim3(clusters * CL);
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  LaunchScope ls("gemm_dgelu_wgrad", st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], pp);
+  if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8 gemm pair launch: %s", cudaGetErrorString(e));
+  return check_launch("fp8 gemm pair");
+}

@@ -81,6 +81,14 @@ struct GemmPlan {
 };
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split);
 
+// One persistent launch of the FC2 data gradient with the dGELU epilogue (g0:
+// A [M, K] K-major, B [K, N]) and a bf16-store GEMM (g1, both operands
+// [K, rows]): the second GEMM's MMAs fill the first one's epilogue time.
+// g1.ws (with g1.ws_flag_bytes) is its split-K exchange area; pair_plan gives
+// the sizes it needs.
+lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t st);
+GemmPlan pair_plan(const GemmArgs& g1);
+
 lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st);
 lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st);
 

@@ -293,8 +293,9 @@ def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profile
     direct = L.profile_collect()
     L.profile_enable(False)
     L.sync_status()
-    # forward: weight casts, LayerNorm, FC1, FC2, state; backward: clears, dY cast, four GEMMs, LayerNorm, state
-    assert sum(n for _, n in direct.values()) == 13 and all(ms > 0 for ms, _ in direct.values())
+    # forward: weight casts, LayerNorm, FC1, FC2, state; backward: clears, dY cast, the FC2 data and weight
+    # gradients in one launch, the FC1 data gradient, the FC1 weight gradient, LayerNorm, state
+    assert sum(n for _, n in direct.values()) == 12 and all(ms > 0 for ms, _ in direct.values())
 
     fm1, bm1, ctx1, g1 = make()
     y1 = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
@@ -350,3 +351,23 @@ def test_mlp_backward_split_k_is_deterministic_and_matches_unsplit(L, M, D, F):
     for k in ("dw1", "dw2", "dln"):
         a, b = host(getattr(runs[0], k)), host(getattr(runs[2], k))
         assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(b).max(), k
+
+
+@pytest.mark.parametrize("M,D,F", [(8192, 768, 3072), (1008, 256, 1024), (2064, 384, 1552)])
+def test_mlp_backward_fc2_weight_gradient_equals_the_standalone_gemm(L, M, D, F):
+    """The FC2 weight gradient runs in one launch with the FC2 data gradient. Without a
+    split-K workspace its K range is not cut, so it must equal, bit for bit, the
+    standalone GEMM of the same codes and scales: dW2 = (dYq^T . Aq) * gsinv[0] * sinv[2]."""
+    p = {k: bf16_dev(v) for k, v in synth.mlp_params(D, F, bias_std=0.02, seed=9).items()}
+    x = bf16_dev(synth.activations(M, D, dist="outliers", seed=9, step=0))
+    dy = bf16_dev(synth.grad(M, D, seed=9, step=0))
+    rec = L.Recipe("hybrid", 4)
+    ctx = L.mlp_ctx(M, D, F)
+    L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], L.ScalingMeta(4, 4), rec, ctx=ctx)
+    bm = L.ScalingMeta(2, 4)
+    gsinv = bm.scale_inv.clone()  # the backward state before the call (its update runs at the end)
+    g = L.mlp_grads(M, D, F, split_k=False)
+    L.ln_mlp_bwd(dy, x, p["gamma"], ctx, bm, rec, grads=g)
+    ref = L.fp8_gemm(g.dyq, 1, L.E5M2, ctx.aq, 1, L.E4M3, D, F, M, gsinv[0:1], ctx.sinv_saved[2:3])
+    L.sync_status()
+    assert torch.equal(g.dw2, ref)
