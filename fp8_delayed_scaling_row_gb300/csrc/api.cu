@@ -15,6 +15,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -453,7 +454,12 @@ int64_t lnfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
 
 int64_t lnfp8_ln_linear_bwd_workspace_size(int64_t M, int64_t K, int64_t N) {
   if (M < 0 || N < 0 || K < 0) return -1;
-  return shared_split_bytes({gemm_plan(M, K, N, EPI_STORE, true), gemm_plan(N, K, M, EPI_STORE, true)});
+  GemmArgs wg;
+  memset(&wg, 0, sizeof(wg));
+  wg.M = N;
+  wg.N = K;
+  wg.K = M;
+  return shared_split_bytes({pair_plan(wg), gemm_plan(M, K, N, EPI_STORE, true), gemm_plan(N, K, M, EPI_STORE, true)});
 }
 
 int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F) {
@@ -464,7 +470,12 @@ int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F) {
   w2.N = F;
   w2.K = M;
   // dW2 runs in one launch with the FC2 data gradient (its own exchange plan), dLN and dW1 alone
-  return shared_split_bytes({pair_plan(w2), gemm_plan(M, D, F, EPI_STORE, true), gemm_plan(F, D, M, EPI_STORE, true)});
+  GemmArgs w1 = w2;
+  w1.M = F;
+  w1.N = D;
+  // the weight gradients run paired with the data gradients (their own exchange plan); without pairing the GEMMs' own
+  return shared_split_bytes({pair_plan(w2), pair_plan(w1), gemm_plan(D, F, M, EPI_STORE, true),
+                             gemm_plan(M, D, F, EPI_STORE, true), gemm_plan(F, D, M, EPI_STORE, true)});
 }
 
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream stream) {
@@ -552,14 +563,20 @@ lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream strea
   dg.out = dln;
   GemmArgs wg = gemm_args(a->dyq, 1, bdt, a->xq, 1, fdt, a->N, a->K, a->M, m.scale_inv + 0, a->sinv_saved + 0);
   wg.out = a->dw;
-  const auto flags = share_split_ws({&dg, &wg}, a->gemm_ws, a->gemm_ws_bytes);
+  // the data and weight gradients share one persistent launch when both are non-empty
+  const bool paired = a->M > 0 && a->K > 0 && a->N > 0 && !pair_disabled();
+  const auto flags = share_split_ws({&dg, &wg}, a->gemm_ws, a->gemm_ws_bytes, paired ? pair_plan(wg).flag_bytes : 0);
   // the accumulated outputs and the split-K flags are cleared first (one launch)
   TRY(zero_launch({{a->dbias, a->N * 4}, {ln ? a->dgamma : nullptr, a->K * 4}, {ln ? a->dbeta : nullptr, a->K * 4},
                    flags},
                   st));
   TRY(cast_launch(a->dy, false, a->M, a->N, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->dbias, st, false));
-  TRY(gemm_launch(dg, st));
-  TRY(wgrad(wg, a->dw, st));
+  if (paired) {
+    TRY(gemm_pair_launch(dg, wg, st));
+  } else {
+    TRY(gemm_launch(dg, st));
+    TRY(wgrad(wg, a->dw, st));
+  }
   if (ln) TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st, false));
   return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
 }
@@ -667,8 +684,10 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
   GemmArgs w1 = gemm_args(a->dhq, 1, bdt, a->lnq, 1, fdt, a->F, a->D, a->M, m.scale_inv + 1, a->sinv_saved + 0);
   w1.out = a->dw1;
   // dW2 shares one launch with the FC2 data gradient when both are non-empty
+  // (and dW1 with dLN): each data gradient shares one persistent launch with its weight gradient
   const bool paired = a->M > 0 && a->F > 0 && a->D > 0 && !pair_disabled();
-  const auto flags = share_split_ws({&w2, &d1, &w1}, a->gemm_ws, a->gemm_ws_bytes, paired ? pair_plan(w2).flag_bytes : 0);
+  const auto flags = share_split_ws({&w2, &d1, &w1}, a->gemm_ws, a->gemm_ws_bytes,
+                                    paired ? std::max(pair_plan(w2).flag_bytes, pair_plan(w1).flag_bytes) : 0);
   // the accumulated outputs and the split-K flags are cleared first (one launch)
   TRY(zero_launch({{a->db2, a->D * 4}, {a->db1, a->F * 4}, {a->dgamma, a->D * 4}, {a->dbeta, a->D * 4}, flags}, st));
   TRY(cast_launch(a->dy, false, a->M, a->D, bdt, m.scale + 0, m.amax_cur + 0, a->dyq, nullptr, a->db2, st, false));
@@ -688,8 +707,12 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
     TRY(gemm_launch(d2, st));
     TRY(wgrad(w2, a->dw2, st));
   }
-  TRY(gemm_launch(d1, st));
-  TRY(wgrad(w1, a->dw1, st));
+  if (paired) {
+    TRY(gemm_pair_launch(d1, w1, st));
+  } else {
+    TRY(gemm_launch(d1, st));
+    TRY(wgrad(w1, a->dw1, st));
+  }
   TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st, false));
   return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
 }

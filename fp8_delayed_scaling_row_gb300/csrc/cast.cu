@@ -197,7 +197,8 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
   if (clear_colsum && colsum && cols > 0 && cudaMemsetAsync(colsum, 0, cols * sizeof(float), st) != cudaSuccess)
     return check_launch("fp8_quantize: clearing colsum");
   if (rows == 0 || cols == 0) return LNFP8_OK;
-  const Grid2 g = cast_grid(rows, cols, 2LL * num_sms());
+  // enough CTAs that each SM keeps several row tiles of loads in flight
+  const Grid2 g = cast_grid(rows, cols, 8LL * num_sms());
   if (g.strips > 0x7FFFFFFF || g.ysplit > 65535)
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8_quantize: tensor too large");
   const CastT t{in, rows, cols, g.rows_per_cta, scale, amax_cur, out, out_t, colsum};
@@ -213,7 +214,7 @@ lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, con
     TRY_CAST(cast_launch(in0, false, rows0, cols0, dtype, scale0, amax0, out0, nullptr, nullptr, st));
     return cast_launch(in1, false, rows1, cols1, dtype, scale1, amax1, out1, nullptr, nullptr, st);
   }
-  const Grid2 g0 = cast_grid(rows0, cols0, num_sms()), g1 = cast_grid(rows1, cols1, num_sms());
+  const Grid2 g0 = cast_grid(rows0, cols0, 4LL * num_sms()), g1 = cast_grid(rows1, cols1, 4LL * num_sms());
   if (max64(g0.strips, g1.strips) > 0x7FFFFFFF || max64(g0.ysplit, g1.ysplit) > 65535)
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "weight cast: tensor too large");
   const CastT a{in0, rows0, cols0, g0.rows_per_cta, scale0, amax0, out0, nullptr, nullptr};

@@ -1132,8 +1132,8 @@ GemmPlan pair_plan(const GemmArgs& sec) {
 }
 
 lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t st) {
-  if (g0.epi != EPI_DGELU || g0.a_layout != 0 || g0.b_layout != 1 || g1.epi != EPI_STORE)
-    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: only dGELU (A [M, K], B [K, N]) with a bf16-store GEMM");
+  if ((g0.epi != EPI_DGELU && g0.epi != EPI_STORE) || g0.a_layout != 0 || g0.b_layout != 1 || g1.epi != EPI_STORE)
+    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: only a dGELU or bf16-store GEMM (A [M, K], B [K, N]) with a bf16-store GEMM");
   for (const GemmArgs* g : {&g0, &g1})
     if (g->M > 0x7FFFFFFF || g->N > 0x7FFFFFFF || g->K > 0x7FFFFFFF)
       return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: dimension above 2^31");
@@ -1150,8 +1150,13 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
   CUtensorMap maps[7];
   bool ok = make_operand_map(&maps[0], g0.a, g0.K, g0.M, BM);
   ok = ok && make_operand_map(&maps[1], g0.b, g0.N, g0.K, BK);
-  ok = ok && make_map(&maps[2], g0.out_q, 1, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
-  ok = ok && make_map(&maps[3], g0.h_in, 2, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (g0.epi == EPI_DGELU) {
+    ok = ok && make_map(&maps[2], g0.out_q, 1, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+    ok = ok && make_map(&maps[3], g0.h_in, 2, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  } else {
+    ok = ok && make_map(&maps[2], g0.out, 2, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    maps[3] = maps[2];  // no H
+  }
   ok = ok && (a1_mn ? make_operand_map(&maps[4], g1.a, g1.M, g1.K, BK) : make_operand_map(&maps[4], g1.a, g1.K, g1.M, BM));
   ok = ok && (b1_mn ? make_operand_map(&maps[5], g1.b, g1.N, g1.K, BK) : make_operand_map(&maps[5], g1.b, g1.K, g1.N, 128));
   ok = ok && make_map(&maps[6], g1.out, 2, g1.N, g1.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1172,6 +1177,7 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
     return pr;
   };
   pp.p0 = prob(g0, false, true, 1);
+  pp.bias0 = g0.bias;
   pp.p1 = prob(g1, a1_mn, b1_mn, pl.splits);
   pp.scale_q = g0.scale_q;
   pp.amax_q = g0.amax_q;
@@ -1183,10 +1189,10 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
   pp.flags = pl.splits > 1 ? reinterpret_cast<unsigned*>(g1.ws) : nullptr;
   pp.ws = pl.splits > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g1.ws) + flag_off) : nullptr;
   if ((int64_t)pp.p0.units + pp.p1.units > 0x7FFFFFFF) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: too many tiles");
-  if (g0.q_dtype == LNFP8_E4M3) {
-    if (a1_mn && b1_mn) return pair_launch_t<true, true, LNFP8_E4M3>(maps, pp, st);
-  } else {
-    if (a1_mn && b1_mn) return pair_launch_t<true, true, LNFP8_E5M2>(maps, pp, st);
+  if (a1_mn && b1_mn) {
+    if (g0.epi == EPI_STORE) return pair_launch_t<EPI_STORE, true, true, LNFP8_E4M3>(maps, pp, st);
+    if (g0.q_dtype == LNFP8_E4M3) return pair_launch_t<EPI_DGELU, true, true, LNFP8_E4M3>(maps, pp, st);
+    return pair_launch_t<EPI_DGELU, true, true, LNFP8_E5M2>(maps, pp, st);
   }
   return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: secondary layouts (%d, %d) are not built", g1.a_layout,
                    g1.b_layout);

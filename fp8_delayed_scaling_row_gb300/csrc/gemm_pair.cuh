@@ -1,6 +1,8 @@
-// Paired persistent GEMM: the FC2 data gradient with the fused dGELU epilogue
-// (the "primary") and one plain bf16-store GEMM (the "secondary", the FC2
-// weight gradient) share every CTA pair of one launch.
+// Paired persistent GEMM: two GEMMs of the backward that read the same
+// gradient codes share every CTA pair of one launch. The "primary" is a data
+// gradient (A [M, K] K-major, B [K, N]) with either the fused dGELU epilogue
+// (FC2) or a bf16 store (FC1); the "secondary" is the matching weight
+// gradient, a bf16 store with both operands [K, rows].
 //
 // The dGELU epilogue (GELU derivative, E5M2 cast, amax, column sums, the
 // read of H) takes several times longer per 256 x 256 tile than the tile's
@@ -9,6 +11,8 @@
 // epilogue. Here each CTA pair walks one schedule: a primary tile, then a
 // slice of its secondary tiles' K blocks, then the next primary tile, ... so
 // the MMAs of the secondary run while the epilogue warps work on the primary.
+// With a bf16-store primary the pairing evens out the two GEMMs' tile counts
+// over the SMs instead (neither fills a whole number of waves alone).
 // Tensor memory holds one primary accumulator (columns 0-255) and one
 // secondary accumulator (256-511); all 16 epilogue warps drain each tile
 // (warp quarter q reads TMEM lanes 32q.., warp slice s the tile's columns
@@ -43,7 +47,8 @@ struct PairProb {
 };
 
 struct PairParams {
-  PairProb p0, p1;  // primary (dGELU), secondary (bf16 store)
+  PairProb p0, p1;  // primary (dGELU or bf16 store), secondary (bf16 store)
+  const uint16_t* bias0;  // primary bias (bf16-store primary)
   // primary epilogue
   const float* scale_q;
   float* amax_q;
@@ -110,10 +115,10 @@ struct SecCursor {
   }
 };
 
-template <bool A1_MN, bool B1_MN, int QDT>
+template <int PEPI, bool A1_MN, bool B1_MN, int QDT>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
-            const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmH0,
+            const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmH0,
             const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
             const __grid_constant__ CUtensorMap tmO1, const PairParams p) {
   using C = PairCfg;
@@ -306,7 +311,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
     bool h_pending = false;
     const float s0 = __fmul_rn(*p.p0.sinv_a, *p.p0.sinv_b);
     const float s1 = __fmul_rn(*p.p1.sinv_a, *p.p1.sinv_b);
-    const float scale_q = *p.scale_q;
+    const float scale_q = PEPI == EPI_DGELU ? *p.scale_q : 0.f;
     float am_f = 0.f;
     uint32_t acc_phase[2] = {0u, 0u};
     const bool combiner = p.colsum != nullptr && quarter == 0;
@@ -314,7 +319,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
     // H prefetch: this warp's two chunks of each of the cluster's primary tiles, one chunk ahead
     int h_i = 0, h_ch = 0;
     auto issue_h = [&]() {
-      if (h_i >= sc.nP) return;
+      if (PEPI != EPI_DGELU || h_i >= sc.nP) return;
       const int u = sc.p_unit(h_i);
       if (lane == 0) {
         mbar_arrive_expect_tx(hbar, 2048);
@@ -407,7 +412,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) {
           const int y = m_blk * BM + quarter * 32;
-          if (y < p.p0.M) tma_store_2d(&tmQ0, sq_a, (int)n0, y);
+          if (y < p.p0.M) tma_store_2d(&tmX0, sq_a, (int)n0, y);
           bulk_commit();
         }
         if (p.colsum) csred[quarter * BN + col0 + lane] = transpose_reduce32(v, lane);
@@ -429,8 +434,9 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
       return true;
     };
 
-    // secondary tile (bf16 store); with two K pieces the halves exchange chunks:
-    // piece q finishes chunk q of every warp's pair and spills the other
+    // bf16-store tile in accumulator buffer b; with two K pieces (secondary
+    // only) the halves exchange chunks: piece q finishes chunk q of every
+    // warp's pair and spills the other
     auto slot_ptr = [&](int m_blk, int n_blk, int ch) {
       const int64_t t = (int64_t)m_blk * p.p1.num_n + n_blk;
       return reinterpret_cast<uint4*>(p.ws + t * (int64_t)(BM * BN)) + ((ew * 2 + ch) * 8) * 32 + lane;
@@ -438,17 +444,15 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
     auto flag_ptr = [&](int m_blk, int n_blk, int q) {
       return p.flags + (((int64_t)m_blk * p.p1.num_n + n_blk) * 2 + q) * kEpiWarps + ew;
     };
-    auto sec_tile = [&](int v) -> bool {
-      const int m_blk = s_m(v), n_blk = s_n(v);
-      const int sp = p.splits1 > 1 ? v % p.splits1 : 0;
-      if (!mbar_wait(tfull_bar(1), acc_phase[1], abort_flag)) return false;
+    auto store_tile = [&](int b, int m_blk, int n_blk, int sp, int splits, const CUtensorMap* tmO,
+                          const uint16_t* bias, int N, int M, float sc_ab) -> bool {
+      if (!mbar_wait(tfull_bar(b), acc_phase[b], abort_flag)) return false;
       tc_fence_after();
-      const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
-      (void)m;
-      if (p.splits1 > 1) {
+      const uint32_t col_base = (uint32_t)(b * 256);
+      if (splits > 1) {
         const int ch = 1 - sp;
         uint32_t rr[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(256 + slice * 64 + ch * 32), rr);
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + col_base + (uint32_t)(slice * 64 + ch * 32), rr);
         uint4* dst = slot_ptr(m_blk, n_blk, ch);
 #pragma unroll
         for (int j = 0; j < 8; ++j) __stcg(dst + j * 32, make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]));
@@ -483,7 +487,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) *const_cast<unsigned*>(f) = 0u;
       }
-      const int ch_first = p.splits1 > 1 ? sp : 0, ch_step = p.splits1 > 1 ? 2 : 1;
+      const int ch_first = splits > 1 ? sp : 0, ch_step = splits > 1 ? 2 : 1;
 #pragma unroll 1
       for (int ch = ch_first; ch < 2; ch += ch_step) {
         const int col0 = slice * 64 + ch * 32;
@@ -491,16 +495,16 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         uint4 bias8[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-          bias8[g] = p.bias1 && n0 + g * 8 < p.p1.N ? __ldg(reinterpret_cast<const uint4*>(p.bias1 + n0 + g * 8))
-                                                    : make_uint4(0u, 0u, 0u, 0u);
+          bias8[g] = bias && n0 + g * 8 < N ? __ldg(reinterpret_cast<const uint4*>(bias + n0 + g * 8))
+                                            : make_uint4(0u, 0u, 0u, 0u);
         uint32_t rr[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(256 + col0), rr);
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + col_base + (uint32_t)col0, rr);
         if (ch + ch_step >= 2) {  // the last load of this warp: release the accumulator
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_remote(tempty1);
+          if (lane == 0) mbar_arrive_remote(b ? tempty1 : tempty0);
         }
-        if (p.splits1 > 1) {  // part_0 + part_1 (fp32 addition commutes)
+        if (splits > 1) {  // part_0 + part_1 (fp32 addition commutes)
           const uint4* src = slot_ptr(m_blk, n_blk, ch);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -512,7 +516,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
           }
         }
         uint4 ob[4];
-        const uint64_t s2 = f2(s1, s1);
+        const uint64_t s2 = f2(sc_ab, sc_ab);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const uint4 bu = bias8[g];
@@ -534,21 +538,27 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) {
           const int y = m_blk * BM + quarter * 32;
-          if (y < p.p1.M) tma_store_2d(&tmO1, so_a, (int)n0, y);
+          if (y < M) tma_store_2d(tmO, so_a, (int)n0, y);
           bulk_commit();
         }
       }
-      acc_phase[1] ^= 1;
+      acc_phase[b] ^= 1;
       return true;
     };
 
     SecCursor cur;
     bool ok = true;
     for (int i = 0; i < sc.gaps() && ok; ++i) {
-      if (i < sc.nP) ok = prim_tile(sc.p_unit(i));
+      if (i < sc.nP) {
+        const int u = sc.p_unit(i);
+        if constexpr (PEPI == EPI_DGELU) ok = prim_tile(u);
+        else ok = store_tile(0, p_m(u), p_n(u), 0, 1, &tmX0, p.bias0, p.p0.N, p.p0.M, s0);
+      }
       if (ok)
         ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int v, int, int, bool, bool last) {
-          return last ? sec_tile(v) : true;
+          return last ? store_tile(1, s_m(v), s_n(v), p.splits1 > 1 ? v % p.splits1 : 0, p.splits1, &tmO1, p.bias1,
+                                   p.p1.N, p.p1.M, s1)
+                      : true;
         });
     }
     if (h_pending) {  // a prefetch may be in flight (the last one, or after an abort)
@@ -572,9 +582,9 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
   cluster_sync();
 }
 
-template <bool A1_MN, bool B1_MN, int QDT>
+template <int PEPI, bool A1_MN, bool B1_MN, int QDT>
 lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaStream_t st) {
-  auto k = pair_kernel<A1_MN, B1_MN, QDT>;
+  auto k = pair_kernel<PEPI, A1_MN, B1_MN, QDT>;
   static bool smem_set = false;
   if (!smem_set) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM) != cudaSuccess)
@@ -608,7 +618,8 @@ lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaSt
   if (pp.splits1 > 1 && clusters < 2) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: split on one cluster");
   cfg.gridDim = dim3(clusters * CL);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  LaunchScope ls("gemm_dgelu_wgrad", st);
+  static const char* kind = PEPI == EPI_DGELU ? "gemm_dgelu_wgrad" : "gemm_dgrad_wgrad";
+  LaunchScope ls(kind, st);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], pp);
   if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8 gemm pair launch: %s", cudaGetErrorString(e));
   return check_launch("fp8 gemm pair");
