@@ -114,18 +114,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def gemm_sources_sha1():
+    h = hashlib.sha1()
+    for f in ("gemm.cu", "gemm_pair.cuh"):
+        h.update(open(os.path.join(ROOT, "fp8_delayed_scaling_row_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def gemm_traffic_from_profile():
-    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if the
-    kernel source is unchanged since it was captured (else None)."""
+    """DRAM bytes of one step's GEMM launches from the committed ncu summary, if
+    the GEMM sources are unchanged since it was captured (else None)."""
     p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        src = open(os.path.join(ROOT, "fp8_delayed_scaling_row_gb300", "csrc", "gemm.cu"), "rb").read()
-        if d.get("gemm_cu_sha1") != hashlib.sha1(src).hexdigest():
+        if d.get("gemm_sources_sha1") != gemm_sources_sha1():
             return None
-        return d.get("bytes_per_launch_step_avg")
+        return d.get("dram_bytes_per_step")
     except Exception:
         return None
 
@@ -370,19 +376,22 @@ def run_gpu(args):
             run._call(run.xs[i % len(run.xs)], run.dys[i % len(run.dys)])
         prof = L.profile_collect()
         L.profile_enable(False)
+    # the GEMM family: FC1 (+GELU), FC2, and the two backward launches that each run a data
+    # gradient and its weight gradient together; one "launch" of the family = one step's set
     gemm_kinds = {k: v for k, v in prof.items() if k.startswith("gemm")}
     g_ms = sum(v[0] for v in gemm_kinds.values())
     g_n = sum(v[1] for v in gemm_kinds.values())
     pk, how = peaks()
     bf16 = _num(pk, "bf16_tflops", "bf16_tflops_burst") or FALLBACK["bf16_tflops"]
     fp8_peak = bf16 * FP8_PER_BF16
-    g_flops = 2.0 * M_TOK * D_MODEL * FFN
-    achieved = g_flops / (g_ms / g_n / 1e3) / 1e12 if g_n else None
-    roofline = {"kernel": "fp8_gemm (tcgen05 kind::f8f6f4; the six GEMMs of the step)", "bound": "tensor",
-                "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+    g_flops = flops_per_step()  # the six GEMMs, 2 * M * D * F each
+    achieved = g_flops / (g_ms / prof_steps / 1e3) / 1e12 if g_n else None
+    roofline = {"kernel": "fp8 GEMM family (tcgen05 kind::f8f6f4): the step's six GEMMs in four launches",
+                "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak if achieved else None, "traffic": gemm_traffic_from_profile(),
                 "peak_source": f"{how} bf16 dense x {FP8_PER_BF16:g} (nominal FP8/BF16 ratio)",
-                "flops_per_launch": g_flops, "launches_timed": g_n, "timed_from": prof_how,
+                "flops_per_launch": g_flops, "launch": "one step's GEMM launches (summed device time)",
+                "gemm_launches_per_step": g_n / prof_steps, "launches_timed": g_n, "timed_from": prof_how,
                 "share_of_step": g_ms / sum(v[0] for v in prof.values()) if prof else None}
     hbm = _num(pk, "hbm_gbs", "hbm_GBs", "hbm_copy_gbs") or FALLBACK["hbm_gbs"]
     per_kernel = {}
