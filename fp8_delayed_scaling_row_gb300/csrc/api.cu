@@ -447,6 +447,13 @@ lnfp8_status fp8_gemm(const uint8_t* A, int a_layout, int a_dtype, const uint8_t
   return gemm_launch(g, (cudaStream_t)stream);
 }
 
+int64_t lnfp8_ln_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t F) {
+  if (M < 0 || D < 0 || F < 0) return -1;
+  if (M == 0 || D == 0 || F == 0) return 0;
+  const int64_t num_m2 = ((M + 127) / 128 + 1) / 2;  // one counter per 256-row block
+  return ((num_m2 * 4 + 255) / 256) * 256;
+}
+
 int64_t lnfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return -1;
   return gemm_plan(M, N, K, EPI_STORE, true).ws_bytes;
@@ -612,10 +619,14 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
     REQ(a->h, who);
     REQ(a->aq, who);
   }
+  OPT(a->gemm_ws, who);
   const int fdt = fwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
+  // FC1 and FC2 in one launch when the caller gave room for the FC1 tiles' readiness counters
+  const int64_t ready_bytes = lnfp8_ln_mlp_fwd_workspace_size(a->M, a->D, a->F);
+  const bool fused = a->M > 0 && a->gemm_ws && ready_bytes > 0 && a->gemm_ws_bytes >= ready_bytes && !pair_disabled();
   TRY(cast2_launch(a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q, a->w2, a->D, a->F, m.scale + 3,
-                   m.amax_cur + 3, a->w2q, fdt, st));
+                   m.amax_cur + 3, a->w2q, fdt, st, fused ? a->gemm_ws : nullptr, fused ? ready_bytes : 0));
   TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
                     a->rsigma, a->ln_out_debug, st));
   GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0, m.scale_inv + 1);
@@ -627,11 +638,17 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   f1.scale_q = m.scale + 2;
   f1.amax_q = m.amax_cur + 2;
   f1.dbg = a->act_debug;
-  TRY(gemm_launch(f1, st));
   GemmArgs f2 = gemm_args(a->aq, 0, fdt, a->w2q, 0, fdt, a->M, a->D, a->F, m.scale_inv + 2, m.scale_inv + 3);
   f2.bias = a->b2;
   f2.out = a->y;
-  TRY(gemm_launch(f2, st));
+  if (fused) {
+    f1.ws = a->gemm_ws;
+    f1.ws_bytes = a->gemm_ws_bytes;
+    TRY(gemm_pair_launch(f1, f2, st));
+  } else {
+    TRY(gemm_launch(f1, st));
+    TRY(gemm_launch(f2, st));
+  }
   return finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st);
 }
 

@@ -1132,8 +1132,9 @@ GemmPlan pair_plan(const GemmArgs& sec) {
 }
 
 lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream_t st) {
-  if ((g0.epi != EPI_DGELU && g0.epi != EPI_STORE) || g0.a_layout != 0 || g0.b_layout != 1 || g1.epi != EPI_STORE)
-    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: only a dGELU or bf16-store GEMM (A [M, K], B [K, N]) with a bf16-store GEMM");
+  const bool fwd = g0.epi == EPI_GELU;  // FC1 (B [N, K]) with FC2 (both operands K-major)
+  if (g0.a_layout != 0 || g1.epi != EPI_STORE || (fwd ? g0.b_layout != 0 : (g0.b_layout != 1 || (g0.epi != EPI_DGELU && g0.epi != EPI_STORE))))
+    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: unsupported primary epilogue or layouts");
   for (const GemmArgs* g : {&g0, &g1})
     if (g->M > 0x7FFFFFFF || g->N > 0x7FFFFFFF || g->K > 0x7FFFFFFF)
       return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: dimension above 2^31");
@@ -1149,8 +1150,11 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
 
   CUtensorMap maps[7];
   bool ok = make_operand_map(&maps[0], g0.a, g0.K, g0.M, BM);
-  ok = ok && make_operand_map(&maps[1], g0.b, g0.N, g0.K, BK);
-  if (g0.epi == EPI_DGELU) {
+  ok = ok && (fwd ? make_operand_map(&maps[1], g0.b, g0.K, g0.N, 128) : make_operand_map(&maps[1], g0.b, g0.N, g0.K, BK));
+  if (fwd) {
+    ok = ok && make_map(&maps[2], g0.out_q, 1, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+    ok = ok && make_map(&maps[3], g0.out, 2, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  } else if (g0.epi == EPI_DGELU) {
     ok = ok && make_map(&maps[2], g0.out_q, 1, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_32B);
     ok = ok && make_map(&maps[3], g0.h_in, 2, g0.N, g0.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
@@ -1176,7 +1180,7 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
     pr.sinv_b = g.sinv_b;
     return pr;
   };
-  pp.p0 = prob(g0, false, true, 1);
+  pp.p0 = prob(g0, false, !fwd, 1);
   pp.bias0 = g0.bias;
   pp.p1 = prob(g1, a1_mn, b1_mn, pl.splits);
   pp.scale_q = g0.scale_q;
@@ -1187,12 +1191,22 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
   pp.splits1 = pl.splits;
   pp.kbs1 = pl.kb_per_split;
   pp.flags = pl.splits > 1 ? reinterpret_cast<unsigned*>(g1.ws) : nullptr;
+  pp.ready = nullptr;
+  if (fwd) {  // per row block readiness counters in g0's workspace (zeroed by the caller)
+    if (pl.splits != 1 || !g0.ws || g0.ws_bytes < (int64_t)pp.p0.num_m2 * 4)
+      return set_error(LNFP8_ERR_INVALID_ARG, "fp8 gemm pair: the forward needs its readiness counters and no K split");
+    pp.ready = reinterpret_cast<unsigned*>(g0.ws);
+  }
   pp.ws = pl.splits > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g1.ws) + flag_off) : nullptr;
   if ((int64_t)pp.p0.units + pp.p1.units > 0x7FFFFFFF) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm pair: too many tiles");
-  if (a1_mn && b1_mn) {
-    if (g0.epi == EPI_STORE) return pair_launch_t<EPI_STORE, true, true, LNFP8_E4M3>(maps, pp, st);
-    if (g0.q_dtype == LNFP8_E4M3) return pair_launch_t<EPI_DGELU, true, true, LNFP8_E4M3>(maps, pp, st);
-    return pair_launch_t<EPI_DGELU, true, true, LNFP8_E5M2>(maps, pp, st);
+  if (fwd && !a1_mn && !b1_mn) {
+    if (g0.q_dtype == LNFP8_E4M3) return pair_launch_t<EPI_GELU, false, false, false, LNFP8_E4M3>(maps, pp, st);
+    return pair_launch_t<EPI_GELU, false, false, false, LNFP8_E5M2>(maps, pp, st);
+  }
+  if (!fwd && a1_mn && b1_mn) {
+    if (g0.epi == EPI_STORE) return pair_launch_t<EPI_STORE, true, true, true, LNFP8_E4M3>(maps, pp, st);
+    if (g0.q_dtype == LNFP8_E4M3) return pair_launch_t<EPI_DGELU, true, true, true, LNFP8_E4M3>(maps, pp, st);
+    return pair_launch_t<EPI_DGELU, true, true, true, LNFP8_E5M2>(maps, pp, st);
   }
   return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: secondary layouts (%d, %d) are not built", g1.a_layout,
                    g1.b_layout);

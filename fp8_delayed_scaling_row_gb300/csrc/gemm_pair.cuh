@@ -1,8 +1,12 @@
-// Paired persistent GEMM: two GEMMs of the backward that read the same
-// gradient codes share every CTA pair of one launch. The "primary" is a data
-// gradient (A [M, K] K-major, B [K, N]) with either the fused dGELU epilogue
-// (FC2) or a bf16 store (FC1); the "secondary" is the matching weight
-// gradient, a bf16 store with both operands [K, rows].
+// Paired persistent GEMM: two independent GEMMs share every CTA pair of one
+// launch. In the backward the "primary" is a data gradient (A [M, K] K-major,
+// B [K, N]) with either the fused dGELU epilogue (FC2) or a bf16 store (FC1),
+// and the "secondary" the matching weight gradient, a bf16 store with both
+// operands [K, rows]. In the forward the primary is FC1 with the GELU epilogue
+// on one half of the token rows and the secondary FC2 (both operands K-major)
+// on the same rows: FC2 tile (rows r, columns n) reads the GELU codes that the
+// FC1 tiles of rows r write in this launch, so the launch orders its work by
+// row blocks and FC2's loads wait (bounded) on per-tile readiness counters.
 //
 // The dGELU epilogue (GELU derivative, E5M2 cast, amax, column sums, the
 // read of H) takes several times longer per 256 x 256 tile than the tile's
@@ -59,7 +63,20 @@ struct PairParams {
   int splits1, kbs1;  // K pieces per secondary tile (1 or 2) and K blocks per piece
   float* ws;          // split exchange: [tile][warp][chunk][8][32] x 16 B
   unsigned* flags;    // [tile][piece][warp]
+  unsigned* ready;    // forward: per row block, the epilogue warps (both CTAs, every FC1 tile) done with its codes; zero at launch
 };
+
+// Forward dependency order (GELU primary): primary tiles run row block by row
+// block (N fastest) and secondary (FC2) tiles row block major. A secondary tile
+// may start in the gap one round after the round in which the last FC1 tile of
+// its row block runs: every wait then points at work earlier in every CTA
+// pair's schedule (no cycles), and by the time a producer gets there those
+// tiles' epilogues have usually finished on all SMs, so the wait rarely holds
+// up the next FC1 tile's loads.
+__device__ __forceinline__ int fwd_release_round(const PairParams& p, int v, int ncl) {
+  const int m2 = (v / p.splits1) / p.p1.num_n;
+  return (p.p0.num_n * (m2 + 1) - 1) / ncl + 1;
+}
 
 // The schedule of one cluster. Its work units are the global units c, c + ncl,
 // ... where global units 0..U0-1 are the primary tiles and the rest the
@@ -96,10 +113,14 @@ struct SecCursor {
   int j = 0;         // local index of the current secondary unit
   int64_t jo = 0;    // schedule offset where it starts
   int64_t off = 0;   // next offset to run
+  // gap: the gap index (for the forward's release rule); dep: forward dependency order
   template <class F>
-  __device__ bool run_gap(const PairSched& sc, const PairParams& p, int64_t end, F&& seg) {
+  __device__ bool run_gap(const PairSched& sc, const PairParams& p, int64_t end, F&& seg, int gap = 0, bool dep = false) {
+    const bool last_gap = gap == sc.gaps() - 1;
+    if (dep && last_gap) end = sc.KS;
     while (off < end) {
       const int v = sc.s_unit(j);
+      if (dep && off == jo && !last_gap && fwd_release_round(p, v, sc.ncl) > gap) break;  // not released yet
       const int len = PairSched::s_len(p, v);
       const int64_t seg_end = min(end, jo + len);
       const int k0 = PairSched::s_kb0(p, v);
@@ -115,7 +136,7 @@ struct SecCursor {
   }
 };
 
-template <int PEPI, bool A1_MN, bool B1_MN, int QDT>
+template <int PEPI, bool B0_MN, bool A1_MN, bool B1_MN, int QDT>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
             const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmH0,
@@ -184,10 +205,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
   PairSched sc;
   sc.init(p, cid, ncl);
   // tile coordinates: primary unit u = tile; secondary unit v = tile * splits1 + piece
-  auto p_m = [&](int u) { return (u % p.p0.num_m2) * CL + rank; };
-  auto p_n = [&](int u) { return u / p.p0.num_m2; };
-  auto s_m = [&](int v) { return ((v / p.splits1) % p.p1.num_m2) * CL + rank; };
-  auto s_n = [&](int v) { return (v / p.splits1) / p.p1.num_m2; };
+  constexpr bool DEP = PEPI == EPI_GELU;  // forward: FC2 depends on this launch's FC1 output
+  auto p_m = [&](int u) { return (DEP ? u / p.p0.num_n : u % p.p0.num_m2) * CL + rank; };
+  auto p_n = [&](int u) { return DEP ? u % p.p0.num_n : u / p.p0.num_m2; };
+  auto s_m = [&](int v) { return (DEP ? (v / p.splits1) / p.p1.num_n : (v / p.splits1) % p.p1.num_m2) * CL + rank; };
+  auto s_n = [&](int v) { return DEP ? (v / p.splits1) % p.p1.num_n : (v / p.splits1) / p.p1.num_m2; };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -203,9 +225,10 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         const uint32_t a_dst = smem_u32(smem + stage * C::STAGE_BYTES);
         const uint32_t b_dst = a_dst + C::A_BYTES;
         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
-        if (prim) {  // dY codes [M, D] K-major; W2 codes [D, F] = [K, N] MN-major
+        if (prim) {  // A [M, K] K-major; B [K, N] (backward) or [N, K] (forward FC1)
           tma_load_2d_cg2(a_dst, &tmA0, kb * BK, m_blk * BM, fl);
-          tma_load_2d_cg2(b_dst, &tmB0, n_blk * BN + rank * 128, kb * BK, fl);
+          if (B0_MN) tma_load_2d_cg2(b_dst, &tmB0, n_blk * BN + rank * 128, kb * BK, fl);
+          else       tma_load_2d_cg2(b_dst, &tmB0, kb * BK, n_blk * BN + rank * 128, fl);
         } else {
           if (!A1_MN) tma_load_2d_cg2(a_dst, &tmA1, kb * BK, m_blk * BM, fl);
           else        tma_load_2d_cg2(a_dst, &tmA1, m_blk * BM, kb * BK, fl);
@@ -216,6 +239,30 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
         return true;
       };
+      // forward: wait (bounded) until every FC1 tile of the row block has written its GELU codes
+      int dep_ok = -1;
+      auto wait_ready = [&](int u_dep) {
+        if (u_dep == dep_ok) return true;
+        const unsigned* f = p.ready + u_dep;
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 0;; ++it) {
+          unsigned v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+          if (v >= 2u * kEpiWarps * (unsigned)p.p0.num_n) break;
+          if ((it & 15) == 15) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > 1000000000ull) {
+              *abort_flag = 1;
+              atomicOr(&g_status, kStatusTimeout);
+              return false;
+            }
+          }
+        }
+        // the codes were written by TMA stores: order the acquire before this thread's TMA loads
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        dep_ok = u_dep;
+        return true;
+      };
       SecCursor cur;
       for (int i = 0; i < sc.gaps() && ok; ++i) {
         if (i < sc.nP) {
@@ -224,10 +271,12 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         }
         if (ok)
           ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int v, int k0, int k1, bool, bool) {
-            for (int kb = k0; kb < k1; ++kb)
+            for (int kb = k0; kb < k1; ++kb) {
+              if (DEP && !wait_ready((v / p.splits1) / p.p1.num_n)) return false;
               if (!load(false, s_m(v), s_n(v), kb)) return false;
+            }
             return true;
-          });
+          }, i, DEP);
       }
       if (!ok && rank == 0) {
         const int64_t pending = issued < STAGES ? issued : STAGES;
@@ -258,7 +307,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint32_t accum = !(fresh && kb == k0 && kk == 0);
-            const bool a_mn = prim ? false : A1_MN, b_mn = prim ? true : B1_MN;
+            const bool a_mn = prim ? false : A1_MN, b_mn = prim ? B0_MN : B1_MN;
             const uint64_t ad = a_mn ? make_desc(a_base + kk * 32 * 128, 1024, 1024) : make_desc(a_base + kk * 32, 16, 1024);
             const uint64_t bd = b_mn ? make_desc(b_base + kk * 32 * 128, 1024, 1024) : make_desc(b_base + kk * 32, 16, 1024);
             mma_f8_cg2(d_tmem, ad, bd, idesc, accum);
@@ -288,7 +337,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
             acc_phase[1] ^= 1;
           }
           return true;
-        });
+        }, i, DEP);
       }
       if (!ok) {
         mma_commit_cg2_mc(drain_bar, 1);
@@ -311,7 +360,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
     bool h_pending = false;
     const float s0 = __fmul_rn(*p.p0.sinv_a, *p.p0.sinv_b);
     const float s1 = __fmul_rn(*p.p1.sinv_a, *p.p1.sinv_b);
-    const float scale_q = PEPI == EPI_DGELU ? *p.scale_q : 0.f;
+    const float scale_q = PEPI != EPI_STORE ? *p.scale_q : 0.f;
     float am_f = 0.f;
     uint32_t acc_phase[2] = {0u, 0u};
     const bool combiner = p.colsum != nullptr && quarter == 0;
@@ -434,6 +483,96 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
       return true;
     };
 
+    // FC1 tile with the GELU epilogue: h = bf16(acc * s + b1) leaves through
+    // tmH0, a = gelu_tanh(h) folds into the amax and leaves as codes through tmX0
+    auto gelu_tile = [&](int u) -> bool {
+      const int m_blk = p_m(u), n_blk = p_n(u);
+      if (!mbar_wait(tfull_bar(0), acc_phase[0], abort_flag)) return false;
+      tc_fence_after();
+      const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
+      const bool row_ok = m < p.p0.M;
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col0 = slice * 64 + ch * 32;
+        const int64_t n0 = (int64_t)n_blk * BN + col0;
+        uint4 bias8[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          bias8[g] = p.bias0 && n0 + g * 8 < p.p0.N ? __ldg(reinterpret_cast<const uint4*>(p.bias0 + n0 + g * 8))
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t rr[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0, rr);
+        if (ch == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(tempty0);
+        }
+        uint4 ob[4];
+        uint2 oq[4];
+        const uint64_t s2 = f2(s0, s0);
+        const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC), H2 = f2(0.5f, 0.5f);
+        const uint64_t q2 = f2(scale_q, scale_q);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int64_t n = n0 + g * 8;
+          const bool ok = row_ok && n < p.p0.N;
+          const uint4 bu = bias8[g];
+          const uint64_t b2[4] = {bf2_to_f2(bu.x), bf2_to_f2(bu.y), bf2_to_f2(bu.z), bf2_to_f2(bu.w)};
+          uint32_t hw[4];
+          uint64_t a2[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint64_t e2 = f2(__uint_as_float(rr[g * 8 + 2 * i]), __uint_as_float(rr[g * 8 + 2 * i + 1]));
+            const uint64_t hf = fma2(e2, s2, b2[i]);
+            hw[i] = pack_bf16x2(lo(hf), hi(hf));
+            const uint64_t h = bf2_to_f2(hw[i]);
+            const uint64_t uu = mul2(h, fma2(mul2(h, h), KC2, K2));
+            const uint64_t t = f2(tanh_fast(lo(uu)), tanh_fast(hi(uu)));
+            const uint64_t hh = mul2(h, H2);
+            a2[i] = fma2(hh, t, hh);
+          }
+          if (ok) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(a2[i])), hi(a2[i]));
+            if (p.dbg) {
+              float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.p0.N + n);
+              d4[0] = make_float4(lo(a2[0]), hi(a2[0]), lo(a2[1]), hi(a2[1]));
+              d4[1] = make_float4(lo(a2[2]), hi(a2[2]), lo(a2[3]), hi(a2[3]));
+            }
+          }
+          ob[g] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          oq[g].x = (uint32_t)cvt_pair<QDT>(mul2(a2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[1], q2)) << 16);
+          oq[g].y = (uint32_t)cvt_pair<QDT>(mul2(a2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[3], q2)) << 16);
+        }
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(so + sw64(r, j)) = ob[j];
+        *reinterpret_cast<uint4*>(sq + sw32(r, 0)) = make_uint4(oq[0].x, oq[0].y, oq[1].x, oq[1].y);
+        *reinterpret_cast<uint4*>(sq + sw32(r, 1)) = make_uint4(oq[2].x, oq[2].y, oq[3].x, oq[3].y);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int y = m_blk * BM + quarter * 32;
+          if (y < p.p0.M) {
+            tma_store_2d(&tmH0, so_a, (int)n0, y);
+            tma_store_2d(&tmX0, sq_a, (int)n0, y);
+          }
+          bulk_commit();
+        }
+      }
+      // this warp's codes of the tile are written: count it towards the tile's readiness
+      if (lane == 0) {
+        bulk_wait0();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.ready + u / p.p0.num_n) : "memory");
+      }
+      __syncwarp();
+      acc_phase[0] ^= 1;
+      return true;
+    };
+
     // bf16-store tile in accumulator buffer b; with two K pieces (secondary
     // only) the halves exchange chunks: piece q finishes chunk q of every
     // warp's pair and spills the other
@@ -552,6 +691,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
       if (i < sc.nP) {
         const int u = sc.p_unit(i);
         if constexpr (PEPI == EPI_DGELU) ok = prim_tile(u);
+        else if constexpr (PEPI == EPI_GELU) ok = gelu_tile(u);
         else ok = store_tile(0, p_m(u), p_n(u), 0, 1, &tmX0, p.bias0, p.p0.N, p.p0.M, s0);
       }
       if (ok)
@@ -559,7 +699,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
           return last ? store_tile(1, s_m(v), s_n(v), p.splits1 > 1 ? v % p.splits1 : 0, p.splits1, &tmO1, p.bias1,
                                    p.p1.N, p.p1.M, s1)
                       : true;
-        });
+        }, i, DEP);
     }
     if (h_pending) {  // a prefetch may be in flight (the last one, or after an abort)
       uint32_t dummy_flag = 0;
@@ -582,9 +722,9 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
   cluster_sync();
 }
 
-template <int PEPI, bool A1_MN, bool B1_MN, int QDT>
+template <int PEPI, bool B0_MN, bool A1_MN, bool B1_MN, int QDT>
 lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaStream_t st) {
-  auto k = pair_kernel<PEPI, A1_MN, B1_MN, QDT>;
+  auto k = pair_kernel<PEPI, B0_MN, A1_MN, B1_MN, QDT>;
   static bool smem_set = false;
   if (!smem_set) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM) != cudaSuccess)
@@ -618,7 +758,7 @@ lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaSt
   if (pp.splits1 > 1 && clusters < 2) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: split on one cluster");
   cfg.gridDim = dim3(clusters * CL);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  static const char* kind = PEPI == EPI_DGELU ? "gemm_dgelu_wgrad" : "gemm_dgrad_wgrad";
+  static const char* kind = PEPI == EPI_DGELU ? "gemm_dgelu_wgrad" : PEPI == EPI_GELU ? "gemm_gelu_fc2" : "gemm_dgrad_wgrad";
   LaunchScope ls(kind, st);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], pp);
   if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8 gemm pair launch: %s", cudaGetErrorString(e));

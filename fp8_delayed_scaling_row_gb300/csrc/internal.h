@@ -26,7 +26,8 @@ lnfp8_status zero_launch(std::initializer_list<std::pair<void*, int64_t>> spans,
 
 lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
                           uint8_t* out0, const uint16_t* in1, int64_t rows1, int64_t cols1, const float* scale1,
-                          float* amax1, uint8_t* out1, int dtype, cudaStream_t st);
+                          float* amax1, uint8_t* out1, int dtype, cudaStream_t st, void* zero = nullptr,
+                          int64_t zero_bytes = 0);
 
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,

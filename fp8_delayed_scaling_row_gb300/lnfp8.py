@@ -32,7 +32,7 @@ EXPORTED = [
     "lnfp8_profile_enable", "lnfp8_profile_sample", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
     "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
     "ln_linear_bwd_noalloc", "ln_mlp_fwd", "ln_mlp_bwd", "lnfp8_gemm_workspace_size",
-    "lnfp8_ln_linear_bwd_workspace_size", "lnfp8_ln_mlp_bwd_workspace_size",
+    "lnfp8_ln_linear_bwd_workspace_size", "lnfp8_ln_mlp_bwd_workspace_size", "lnfp8_ln_mlp_fwd_workspace_size",
 ]
 
 
@@ -74,7 +74,8 @@ class CLnMlpFwd(C.Structure):
     _fields_ = [("M", _I64), ("D", _I64), ("F", _I64), ("x", _P), ("gamma", _P), ("beta", _P), ("eps", C.c_float),
                 ("w1", _P), ("b1", _P), ("w2", _P), ("b2", _P), ("y", _P), ("lnq", _P), ("mu", _P), ("rsigma", _P),
                 ("w1q", _P), ("w2q", _P), ("h", _P), ("aq", _P), ("sinv_saved", _P), ("meta", CMeta),
-                ("recipe", CRecipe), ("defer_update", C.c_int), ("ln_out_debug", _P), ("act_debug", _P)]
+                ("recipe", CRecipe), ("defer_update", C.c_int), ("ln_out_debug", _P), ("act_debug", _P),
+                ("gemm_ws", _P), ("gemm_ws_bytes", _I64)]
 
 
 class CLnMlpBwd(C.Structure):
@@ -113,6 +114,7 @@ _c_gemm = _sig("fp8_gemm", [_P, C.c_int, C.c_int, _P, C.c_int, C.c_int, _I64, _I
 _c_gemm_ws = _sig("lnfp8_gemm_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_lin_bwd_ws = _sig("lnfp8_ln_linear_bwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_mlp_bwd_ws = _sig("lnfp8_ln_mlp_bwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
+_c_mlp_fwd_ws = _sig("lnfp8_ln_mlp_fwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_lin_fwd = _sig("ln_linear_fwd", [C.POINTER(CLnLinearFwd), _P])
 _c_lin_bwd = _sig("ln_linear_bwd", [C.POINTER(CLnLinearBwd), _P])
 _c_lin_bwd_noalloc = _sig("ln_linear_bwd_noalloc", [C.POINTER(CLnLinearBwd), _P])
@@ -283,6 +285,10 @@ def ln_mlp_bwd_workspace_size(M, D, F) -> int:
     return int(_c_mlp_bwd_ws(M, D, F))
 
 
+def ln_mlp_fwd_workspace_size(M, D, F) -> int:
+    return int(_c_mlp_fwd_ws(M, D, F))
+
+
 def _ws(nbytes, device):
     return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
 
@@ -400,15 +406,20 @@ class MlpCtx:
     sinv_saved: torch.Tensor
     ln_out_debug: torch.Tensor | None = None
     act_debug: torch.Tensor | None = None
+    gemm_ws: torch.Tensor | None = None  # FC1 tiles' readiness counters (FC1 and FC2 in one launch)
 
 
-def mlp_ctx(M, D, F, *, device="cuda", debug=False) -> MlpCtx:
+def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False) -> MlpCtx:
+    """Saved tensors of one LayerNormMLP forward. fused=True also allocates the row-block
+    readiness counters with which the forward runs FC1 and FC2 as one launch (same
+    results; at 8192 x 768 -> 3072 -> 768 the two launches are still faster)."""
     return MlpCtx(lnq=_e((M, D), torch.uint8, device), mu=_e((M,), torch.float32, device),
                   rsigma=_e((M,), torch.float32, device), w1q=_e((F, D), torch.uint8, device),
                   w2q=_e((D, F), torch.uint8, device), h=_e((M, F), torch.bfloat16, device),
                   aq=_e((M, F), torch.uint8, device), sinv_saved=_e((4,), torch.float32, device),
                   ln_out_debug=_e((M, D), torch.float32, device) if debug else None,
-                  act_debug=_e((M, F), torch.float32, device) if debug else None)
+                  act_debug=_e((M, F), torch.float32, device) if debug else None,
+                  gemm_ws=_ws(ln_mlp_fwd_workspace_size(M, D, F), device) if fused else None)
 
 
 def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, meta: ScalingMeta, recipe: Recipe, *, eps=1e-5, y=None,
@@ -423,7 +434,8 @@ def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, meta: ScalingMeta, recipe: Recipe
                   w2=_ptr(w2), b2=_ptr(b2), y=_ptr(y), lnq=_ptr(ctx.lnq), mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma),
                   w1q=_ptr(ctx.w1q), w2q=_ptr(ctx.w2q), h=_ptr(ctx.h), aq=_ptr(ctx.aq),
                   sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(), recipe=recipe.c(), defer_update=int(defer_update),
-                  ln_out_debug=_ptr(ctx.ln_out_debug), act_debug=_ptr(ctx.act_debug))
+                  ln_out_debug=_ptr(ctx.ln_out_debug), act_debug=_ptr(ctx.act_debug), gemm_ws=_ptr(ctx.gemm_ws),
+                  gemm_ws_bytes=ctx.gemm_ws.numel() if ctx.gemm_ws is not None else 0)
     _check(_c_mlp_fwd(C.byref(a), _stream(stream)))
     return y, ctx
 

@@ -335,6 +335,8 @@ typedef struct {
   int defer_update;
   float* ln_out_debug;    /* optional [M, D] fp32 pre-cast LN output */
   float* act_debug;       /* optional [M, F] fp32 pre-cast GELU output */
+  void* gemm_ws;          /* optional, lnfp8_ln_mlp_fwd_workspace_size bytes: FC1 and FC2 run as one launch */
+  int64_t gemm_ws_bytes;
 } lnfp8_ln_mlp_fwd_args;
 
 typedef struct {
@@ -375,6 +377,14 @@ typedef struct {
  *   a = gelu_tanh(h) (fp32); aq = fp8(a * scale[2]);
  *   out = bf16((aq . w2q^T) * sinv[2]*sinv[3] + b2); then the state update. */
 lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* args, lnfp8_stream stream);
+
+/* Bytes of args->gemm_ws with which ln_mlp_fwd runs FC1 (+GELU) and FC2 as one
+ * persistent launch: FC2's tiles start as soon as the FC1 tiles of their rows
+ * are written, tracked by one counter per 256-row block in the workspace (cleared
+ * by the call's first kernel). 0 when M is 0, -1 for negative sizes. With a
+ * NULL or smaller workspace the two GEMMs run as separate launches; the
+ * results are identical. */
+int64_t lnfp8_ln_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t F);
 
 /* LayerNormMLP backward (gradients E5M2 under HYBRID):
  *   dyq = fp8(dy * gscale[0]); db2 = sum_rows dy;

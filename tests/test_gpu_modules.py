@@ -371,3 +371,27 @@ def test_mlp_backward_fc2_weight_gradient_equals_the_standalone_gemm(L, M, D, F)
     ref = L.fp8_gemm(g.dyq, 1, L.E5M2, ctx.aq, 1, L.E4M3, D, F, M, gsinv[0:1], ctx.sinv_saved[2:3])
     L.sync_status()
     assert torch.equal(g.dw2, ref)
+
+
+@pytest.mark.parametrize("M,D,F", [(8192, 768, 3072), (1000, 256, 1024), (16, 128, 384)])
+def test_mlp_forward_fused_launch_equals_two_launches(L, M, D, F):
+    """With its readiness-counter workspace the forward runs FC1 (+GELU) and FC2 as one
+    launch, FC2 tiles starting as the FC1 tiles of their rows finish. The arithmetic
+    is the same as two launches: Y, H, the GELU codes and the state match bit for bit."""
+    p = {k: bf16_dev(v) for k, v in synth.mlp_params(D, F, bias_std=0.02, seed=4).items()}
+    rec = L.Recipe("hybrid", 4)
+    outs = []
+    for fused in (True, False, True):
+        fm = L.ScalingMeta(4, 4)
+        ctx = L.mlp_ctx(M, D, F, fused=fused)
+        assert (ctx.gemm_ws is not None) == fused
+        for step in range(2):  # the second step casts with scales from the first
+            x = bf16_dev(synth.activations(M, D, dist="outliers", seed=4, step=step))
+            y, _ = L.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], fm, rec, ctx=ctx)
+        L.sync_status()
+        outs.append((y, ctx, fm))
+    for (y0, c0, m0), (y1, c1, m1) in [(outs[0], outs[1]), (outs[0], outs[2])]:
+        assert torch.equal(y0, y1)
+        assert torch.equal(c0.h, c1.h) and torch.equal(c0.aq, c1.aq)
+        for name in ("scale", "scale_inv", "amax_history"):
+            assert torch.equal(getattr(m0, name), getattr(m1, name)), name
