@@ -86,7 +86,7 @@ struct Cfg {
   static constexpr int BAR_OFF = CSUM_OFF + CSUM_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // a power of two holding both accumulators
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -939,7 +939,7 @@ uint32_t make_idesc(int m_mma, int n_mma, int a_dt, int b_dt, bool a_mn, bool b_
          ((uint32_t)(m_mma >> 4) << 24);   // M / 16
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, int QDT, bool TWO = (BN == 256)>
+template <int BN, bool A_MN, bool B_MN, int EPI, int QDT, bool TWO = (BN >= 192)>
 lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em, const KParams& kp,
                       cudaStream_t st) {
   auto k = gemm_kernel<BN, A_MN, B_MN, EPI, QDT, TWO>;
@@ -1011,7 +1011,7 @@ lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st) {
 // Splitting is considered for the bf16-store epilogue with a workspace only,
 // when all units fit in one round (the exchange then overlaps no other
 // tile's work, so it is paid once), and taken when it saves more than a tenth.
-GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split) {
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split, bool kmajor) {
   GemmPlan pl;
   const int64_t num_m = (M + BM - 1) / BM;
   const int64_t num_m2 = (num_m + CL - 1) / CL;
@@ -1035,6 +1035,11 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split) {
   }
   // without a split, 128-wide single-SM tiles when 256-wide ones leave most SMs idle
   if (pl.splits == 1 && epi == EPI_STORE && num_m * ((N + 255) / 256) < (int64_t)num_sms()) pl.bn = 128;
+  // 192-wide pair tiles (A and B K-major, N a multiple of 192) when their rounds of 3/4-size tiles take less time
+  if (pl.splits == 1 && pl.bn == 256 && epi == EPI_STORE && kmajor && N % 192 == 0) {
+    const int64_t r256 = (tiles + clusters - 1) / clusters, r192 = (num_m2 * (N / 192) + clusters - 1) / clusters;
+    if (4 * 3 * r192 < 4 * 4 * r256 * 9 / 10) pl.bn = 192;
+  }
   pl.kb_per_split = (int)((num_kb + pl.splits - 1) / pl.splits);
   const int64_t rows = num_m2 * CL, cols = (N + pl.bn - 1) / pl.bn;
   pl.flag_bytes = pl.splits > 1 ? ((pl.splits * rows * cols * 8 * 4 + 255) / 256) * 256 : 0;
@@ -1049,11 +1054,12 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm: dimension above 2^31");
   const bool a_mn = g.a_layout == 1, b_mn = g.b_layout == 1;
   const int64_t num_m = (g.M + BM - 1) / BM;
-  GemmPlan pl = gemm_plan(g.M, g.N, g.K, g.epi, g.ws != nullptr);
+  // the 192-wide tiles are built for K-major A and B only
+  GemmPlan pl = gemm_plan(g.M, g.N, g.K, g.epi, g.ws != nullptr, !a_mn && !b_mn);
   // the slots start after the flag area, which the caller may size for several GEMMs
   const int64_t flag_off = g.ws_flag_bytes > 0 ? g.ws_flag_bytes : pl.flag_bytes;
   if (pl.splits > 1 && (flag_off < pl.flag_bytes || flag_off % 256 || g.ws_bytes < flag_off + pl.slot_bytes))
-    pl = gemm_plan(g.M, g.N, g.K, g.epi, false);
+    pl = gemm_plan(g.M, g.N, g.K, g.epi, false, !a_mn && !b_mn);
   const int bn = pl.bn;
   const int64_t num_n = (g.N + bn - 1) / bn;
   if (num_m * num_n > 0x7FFFFFFF) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8 gemm: too many tiles");
@@ -1063,7 +1069,7 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   bool ok = a_mn ? make_operand_map(&ta, g.a, g.M, K, BK) : make_operand_map(&ta, g.a, K, g.M, BM);
   // each CTA of a pair loads half of the B tile: [bn/2 rows] K-major, [128 n] or [BK/2 k rows] MN-major
   ok = ok && (b_mn ? make_operand_map(&tb, g.b, g.N, K, bn == 256 ? BK : BK / CL)
-                   : make_operand_map(&tb, g.b, K, g.N, bn / CL));
+                   : make_operand_map(&tb, g.b, K, g.N, bn / CL));  // 128 or 96 rows per CTA of a pair
   // epilogue boxes: 32 x 32 per warp; unused maps are copies of a valid one
   EpiMaps em;
   em.o = em.q = em.h = ta;
@@ -1081,7 +1087,7 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.num_kb = (int)((g.K + BK - 1) / BK);
   // 256-wide tiles run the 2-SM MMA (M = 256 over the CTA pair, N = 256);
   // 128-wide tiles the 1-SM MMA (M = 128; N = 128 per instruction for MN-major B)
-  kp.idesc = bn == 256 ? make_idesc(256, 256, g.a_dtype, g.b_dtype, a_mn, b_mn)
+  kp.idesc = bn >= 192 ? make_idesc(256, bn, g.a_dtype, g.b_dtype, a_mn, b_mn)
                        : make_idesc(128, b_mn ? 128 : bn, g.a_dtype, g.b_dtype, a_mn, b_mn);
   kp.sinv_a = g.sinv_a;
   kp.sinv_b = g.sinv_b;
@@ -1100,6 +1106,11 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
 
   if (g.epi == EPI_STORE) {
     if (bn == 256) return launch_layouts<256, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, em, kp, st);
+    if (bn == 192) {
+      if (!a_mn && !b_mn) return launch_t<192, false, false, EPI_STORE, LNFP8_E4M3>(ta, tb, em, kp, st);
+      return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: 192-wide tiles with layouts (%d, %d) are not built",
+                       g.a_layout, g.b_layout);
+    }
     return launch_layouts<128, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, em, kp, st);
   }
   if (g.epi == EPI_GELU && !a_mn && !b_mn) {

@@ -80,7 +80,8 @@ struct GemmPlan {
   int64_t slot_bytes; // partial-product slots after the flag area
   int64_t ws_bytes;   // flag_bytes + slot_bytes (0 without a split)
 };
-GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split);
+// kmajor: both operands K-major (the only layout the 192-wide tiles are built for)
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split, bool kmajor = false);
 
 // One persistent launch of the FC2 data gradient with the dGELU epilogue (g0:
 // A [M, K] K-major, B [K, N]) and a bf16-store GEMM (g1, both operands

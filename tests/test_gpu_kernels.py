@@ -204,10 +204,11 @@ def test_gemm_exact_integer_problems(L, a_layout, b_layout, M, N, K, adt, bdt):
 
 
 @pytest.mark.parametrize("a_layout,b_layout", [(0, 0), (0, 1), (1, 1), (1, 0)])
-@pytest.mark.parametrize("M,N,K", [(4864, 1024, 1024), (4880, 1040, 1104)])
+@pytest.mark.parametrize("M,N,K", [(4864, 1024, 1024), (4880, 1040, 1104), (8192, 768, 256), (8208, 1152, 272)])
 def test_gemm_exact_integer_problems_on_the_pair_tiles(L, a_layout, b_layout, M, N, K):
     """Enough tiles for the 256-wide CTA-pair tiles (2-SM MMA) and more K blocks
-    than pipeline stages, with ragged M, N and K tails."""
+    than pipeline stages, with ragged M, N and K tails. With both operands K-major,
+    N = 768 and 1152 take the 192-wide pair tiles (fewer rounds over the SMs)."""
     rng = np.random.default_rng(M + N + K + a_layout)
     a = _int_codes((M, K), fp8.E4M3, rng)
     b = _int_codes((N, K), fp8.E5M2, rng)
