@@ -312,6 +312,116 @@ def timed_steps(torch, run, steps, warmup, flush, barrier):
     return sum(a.elapsed_time(b) for a, b in ev), launches
 
 
+def end_to_end(torch, run, steps, dev, barrier, max_over_ranks, world, graph=True):
+    """Steps fed from and drained to pinned host memory through the public API.
+
+    Every step copies its X and dY host->device and its Y and dX device->host inside
+    the timed region. The copies run on their own streams and the device buffers
+    alternate between two sets, so step i's input copies and step i-1's output
+    copies overlap step i-1's and step i's compute (a training loop would stream
+    batches the same way). Each set's step is one captured CUDA graph when graphs
+    are on."""
+    L = run.L
+    xh = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in run.xs_host]
+    dyh = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in run.dys_host]
+    yh = [torch.empty(run.m, run.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dxh = [torch.empty(run.m, run.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xd = [torch.empty(run.m, run.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    dyd = [torch.empty_like(xd[0]) for _ in range(2)]
+    yd = [run.y, torch.empty_like(run.y)]
+    gd = [run.grads, L.mlp_grads(run.m, run.d, run.f, device=dev)]
+    comp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def call(b):
+        L.ln_mlp_fwd(xd[b], run.p["gamma"], run.p["beta"], run.p["w1"], run.p["b1"], run.p["w2"], run.p["b2"], run.fm,
+                     run.rec, y=yd[b], ctx=run.ctx)
+        L.ln_mlp_bwd(dyd[b], xd[b], run.p["gamma"], run.ctx, run.bm, run.rec, grads=gd[b])
+
+    graphs = None
+    if graph:
+        sd_f, sd_b = run.fm.state_dict(), run.bm.state_dict()
+        s = torch.cuda.Stream()
+        s.wait_stream(comp)
+        with torch.cuda.stream(s):
+            for b in range(2):
+                call(b)
+        comp.wait_stream(s)
+        torch.cuda.synchronize()
+        graphs = []
+        for b in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call(b)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        run.fm.load_state_dict(sd_f)
+        run.bm.load_state_dict(sd_b)
+
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
+
+    copy_ev = []  # (h2d start, h2d end, d2h start, d2h end) per timed step
+
+    def issue(i, timed=False):
+        b = i % 2
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(done[b])       # step i-2 has finished reading this set's inputs
+            if ev:
+                ev[0].record(h2d)
+            xd[b].copy_(xh[i % len(xh)], non_blocking=True)
+            dyd[b].copy_(dyh[i % len(dyh)], non_blocking=True)
+            if ev:
+                ev[1].record(h2d)
+            in_ready[b].record(h2d)
+        comp.wait_event(in_ready[b])
+        comp.wait_event(out_read[b])      # step i-2's outputs have left this set
+        if graphs is not None:
+            graphs[b].replay()
+        else:
+            call(b)
+        done[b].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(done[b])
+            if ev:
+                ev[2].record(d2h)
+            yh[b].copy_(yd[b], non_blocking=True)
+            dxh[b].copy_(gd[b].dx, non_blocking=True)
+            if ev:
+                ev[3].record(d2h)
+            out_read[b].record(d2h)
+        if ev:
+            copy_ev.append(ev)
+
+    for b in range(2):
+        done[b].record(comp)
+        out_read[b].record(comp)
+    for i in range(3):
+        issue(i)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    h2d.wait_stream(comp)
+    d2h.wait_stream(comp)
+    for i in range(steps):
+        issue(i, timed=True)
+    comp.wait_stream(d2h)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    h2d_ms = sum(a.elapsed_time(b) for a, b, _, _ in copy_ev) / len(copy_ev)
+    d2h_ms = sum(c.elapsed_time(d) for _, _, c, d in copy_ev) / len(copy_ev)
+    return {"value": flops_per_step(run.m, run.d, run.f) * steps * world / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 2 * run.m * run.d * 2, "d2h_bytes_per_step": 2 * run.m * run.d * 2,
+            "steps": steps, "ms_per_step": ms / steps, "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
+            "copies": "X, dY host->device (pinned) and Y, dX device->host every step, on their own streams, "
+                      "overlapping the neighbouring steps' compute (two device buffer sets)"}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -410,34 +520,7 @@ def run_gpu(args):
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e_steps = min(args.steps, 200)
-    xh = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in run.xs_host]
-    dyh = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in run.dys_host]
-    yh = torch.empty(M_TOK, D_MODEL, dtype=torch.bfloat16).pin_memory()
-    dxh = torch.empty(M_TOK, D_MODEL, dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty(M_TOK, D_MODEL, dtype=torch.bfloat16, device=dev)
-    dyd = torch.empty_like(xd)
-    for i in range(3):
-        xd.copy_(xh[i % len(xh)], non_blocking=True)
-        dyd.copy_(dyh[i % len(dyh)], non_blocking=True)
-        run.step(i, xd, dyd)
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(e2e_steps):
-        xd.copy_(xh[i % len(xh)], non_blocking=True)
-        dyd.copy_(dyh[i % len(dyh)], non_blocking=True)
-        run.step(i, xd, dyd)
-        yh.copy_(run.y, non_blocking=True)
-        dxh.copy_(run.grads.dx, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    e2e = {"value": flops_per_step() * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": 2 * M_TOK * D_MODEL * 2, "d2h_bytes_per_step": 2 * M_TOK * D_MODEL * 2,
-           "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
-           "copies": "X, dY host->device (pinned) and Y, dX device->host, each step"}
+    e2e = end_to_end(torch, run, e2e_steps, dev, barrier, max_over_ranks, world, graph=bool(args.graph))
 
     # ---- D = 2048: LayerNormMLP 2048 -> 8192 -> 2048 over 16384 tokens (the scale-up width)
     d2048 = None
