@@ -510,8 +510,10 @@ def run_gpu(args):
                          "share": kms / sum(v[0] for v in prof.values())}
     # LayerNorm / cast kernels against HBM (algorithmic bytes per launch)
     hbm_kernels = {
-        "ln_fwd_cast": M_TOK * D_MODEL * (2 + 1) + M_TOK * 8,
-        "ln_bwd": M_TOK * D_MODEL * (2 + 2 + 2) + M_TOK * 8,
+        "ln_fwd_cast": M_TOK * D_MODEL * (2 + 1) + M_TOK * 8,        # X read, codes written, mu/rsigma
+        "ln_bwd": M_TOK * D_MODEL * (2 + 2 + 2) + M_TOK * 8,         # dLN, X read, dX written, mu/rsigma
+        "cast_colsum": M_TOK * D_MODEL * (2 + 1) + D_MODEL * 4,       # dY read, codes written, db2
+        "cast_pair": 2 * FFN * D_MODEL * (2 + 1),                     # W1, W2 read, codes written
     }
     for k, nbytes in hbm_kernels.items():
         if k in per_kernel:
