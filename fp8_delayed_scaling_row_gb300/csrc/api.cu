@@ -359,6 +359,31 @@ lnfp8_status amax_history_update(const lnfp8_meta* meta, const lnfp8_recipe* rec
   return update_launch(meta, mask, recipe->margin, scale_inv_before, (cudaStream_t)stream);
 }
 
+lnfp8_status amax_history_update_many(const lnfp8_meta* metas, int count, const lnfp8_recipe* recipe,
+                                      const int* dtypes, float* const* scale_inv_before, lnfp8_stream stream) {
+  const char* who = "amax_history_update_many";
+  clear_error();
+  if (count < 0 || count > kMaxUpdateSets)
+    return set_error(LNFP8_ERR_INVALID_ARG, "%s: count = %d (0..%d)", who, count, kMaxUpdateSets);
+  if (count == 0) return LNFP8_OK;
+  if (!metas || !dtypes) return set_error(LNFP8_ERR_INVALID_ARG, "%s: metas or dtypes is NULL", who);
+  const lnfp8_meta* ptrs[kMaxUpdateSets];
+  uint64_t masks[kMaxUpdateSets];
+  int off = 0;
+  for (int k = 0; k < count; ++k) {
+    TRY(validate_meta(&metas[k], 0, who));
+    TRY(check_recipe(recipe, &metas[k], who));
+    uint64_t mask = 0;
+    for (int i = 0; i < metas[k].n; ++i, ++off) {
+      TRY(check_dtype(dtypes[off], who));
+      if (dtypes[off] == LNFP8_E5M2) mask |= 1ull << i;
+    }
+    ptrs[k] = &metas[k];
+    masks[k] = mask;
+  }
+  return update_many_launch(ptrs, masks, scale_inv_before, count, recipe->margin, (cudaStream_t)stream);
+}
+
 lnfp8_status fp8_quantize(const void* in, int in_is_fp32, int64_t rows, int64_t cols, int dtype, const float* scale,
                           float* amax_cur, uint8_t* out, uint8_t* out_t, float* colsum, lnfp8_stream stream) {
   const char* who = "fp8_quantize";

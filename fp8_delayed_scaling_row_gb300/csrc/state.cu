@@ -16,16 +16,26 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads)
-update_kernel(float* __restrict__ scale, float* __restrict__ scale_inv, float* __restrict__ hist,
-              float* __restrict__ cur, int n, int L, uint64_t e5m2_mask, int margin,
-              float* __restrict__ sinv_before) {
-  extern __shared__ float shist[];  // the new window of this slot, L floats
-  __shared__ uint32_t red[kThreads / 32];
-  const int i = blockIdx.x;
+struct UpdateSet {
+  float* scale;
+  float* scale_inv;
+  float* hist;
+  float* cur;
+  float* sinv_before;
+  uint64_t e5m2_mask;
+  int n, L;
+};
+struct UpdateTable {
+  UpdateSet set[kMaxUpdateSets];
+  int first[kMaxUpdateSets];  // first CTA of each set
+  int count, margin;
+};
+
+// Slot i of one tensor set: roll its history, insert cur, reduce, rescale.
+__device__ void update_slot(float* __restrict__ scale, float* __restrict__ scale_inv, float* __restrict__ hist,
+                            float* __restrict__ cur, int n, int L, int i, bool e5m2, int margin,
+                            float* __restrict__ sinv_before, float* shist, uint32_t* red) {
   const int t = threadIdx.x;
-  pdl_wait();
-  pdl_launch_dependents();
   const float c = cur[i];
   // read phase: the new row j is the old row j-1, the new row 0 is cur
   uint32_t m = 0;
@@ -45,7 +55,7 @@ update_kernel(float* __restrict__ scale, float* __restrict__ scale_inv, float* _
     const float a = __uint_as_float(a_bits);
     if (sinv_before) sinv_before[i] = scale_inv[i];
     cur[i] = 0.f;
-    const float fmax = ((e5m2_mask >> i) & 1ull) ? 57344.0f : 448.0f;
+    const float fmax = e5m2 ? 57344.0f : 448.0f;
     if (isfinite(a) && a > 0.f) {
       float s = fmax / a;
       if (margin > 0) s = s / (float)(1u << margin);
@@ -55,6 +65,33 @@ update_kernel(float* __restrict__ scale, float* __restrict__ scale_inv, float* _
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(kThreads)
+update_kernel(float* __restrict__ scale, float* __restrict__ scale_inv, float* __restrict__ hist,
+              float* __restrict__ cur, int n, int L, uint64_t e5m2_mask, int margin,
+              float* __restrict__ sinv_before) {
+  extern __shared__ float shist[];  // the new window of this slot, L floats
+  __shared__ uint32_t red[kThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int i = blockIdx.x;
+  update_slot(scale, scale_inv, hist, cur, n, L, i, (e5m2_mask >> i) & 1ull, margin, sinv_before, shist, red);
+}
+
+// Several tensor sets (e.g. every layer of a model, updated after the step) in
+// one launch: CTA b updates slot b - first[s] of set s.
+__global__ void __launch_bounds__(kThreads) update_many_kernel(const UpdateTable tab) {
+  extern __shared__ float shist[];
+  __shared__ uint32_t red[kThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  int s = 0;
+  while (s + 1 < tab.count && (int)blockIdx.x >= tab.first[s + 1]) ++s;
+  const UpdateSet& u = tab.set[s];
+  const int i = blockIdx.x - tab.first[s];
+  update_slot(u.scale, u.scale_inv, u.hist, u.cur, u.n, u.L, i, (u.e5m2_mask >> i) & 1ull, tab.margin,
+              u.sinv_before, shist, red);
 }
 
 __global__ void init_kernel(float* scale, float* scale_inv, float* hist, float* cur, int n, int L) {
@@ -102,6 +139,32 @@ lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, 
                  m->amax_cur, m->n, m->history_len, e5m2_mask, margin, sinv_before) != cudaSuccess)
     return check_launch("amax_history_update launch");
   return check_launch("amax_history_update");
+}
+
+lnfp8_status update_many_launch(const lnfp8_meta* const* metas, const uint64_t* e5m2_masks, float* const* sinv_before,
+                                int count, int margin, cudaStream_t st) {
+  UpdateTable tab = {};
+  int slots = 0, maxL = 1;
+  for (int k = 0; k < count; ++k) {
+    const lnfp8_meta* m = metas[k];
+    tab.set[k] = UpdateSet{m->scale, m->scale_inv, m->amax_history, m->amax_cur, sinv_before ? sinv_before[k] : nullptr,
+                           e5m2_masks[k], m->n, m->history_len};
+    tab.first[k] = slots;
+    slots += m->n;
+    maxL = m->history_len > maxL ? m->history_len : maxL;
+  }
+  tab.count = count;
+  tab.margin = margin;
+  if (!slots) return LNFP8_OK;
+  const size_t smem = (size_t)maxL * sizeof(float);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(update_many_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return check_launch("amax_history_update_many: smem attribute");
+  }
+  LaunchScope ls("state_update_many", st);
+  if (launch_pdl(update_many_kernel, dim3(slots), dim3(kThreads), smem, st, tab) != cudaSuccess)
+    return check_launch("amax_history_update_many launch");
+  return check_launch("amax_history_update_many");
 }
 
 }  // namespace lnfp8

@@ -29,7 +29,7 @@ _FORMATS = {"e4m3": FORMAT_E4M3, "hybrid": FORMAT_HYBRID, "e5m2": FORMAT_E5M2}
 
 EXPORTED = [
     "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_launch_count",
-    "lnfp8_profile_enable", "lnfp8_profile_sample", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update",
+    "lnfp8_profile_enable", "lnfp8_profile_sample", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update", "amax_history_update_many",
     "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
     "ln_linear_bwd_noalloc", "ln_mlp_fwd", "ln_mlp_bwd", "lnfp8_gemm_workspace_size",
     "lnfp8_ln_linear_bwd_workspace_size", "lnfp8_ln_mlp_bwd_workspace_size", "lnfp8_ln_mlp_fwd_workspace_size",
@@ -106,6 +106,8 @@ _c_prof_get = _sig("lnfp8_profile_get", [C.c_int, C.POINTER(C.c_char_p), C.POINT
                                          C.POINTER(C.c_longlong)])
 _c_meta_init = _sig("lnfp8_meta_init", [C.POINTER(CMeta), _P])
 _c_update = _sig("amax_history_update", [C.POINTER(CMeta), C.POINTER(CRecipe), C.POINTER(C.c_int), _P, _P])
+_c_update_many = _sig("amax_history_update_many", [C.POINTER(CMeta), C.c_int, C.POINTER(CRecipe), C.POINTER(C.c_int),
+                                                   C.POINTER(_P), _P])
 _c_quant = _sig("fp8_quantize", [_P, C.c_int, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P])
 _c_ln_fwd = _sig("ln_fwd_cast", [_P, _P, _P, C.c_float, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P, _P])
 _c_ln_bwd = _sig("ln_bwd", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P])
@@ -239,6 +241,21 @@ def amax_history_update(meta: ScalingMeta, recipe: Recipe, dtypes, scale_inv_bef
 
 
 # ------------------------------------------------------------------ kernels
+
+def amax_history_update_many(metas, recipe: Recipe, dtypes_per_meta, scale_inv_before=None, stream=None) -> None:
+    """One launch of the state update for several ScalingMeta sets (e.g. all layers after a step)."""
+    metas = list(metas)
+    arr = (CMeta * len(metas))(*[m.c() for m in metas])
+    flat = [int(d) for ds in dtypes_per_meta for d in ds]
+    if len(flat) != sum(m.n for m in metas):
+        raise ValueError("one dtype per slot of every meta")
+    dts = (C.c_int * max(len(flat), 1))(*flat)
+    sinv = None
+    if scale_inv_before is not None:
+        sinv = (_P * len(metas))(*[_ptr(t) for t in scale_inv_before])
+    rc = recipe.c()
+    _check(_c_update_many(arr, len(metas), C.byref(rc), dts, sinv, _stream(stream)))
+
 def fp8_quantize(x, dtype, scale, amax_cur, *, out=None, out_t=None, colsum=None, stream=None):
     """codes = fp8(x * scale) with amax; x is a 2-D bf16 or fp32 CUDA tensor."""
     rows, cols = x.shape

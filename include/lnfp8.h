@@ -159,6 +159,17 @@ lnfp8_status amax_history_update(const lnfp8_meta* meta, const lnfp8_recipe* rec
                                  const int* dtype_per_tensor, float* scale_inv_before,
                                  lnfp8_stream stream);
 
+/* The same update for `count` tensor sets (0..64; e.g. every layer of a model
+ * after the step, its module calls having run with defer_update) in ONE kernel
+ * launch. metas: HOST array [count]; dtypes: HOST array, the sets' per-slot
+ * lnfp8_dtype values one after another (sum of the n's entries);
+ * scale_inv_before: HOST array [count] of optional device pointers (each [n] or
+ * NULL), or NULL. The results equal count separate amax_history_update calls
+ * bit for bit. */
+lnfp8_status amax_history_update_many(const lnfp8_meta* metas, int count, const lnfp8_recipe* recipe,
+                                      const int* dtypes, float* const* scale_inv_before,
+                                      lnfp8_stream stream);
+
 /* Scaled cast (K2) --------------------------------------------------------- */
 
 /* code = fp8(x * (*scale)), round to nearest even, saturating; *amax_cur =

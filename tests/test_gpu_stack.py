@@ -1,0 +1,177 @@
+"""A stack of transformer-block FP8 modules, several steps (GPU).
+
+Each of the stack's layers runs the block the pages' model is built from,
+around a synthetic attention output (attention itself is not on the path):
+
+    qkv = LayerNormLinear(h)            768 -> 2304 (discarded: attention is synthetic)
+    h   = h + Linear(attn)              768 -> 768 on attn ~ N(0, 1)
+    h   = h + LayerNormMLP(h)           768 -> 3072 -> 768
+
+and the backward in reverse with synthetic dQKV ~ N(0, 0.01) and the residual
+gradient flowing through. Every module call defers its state update; after the
+step one ``amax_history_update_many`` launch updates all layers' forward and
+backward states. The checks, per step and layer: every module output and
+gradient against the oracle module fed the same inputs and the same pre-step
+state (1e-2 relative Frobenius); the states after the one-launch update equal,
+bit for bit, the oracle state machine fed the amaxes the GPU recorded, and equal
+separate per-set updates. The residual adds are test plumbing (torch on the
+GPU side, numpy on the oracle side, both rounding to bf16).
+"""
+import numpy as np
+import pytest
+
+from fp8_delayed_scaling_row_gb300 import synth
+from oracle import modules as omod
+from oracle.delayed_scaling import Recipe as ORecipe, ScalingState
+from oracle.gemm import bf16_to_f32, to_bf16_bits
+from helpers import bf16_dev, host, rel_fro
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_delayed_scaling_row_gb300 import lnfp8
+    return lnfp8
+
+
+def _state(meta):
+    s = ScalingState(meta.n, meta.history_len)
+    s.scale[:] = host(meta.scale)
+    s.scale_inv[:] = host(meta.scale_inv)
+    s.amax_history[:] = host(meta.amax_history)
+    s.amax_cur[:] = host(meta.amax_cur)
+    return s
+
+
+def _bits_equal(meta, st):
+    for name in ("scale", "scale_inv", "amax_history", "amax_cur"):
+        g = host(getattr(meta, name)).astype(np.float32)
+        if not np.array_equal(g.view(np.uint32), getattr(st, name).view(np.uint32)):
+            return False
+    return True
+
+
+def _bf16_add(a, b):
+    """bf16(a + b) of two bf16-valued float arrays (the residual add)."""
+    return bf16_to_f32(to_bf16_bits(np.asarray(a, np.float64) + np.asarray(b, np.float64))).astype(np.float64)
+
+
+def _to_bits(v):
+    return to_bf16_bits(np.asarray(v, np.float64))
+
+
+@pytest.mark.parametrize("layers,M,steps", [(4, 512, 3)])
+def test_block_stack_with_one_state_update_launch(L, layers, M, steps):
+    D, F, NQKV = 768, 3072, 2304
+    rec, orec = L.Recipe("hybrid", 16), ORecipe("hybrid", 16)
+    ff, gf = orec.fwd_fmt(), orec.bwd_fmt()
+    E4, E5 = L.E4M3, L.E5M2
+    P = []
+    for l in range(layers):
+        P.append(dict(
+            qkv=synth.linear_params(NQKV, D, layer=l, bias_std=0.02, wtid=synth.TID["wqkv"], btid=synth.TID["bqkv"]),
+            proj=synth.linear_params(D, D, layer=l, ln=False, bias_std=0.02, wtid=synth.TID["wproj"],
+                                     btid=synth.TID["bproj"]),
+            mlp=synth.mlp_params(D, F, layer=l, bias_std=0.02)))
+    dev = [dict(qkv={k: (bf16_dev(v) if v is not None else None) for k, v in p["qkv"].items()},
+                proj={k: (bf16_dev(v) if v is not None else None) for k, v in p["proj"].items()},
+                mlp={k: bf16_dev(v) for k, v in p["mlp"].items()}) for p in P]
+    # per layer: forward metas (qkv 2, proj 2, mlp 4) and backward metas (1, 1, 2)
+    M_ = [dict(fq=L.ScalingMeta(2, 16), fp=L.ScalingMeta(2, 16), fm=L.ScalingMeta(4, 16),
+               bq=L.ScalingMeta(1, 16), bp=L.ScalingMeta(1, 16), bm=L.ScalingMeta(2, 16)) for _ in range(layers)]
+    order = ["fq", "fp", "fm", "bq", "bp", "bm"]
+    dts = {"fq": [E4, E4], "fp": [E4, E4], "fm": [E4] * 4, "bq": [E5], "bp": [E5], "bm": [E5, E5]}
+    ofmts = {"fq": [ff] * 2, "fp": [ff] * 2, "fm": [ff] * 4, "bq": [gf], "bp": [gf], "bm": [gf] * 2}
+    for step in range(steps):
+        pre = [{k: _state(m[k]) for k in order} for m in M_]
+        h = bf16_to_f32(synth.activations(M, D, dist="outliers", step=step)).astype(np.float64)
+        saved = []
+        for l in range(layers):
+            p, d, m, st = P[l], dev[l], M_[l], pre[l]
+            hb = _to_bits(h)
+            attn = synth.activations(M, D, step=step, tid=synth.TID["attn"], layer=l)
+            xq = bf16_dev(hb)
+            qkv, cq = L.ln_linear_fwd(xq, d["qkv"]["gamma"], d["qkv"]["beta"], d["qkv"]["w"], d["qkv"]["b"], m["fq"], rec,
+                                      defer_update=True)
+            oq_y, ocq, _ = omod.ln_linear_fwd(hb, p["qkv"]["gamma"], p["qkv"]["beta"], p["qkv"]["w"], p["qkv"]["b"],
+                                              st["fq"].copy(), orec, update=False)
+            assert rel_fro(host(qkv), oq_y) < TOL, (step, l, "qkv")
+            xa = bf16_dev(attn)
+            pr, cp = L.ln_linear_fwd(xa, None, None, d["proj"]["w"], d["proj"]["b"], m["fp"], rec, defer_update=True)
+            op_y, ocp, _ = omod.ln_linear_fwd(attn, None, None, p["proj"]["w"], p["proj"]["b"], st["fp"].copy(), orec,
+                                              update=False)
+            assert rel_fro(host(pr), op_y) < TOL, (step, l, "proj")
+            h = _bf16_add(h, host(pr))
+            hb2 = _to_bits(h)
+            xm = bf16_dev(hb2)
+            y, cm = L.ln_mlp_fwd(xm, d["mlp"]["gamma"], d["mlp"]["beta"], d["mlp"]["w1"], d["mlp"]["b1"], d["mlp"]["w2"],
+                                 d["mlp"]["b2"], m["fm"], rec, defer_update=True)
+            om_y, ocm, _ = omod.ln_mlp_fwd(hb2, p["mlp"]["gamma"], p["mlp"]["beta"], p["mlp"]["w1"], p["mlp"]["b1"],
+                                           p["mlp"]["w2"], p["mlp"]["b2"], st["fm"].copy(), orec, update=False)
+            assert rel_fro(host(y), om_y) < TOL, (step, l, "mlp")
+            h = _bf16_add(h, host(y))
+            saved.append((xq, cq, ocq, xa, cp, ocp, xm, cm, ocm))
+        dh = bf16_to_f32(synth.grad(M, D, step=step)).astype(np.float64)
+        for l in reversed(range(layers)):
+            p, d, m, st = P[l], dev[l], M_[l], pre[l]
+            xq, cq, ocq, xa, cp, ocp, xm, cm, ocm = saved[l]
+            g = L.ln_mlp_bwd(bf16_dev(_to_bits(dh)), xm, d["mlp"]["gamma"], cm, m["bm"], rec, defer_update=True)
+            og = omod.ln_mlp_bwd(_to_bits(dh), ocm, st["bm"].copy(), orec, update=False)
+            for k in ("dx", "dw1", "dw2", "dgamma"):
+                assert rel_fro(host(getattr(g, k)), og[k]) < TOL, (step, l, "mlp", k)
+            dh = _bf16_add(dh, host(g.dx))
+            gp = L.ln_linear_bwd(bf16_dev(_to_bits(dh)), xa, None, cp, m["bp"], rec, defer_update=True)
+            ogp = omod.ln_linear_bwd(_to_bits(dh), ocp, st["bp"].copy(), orec, update=False)
+            assert rel_fro(host(gp.dw), ogp["dw"]) < TOL, (step, l, "proj dw")
+            dqkv = synth.grad(M, NQKV, step=step, layer=l, tid=synth.TID["attn"])
+            gq = L.ln_linear_bwd(bf16_dev(dqkv), xq, d["qkv"]["gamma"], cq, m["bq"], rec, defer_update=True)
+            ogq = omod.ln_linear_bwd(dqkv, ocq, st["bq"].copy(), orec, update=False)
+            for k in ("dx", "dw", "dgamma"):
+                assert rel_fro(host(getattr(gq, k)), ogq[k]) < TOL, (step, l, "qkv", k)
+            dh = _bf16_add(dh, host(gq.dx))
+        L.sync_status()
+        # one launch for every layer's six states; a copy updated set by set must agree
+        copies = [{k: _state(m[k]) for k in order} for m in M_]
+        metas = [m[k] for m in M_ for k in order]
+        L.amax_history_update_many(metas, rec, [dts[k] for _ in M_ for k in order])
+        L.sync_status()
+        for l in range(layers):
+            for k in order:
+                ost = copies[l][k].copy()
+                ost.update(ofmts[k])
+                assert _bits_equal(M_[l][k], ost), (step, l, k)
+                # the teacher-forced oracle: the pre-step state fed the amaxes the GPU recorded
+                tf = pre[l][k].copy()
+                for i in range(tf.n):
+                    tf.record(i, copies[l][k].amax_cur[i])
+                tf.update(ofmts[k])
+                assert _bits_equal(M_[l][k], tf), (step, l, k, "teacher-forced")
+
+
+def test_update_many_equals_separate_updates(L):
+    rec = L.Recipe("hybrid", 8)
+    rng = np.random.default_rng(3)
+    metas = [L.ScalingMeta(n, 8) for n in (1, 2, 4, 3)]
+    twins = [L.ScalingMeta(m.n, 8) for m in metas]
+    dts = [[L.E4M3] * m.n if i % 2 == 0 else [L.E5M2] * m.n for i, m in enumerate(metas)]
+    for step in range(5):
+        for m, t in zip(metas, twins):
+            a = torch.tensor((rng.random(m.n) * 10.0 ** rng.integers(-3, 3)).astype(np.float32), device="cuda")
+            m.amax_cur.copy_(a)
+            t.amax_cur.copy_(a)
+        snaps = [torch.zeros(m.n, device="cuda") for m in metas]
+        before = [m.scale_inv.clone() for m in metas]
+        L.amax_history_update_many(metas, rec, dts, scale_inv_before=snaps)
+        for t, d in zip(twins, dts):
+            L.amax_history_update(t, rec, d)
+        L.sync_status()
+        for m, t in zip(metas, twins):
+            for name in ("scale", "scale_inv", "amax_history", "amax_cur"):
+                assert torch.equal(getattr(m, name), getattr(t, name)), (step, name)
+        for sn, b in zip(snaps, before):
+            assert torch.equal(sn, b), step
+    L.amax_history_update_many([], rec, [])  # nothing to do
