@@ -253,7 +253,7 @@ extern "C" {
 
 const char* lnfp8_last_error(void) { return g_msg; }
 
-int lnfp8_version(void) { return 100; }
+int lnfp8_version(void) { return 200; }
 
 long long lnfp8_launch_count(void) { return g_launches.load(); }
 
@@ -399,6 +399,33 @@ lnfp8_status fp8_quantize(const void* in, int in_is_fp32, int64_t rows, int64_t 
   return cast_launch(in, in_is_fp32 != 0, rows, cols, dtype, scale, amax_cur, out, out_t, colsum, (cudaStream_t)stream);
 }
 
+lnfp8_status fp8_weight_quantize(const uint16_t* w, int64_t rows, int64_t cols, const lnfp8_meta* meta,
+                                 const lnfp8_recipe* recipe, int dtype, uint8_t* codes, lnfp8_stream stream) {
+  const char* who = "fp8_weight_quantize";
+  clear_error();
+  TRY(tokens(rows, who));
+  TRY(feat(cols, "cols", who));
+  TRY(check_dtype(dtype, who));
+  if (!meta || !recipe) return set_error(LNFP8_ERR_INVALID_ARG, "%s: meta and recipe are required", who);
+  TRY(validate_meta(meta, 1, who));
+  TRY(check_recipe(recipe, nullptr, who));  // the weight's own history length is its own
+  if (rows > 0) {
+    REQ(w, who);
+    REQ(codes, who);
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  TRY(cast_launch(w, false, rows, cols, dtype, meta->scale, meta->amax_cur, nullptr, nullptr, nullptr, st));
+  TRY(update_launch(meta, mask_all(1, dtype), recipe->margin, nullptr, st));
+  return cast_launch(w, false, rows, cols, dtype, meta->scale, meta->amax_cur, codes, nullptr, nullptr, st);
+}
+
+// Copies a weight's stored scale_inv into the forward's saved snapshot (after the state step wrote it).
+static lnfp8_status save_weight_sinv(float* sinv_saved_slot, const float* w_scale_inv, cudaStream_t st) {
+  if (cudaMemcpyAsync(sinv_saved_slot, w_scale_inv, sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return check_launch("saving the weight's scale_inv");
+  return LNFP8_OK;
+}
+
 lnfp8_status ln_fwd_cast(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int64_t D,
                          int dtype, const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
                          float* y_debug, lnfp8_stream stream) {
@@ -525,7 +552,8 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
     REQ(a->beta, who);
     if (a->K > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: K > 8192 with LayerNorm", who);
   }
-  REQ(a->w, who);
+  const bool w8 = a->w_scale_inv != nullptr;  // weight stored as FP8 codes
+  if (!w8) REQ(a->w, who);
   REQ(a->wq, who);
   OPT(a->bias, who);
   OPT(a->ln_out_debug, who);
@@ -541,17 +569,19 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
   }
   const int fdt = fwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
-  TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
+  if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
   if (ln)
     TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,
                       a->rsigma, a->ln_out_debug, st));
   else
     TRY(cast_launch(a->x, false, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, nullptr, nullptr, st));
-  GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, m.scale_inv + 0, m.scale_inv + 1);
+  GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, m.scale_inv + 0,
+                         w8 ? a->w_scale_inv : m.scale_inv + 1);
   g.bias = a->bias;
   g.out = a->y;
   TRY(gemm_launch(g, st));
-  return finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st);
+  TRY(finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st));
+  return w8 ? save_weight_sinv(a->sinv_saved + 1, a->w_scale_inv, st) : LNFP8_OK;
 }
 
 lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream stream) {
@@ -626,8 +656,13 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   TRY(check_recipe(&a->recipe, &a->meta, who));
   REQ(a->gamma, who);
   REQ(a->beta, who);
-  REQ(a->w1, who);
-  REQ(a->w2, who);
+  const bool w8 = a->w1_scale_inv != nullptr;  // weights stored as FP8 codes
+  if (w8 != (a->w2_scale_inv != nullptr))
+    return set_error(LNFP8_ERR_INVALID_ARG, "%s: w1_scale_inv and w2_scale_inv must be given together", who);
+  if (!w8) {
+    REQ(a->w1, who);
+    REQ(a->w2, who);
+  }
   REQ(a->w1q, who);
   REQ(a->w2q, who);
   OPT(a->b1, who);
@@ -650,11 +685,15 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   // FC1 and FC2 in one launch when the caller gave room for the FC1 tiles' readiness counters
   const int64_t ready_bytes = lnfp8_ln_mlp_fwd_workspace_size(a->M, a->D, a->F);
   const bool fused = a->M > 0 && a->gemm_ws && ready_bytes > 0 && a->gemm_ws_bytes >= ready_bytes && !pair_disabled();
-  TRY(cast2_launch(a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q, a->w2, a->D, a->F, m.scale + 3,
-                   m.amax_cur + 3, a->w2q, fdt, st, fused ? a->gemm_ws : nullptr, fused ? ready_bytes : 0));
+  if (!w8)
+    TRY(cast2_launch(a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q, a->w2, a->D, a->F, m.scale + 3,
+                     m.amax_cur + 3, a->w2q, fdt, st, fused ? a->gemm_ws : nullptr, fused ? ready_bytes : 0));
+  else if (fused)
+    TRY(zero_launch({{a->gemm_ws, ready_bytes}}, st));
   TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
                     a->rsigma, a->ln_out_debug, st));
-  GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0, m.scale_inv + 1);
+  GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0,
+                          w8 ? a->w1_scale_inv : m.scale_inv + 1);
   f1.epi = EPI_GELU;
   f1.bias = a->b1;
   f1.out = a->h;
@@ -663,7 +702,8 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   f1.scale_q = m.scale + 2;
   f1.amax_q = m.amax_cur + 2;
   f1.dbg = a->act_debug;
-  GemmArgs f2 = gemm_args(a->aq, 0, fdt, a->w2q, 0, fdt, a->M, a->D, a->F, m.scale_inv + 2, m.scale_inv + 3);
+  GemmArgs f2 = gemm_args(a->aq, 0, fdt, a->w2q, 0, fdt, a->M, a->D, a->F, m.scale_inv + 2,
+                          w8 ? a->w2_scale_inv : m.scale_inv + 3);
   f2.bias = a->b2;
   f2.out = a->y;
   if (fused) {
@@ -674,7 +714,10 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
     TRY(gemm_launch(f1, st));
     TRY(gemm_launch(f2, st));
   }
-  return finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st);
+  TRY(finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st));
+  if (!w8) return LNFP8_OK;
+  TRY(save_weight_sinv(a->sinv_saved + 1, a->w1_scale_inv, st));
+  return save_weight_sinv(a->sinv_saved + 3, a->w2_scale_inv, st);
 }
 
 lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {

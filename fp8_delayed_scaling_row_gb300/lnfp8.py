@@ -30,7 +30,7 @@ _FORMATS = {"e4m3": FORMAT_E4M3, "hybrid": FORMAT_HYBRID, "e5m2": FORMAT_E5M2}
 EXPORTED = [
     "lnfp8_last_error", "lnfp8_sync_status", "lnfp8_version", "lnfp8_selftest_timeout", "lnfp8_launch_count",
     "lnfp8_profile_enable", "lnfp8_profile_sample", "lnfp8_profile_collect", "lnfp8_profile_get", "lnfp8_meta_init", "amax_history_update", "amax_history_update_many",
-    "fp8_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
+    "fp8_quantize", "fp8_weight_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
     "ln_linear_bwd_noalloc", "ln_mlp_fwd", "ln_mlp_bwd", "lnfp8_gemm_workspace_size",
     "lnfp8_ln_linear_bwd_workspace_size", "lnfp8_ln_mlp_bwd_workspace_size", "lnfp8_ln_mlp_fwd_workspace_size",
 ]
@@ -60,7 +60,7 @@ class CLnLinearFwd(C.Structure):
     _fields_ = [("M", _I64), ("K", _I64), ("N", _I64), ("x", _P), ("gamma", _P), ("beta", _P), ("eps", C.c_float),
                 ("w", _P), ("bias", _P), ("y", _P), ("xq", _P), ("wq", _P), ("mu", _P), ("rsigma", _P),
                 ("sinv_saved", _P), ("meta", CMeta), ("recipe", CRecipe), ("defer_update", C.c_int),
-                ("ln_out_debug", _P)]
+                ("ln_out_debug", _P), ("w_scale_inv", _P)]
 
 
 class CLnLinearBwd(C.Structure):
@@ -75,7 +75,7 @@ class CLnMlpFwd(C.Structure):
                 ("w1", _P), ("b1", _P), ("w2", _P), ("b2", _P), ("y", _P), ("lnq", _P), ("mu", _P), ("rsigma", _P),
                 ("w1q", _P), ("w2q", _P), ("h", _P), ("aq", _P), ("sinv_saved", _P), ("meta", CMeta),
                 ("recipe", CRecipe), ("defer_update", C.c_int), ("ln_out_debug", _P), ("act_debug", _P),
-                ("gemm_ws", _P), ("gemm_ws_bytes", _I64)]
+                ("gemm_ws", _P), ("gemm_ws_bytes", _I64), ("w1_scale_inv", _P), ("w2_scale_inv", _P)]
 
 
 class CLnMlpBwd(C.Structure):
@@ -109,6 +109,7 @@ _c_update = _sig("amax_history_update", [C.POINTER(CMeta), C.POINTER(CRecipe), C
 _c_update_many = _sig("amax_history_update_many", [C.POINTER(CMeta), C.c_int, C.POINTER(CRecipe), C.POINTER(C.c_int),
                                                    C.POINTER(_P), _P])
 _c_quant = _sig("fp8_quantize", [_P, C.c_int, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P])
+_c_wquant = _sig("fp8_weight_quantize", [_P, _I64, _I64, C.POINTER(CMeta), C.POINTER(CRecipe), C.c_int, _P, _P])
 _c_ln_fwd = _sig("ln_fwd_cast", [_P, _P, _P, C.c_float, _I64, _I64, C.c_int, _P, _P, _P, _P, _P, _P, _P])
 _c_ln_bwd = _sig("ln_bwd", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P])
 _c_gemm = _sig("fp8_gemm", [_P, C.c_int, C.c_int, _P, C.c_int, C.c_int, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I64,
@@ -266,6 +267,38 @@ def fp8_quantize(x, dtype, scale, amax_cur, *, out=None, out_t=None, colsum=None
     return out, out_t, colsum
 
 
+@dataclass
+class FP8Weight:
+    """A weight kept as FP8 codes (fp8_model_init): codes [rows, cols] uint8 in the
+    recipe's forward format, and the weight's own state (n = 1), whose scale_inv
+    [1] is the codes' dequantisation factor."""
+    codes: torch.Tensor
+    meta: "ScalingMeta"
+    dtype: int
+
+    @property
+    def scale_inv(self) -> torch.Tensor:
+        return self.meta.scale_inv
+
+    @property
+    def shape(self):
+        return self.codes.shape
+
+
+def quantize_weight(w, recipe: Recipe, *, meta: ScalingMeta | None = None, codes=None, stream=None) -> FP8Weight:
+    """Converts a bf16 weight [rows, cols] to FP8 storage once, on the device: its
+    amax, the delayed-scaling state update of its own state, then the cast."""
+    rows, cols = w.shape
+    if w.dtype != torch.bfloat16:
+        raise TypeError("quantize_weight takes a bf16 weight")
+    meta = meta if meta is not None else ScalingMeta(1, 1, device=w.device, stream=stream)
+    codes = codes if codes is not None else _e((rows, cols), torch.uint8, w.device)
+    dt = recipe.fwd_dtype
+    cm, cr = meta.c(), recipe.c()
+    _check(_c_wquant(_ptr(w), rows, cols, C.byref(cm), C.byref(cr), dt, _ptr(codes), _stream(stream)))
+    return FP8Weight(codes=codes, meta=meta, dtype=dt)
+
+
 def ln_fwd_cast(x, gamma, beta, dtype, scale, amax_cur, *, eps=1e-5, out=None, mu=None, rsigma=None, y_debug=None,
                 stream=None):
     M, D = x.shape
@@ -336,8 +369,9 @@ def _e(shape, dtype, dev):
     return torch.empty(shape, dtype=dtype, device=dev)
 
 
-def linear_ctx(M, K, N, *, ln=True, device="cuda", debug=False) -> LinearCtx:
-    return LinearCtx(xq=_e((M, K), torch.uint8, device), wq=_e((N, K), torch.uint8, device),
+def linear_ctx(M, K, N, *, ln=True, device="cuda", debug=False, weight_codes=True) -> LinearCtx:
+    return LinearCtx(xq=_e((M, K), torch.uint8, device),
+                     wq=_e((N, K), torch.uint8, device) if weight_codes else None,
                      mu=_e((M,), torch.float32, device) if ln else None,
                      rsigma=_e((M,), torch.float32, device) if ln else None,
                      sinv_saved=_e((2,), torch.float32, device),
@@ -346,16 +380,22 @@ def linear_ctx(M, K, N, *, ln=True, device="cuda", debug=False) -> LinearCtx:
 
 def ln_linear_fwd(x, gamma, beta, w, bias, meta: ScalingMeta, recipe: Recipe, *, eps=1e-5, y=None,
                   ctx: LinearCtx | None = None, defer_update=False, debug=False, stream=None):
-    """LayerNormLinear (gamma given) or Linear (gamma None) forward; returns (y, ctx)."""
+    """LayerNormLinear (gamma given) or Linear (gamma None) forward; returns (y, ctx).
+    w is a bf16 weight (cast every call) or an FP8Weight (its codes are used as they are)."""
     M, K = x.shape
     N = w.shape[0]
     dev = x.device
-    ctx = ctx if ctx is not None else linear_ctx(M, K, N, ln=gamma is not None, device=dev, debug=debug)
+    w8 = isinstance(w, FP8Weight)
+    ctx = ctx if ctx is not None else linear_ctx(M, K, N, ln=gamma is not None, device=dev, debug=debug,
+                                                 weight_codes=not w8)
+    if w8:
+        ctx.wq = w.codes
     y = y if y is not None else _e((M, N), torch.bfloat16, dev)
-    a = CLnLinearFwd(M=M, K=K, N=N, x=_ptr(x), gamma=_ptr(gamma), beta=_ptr(beta), eps=eps, w=_ptr(w),
-                     bias=_ptr(bias), y=_ptr(y), xq=_ptr(ctx.xq), wq=_ptr(ctx.wq), mu=_ptr(ctx.mu),
-                     rsigma=_ptr(ctx.rsigma), sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(), recipe=recipe.c(),
-                     defer_update=int(defer_update), ln_out_debug=_ptr(ctx.ln_out_debug))
+    a = CLnLinearFwd(M=M, K=K, N=N, x=_ptr(x), gamma=_ptr(gamma), beta=_ptr(beta), eps=eps,
+                     w=None if w8 else _ptr(w), bias=_ptr(bias), y=_ptr(y), xq=_ptr(ctx.xq), wq=_ptr(ctx.wq),
+                     mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma), sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(),
+                     recipe=recipe.c(), defer_update=int(defer_update), ln_out_debug=_ptr(ctx.ln_out_debug),
+                     w_scale_inv=_ptr(w.scale_inv) if w8 else None)
     _check(_c_lin_fwd(C.byref(a), _stream(stream)))
     return y, ctx
 
@@ -426,13 +466,15 @@ class MlpCtx:
     gemm_ws: torch.Tensor | None = None  # FC1 tiles' readiness counters (FC1 and FC2 in one launch)
 
 
-def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False) -> MlpCtx:
+def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False, weight_codes=True) -> MlpCtx:
     """Saved tensors of one LayerNormMLP forward. fused=True also allocates the row-block
     readiness counters with which the forward runs FC1 and FC2 as one launch (same
-    results; at 8192 x 768 -> 3072 -> 768 the two launches are still faster)."""
+    results; at 8192 x 768 -> 3072 -> 768 the two launches are still faster).
+    weight_codes=False leaves w1q/w2q to FP8-stored weights."""
     return MlpCtx(lnq=_e((M, D), torch.uint8, device), mu=_e((M,), torch.float32, device),
-                  rsigma=_e((M,), torch.float32, device), w1q=_e((F, D), torch.uint8, device),
-                  w2q=_e((D, F), torch.uint8, device), h=_e((M, F), torch.bfloat16, device),
+                  rsigma=_e((M,), torch.float32, device),
+                  w1q=_e((F, D), torch.uint8, device) if weight_codes else None,
+                  w2q=_e((D, F), torch.uint8, device) if weight_codes else None, h=_e((M, F), torch.bfloat16, device),
                   aq=_e((M, F), torch.uint8, device), sinv_saved=_e((4,), torch.float32, device),
                   ln_out_debug=_e((M, D), torch.float32, device) if debug else None,
                   act_debug=_e((M, F), torch.float32, device) if debug else None,
@@ -441,18 +483,26 @@ def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False) -> MlpCtx:
 
 def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, meta: ScalingMeta, recipe: Recipe, *, eps=1e-5, y=None,
                ctx: MlpCtx | None = None, defer_update=False, debug=False, stream=None):
-    """LayerNormMLP forward; returns (y, ctx)."""
+    """LayerNormMLP forward; returns (y, ctx). w1 and w2 are both bf16 weights (cast
+    every call) or both FP8Weight (their codes are used as they are)."""
     M, D = x.shape
     F = w1.shape[0]
     dev = x.device
-    ctx = ctx if ctx is not None else mlp_ctx(M, D, F, device=dev, debug=debug)
+    w8 = isinstance(w1, FP8Weight)
+    if w8 != isinstance(w2, FP8Weight):
+        raise TypeError("w1 and w2 must both be FP8Weight or both bf16")
+    ctx = ctx if ctx is not None else mlp_ctx(M, D, F, device=dev, debug=debug, weight_codes=not w8)
+    if w8:
+        ctx.w1q, ctx.w2q = w1.codes, w2.codes
     y = y if y is not None else _e((M, D), torch.bfloat16, dev)
-    a = CLnMlpFwd(M=M, D=D, F=F, x=_ptr(x), gamma=_ptr(gamma), beta=_ptr(beta), eps=eps, w1=_ptr(w1), b1=_ptr(b1),
-                  w2=_ptr(w2), b2=_ptr(b2), y=_ptr(y), lnq=_ptr(ctx.lnq), mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma),
+    a = CLnMlpFwd(M=M, D=D, F=F, x=_ptr(x), gamma=_ptr(gamma), beta=_ptr(beta), eps=eps,
+                  w1=None if w8 else _ptr(w1), b1=_ptr(b1), w2=None if w8 else _ptr(w2), b2=_ptr(b2), y=_ptr(y),
+                  lnq=_ptr(ctx.lnq), mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma),
                   w1q=_ptr(ctx.w1q), w2q=_ptr(ctx.w2q), h=_ptr(ctx.h), aq=_ptr(ctx.aq),
                   sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(), recipe=recipe.c(), defer_update=int(defer_update),
                   ln_out_debug=_ptr(ctx.ln_out_debug), act_debug=_ptr(ctx.act_debug), gemm_ws=_ptr(ctx.gemm_ws),
-                  gemm_ws_bytes=ctx.gemm_ws.numel() if ctx.gemm_ws is not None else 0)
+                  gemm_ws_bytes=ctx.gemm_ws.numel() if ctx.gemm_ws is not None else 0,
+                  w1_scale_inv=_ptr(w1.scale_inv) if w8 else None, w2_scale_inv=_ptr(w2.scale_inv) if w8 else None)
     _check(_c_mlp_fwd(C.byref(a), _stream(stream)))
     return y, ctx
 

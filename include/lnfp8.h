@@ -186,6 +186,24 @@ lnfp8_status fp8_quantize(const void* in, int in_is_fp32, int64_t rows, int64_t 
                           const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                           float* colsum, lnfp8_stream stream);
 
+/* One-time conversion of a weight to FP8 storage (TE tutorial closing list:
+ * fp8_model_init stores the weights themselves in FP8). Three kernels on
+ * `stream`, all on the device:
+ *   1. amax_cur[0] = max(amax_cur[0], max|w|);
+ *   2. the state update of `meta` (amax_history_update with dtype) - with a
+ *      freshly initialised meta of any history length this gives
+ *      scale = fp8_max / max|w| / 2^margin (kept at its old value when the
+ *      weight is all zeros or not finite);
+ *   3. codes = fp8(w * scale[0]) (round to nearest even, saturating), and the
+ *      cast's own amax of w is recorded into amax_cur[0] again.
+ * meta: n = 1, the weight's own state (any history length; the recipe gives
+ * only the margin); afterwards meta->scale_inv[0] is the codes' scale_inv
+ * (pass it as the forward's w_scale_inv). dtype: lnfp8_dtype of the codes (the
+ * forward format of the recipe the forward will run with).
+ * w [rows, cols] bf16; codes [rows, cols]; cols a multiple of 16. */
+lnfp8_status fp8_weight_quantize(const uint16_t* w, int64_t rows, int64_t cols, const lnfp8_meta* meta,
+                                 const lnfp8_recipe* recipe, int dtype, uint8_t* codes, lnfp8_stream stream);
+
 /* LayerNorm + amax + cast (K1) and LayerNorm backward (K5) --------------- */
 
 /* Per row of x [M, D] bf16: mu = mean, var = biased variance,
@@ -251,6 +269,12 @@ typedef struct {
   lnfp8_recipe recipe;
   int defer_update;       /* 1: accumulate amax_cur only; the caller runs amax_history_update */
   float* ln_out_debug;    /* optional [M, K] fp32 pre-cast input, may be NULL */
+  /* FP8-stored weight (fp8_model_init): NULL, or device [1] scale_inv of a
+   * weight kept as codes. When set, wq is an INPUT (the weight's [N, K] codes
+   * in the recipe's forward format, read only), w is ignored and may be NULL,
+   * the forward casts no weight and records no weight amax, the GEMM uses
+   * w_scale_inv[0] for the weight and sinv_saved[1] receives it. */
+  const float* w_scale_inv;
 } lnfp8_ln_linear_fwd_args;
 
 typedef struct {
@@ -281,7 +305,9 @@ typedef struct {
  * te.Linear when gamma is NULL):
  *   y = LN(x); xq = fp8(y * scale[0]); wq = fp8(w * scale[1]);
  *   out = (xq . wq^T) * (scale_inv[0] * scale_inv[1]) + bias  (bf16);
- * then the forward state update unless defer_update. */
+ * then the forward state update unless defer_update. With w_scale_inv set
+ * (weights stored in FP8, TE tutorial closing list: fp8_model_init), wq is the
+ * given codes and w_scale_inv[0] takes the place of scale_inv[1]. */
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* args, lnfp8_stream stream);
 
 /* LayerNormLinear backward: dyq = fp8(dy * gscale[0]) (E5M2 under HYBRID);
@@ -348,6 +374,13 @@ typedef struct {
   float* act_debug;       /* optional [M, F] fp32 pre-cast GELU output */
   void* gemm_ws;          /* optional, lnfp8_ln_mlp_fwd_workspace_size bytes: FC1 and FC2 run as one launch */
   int64_t gemm_ws_bytes;
+  /* FP8-stored weights (fp8_model_init): both NULL, or device [1] scale_inv of
+   * W1 and of W2 kept as codes. When set, w1q and w2q are INPUTS (codes in the
+   * recipe's forward format, read only), w1 and w2 are ignored and may be NULL,
+   * the forward casts no weight and records no weight amax (slots 1 and 3),
+   * and sinv_saved[1], sinv_saved[3] receive these values. */
+  const float* w1_scale_inv;
+  const float* w2_scale_inv;
 } lnfp8_ln_mlp_fwd_args;
 
 typedef struct {

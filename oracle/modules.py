@@ -108,16 +108,38 @@ class Ctx:
     debug: dict = field(default_factory=dict)
 
 
+def quantize_weight(w, recipe: Recipe, state: ScalingState | None = None):
+    """A weight converted once to FP8 storage (TE tutorial, closing list of
+    things to try: ``fp8_model_init()`` keeps the weights themselves in FP8 for
+    inference). The pages name the feature only; the reading here is the
+    delayed-scaling rule applied to the weight's own state (n = 1, fresh unless
+    given): record max|W|, run the end-of-step update (so with a fresh state
+    scale = fp8_max / max|W| / 2^margin), cast W with that scale, and record the
+    cast's amax as every cast does. Returns (codes, scale_inv, state)."""
+    fmt = recipe.fwd_fmt()
+    st = state if state is not None else ScalingState(1, 1)
+    W = _in(w)
+    st.record(0, _fp8.amax(W.astype(np.float32)))
+    st.update([fmt], recipe.amax_compute_algo, recipe.margin)
+    codes = _fp8.quantize(W, st.scale[0], fmt)
+    st.record(0, _fp8.amax(W.astype(np.float32)))
+    return codes, np.float32(st.scale_inv[0]), st
+
+
 def ln_linear_fwd(x, gamma, beta, w, b, state: ScalingState, recipe: Recipe, *,
-                  exact: bool = False, update: bool = True):
+                  exact: bool = False, update: bool = True, fp8_weight=None):
     """LayerNormLinear (gamma given) or Linear (gamma None) forward.
 
+    fp8_weight: None, or (codes, scale_inv) of a weight kept in FP8 (see
+    quantize_weight); then w is unused, no weight is cast, slot 1 records no
+    amax, and the GEMM and the saved scale_inv take the weight's own value.
     Returns (Y [M, N] float values rounded to bf16, ctx, aux) where aux holds
     mu, rsigma and the fp32 pre-cast LN output."""
     nm = _Numerics(exact)
     fmt = recipe.fwd_fmt()
+    if fp8_weight is not None and exact:
+        raise ValueError("exact=True has no FP8-stored weight")
     X = _in(x)
-    W = _in(w)
     aux = {}
     if gamma is not None:
         y, mu, rs = _ln.forward(X, _in(gamma), _in(beta))
@@ -131,9 +153,13 @@ def ln_linear_fwd(x, gamma, beta, w, b, state: ScalingState, recipe: Recipe, *,
     aux["y"] = y
     state.record(0, nm.amax(y))
     yq = nm.cast(y, state.scale[0], fmt)
-    state.record(1, nm.amax(W.astype(np.float32)))
-    wq = nm.cast(W, state.scale[1], fmt)
     sinv = state.scale_inv.copy()
+    if fp8_weight is None:
+        W = _in(w)
+        state.record(1, nm.amax(W.astype(np.float32)))
+        wq = nm.cast(W, state.scale[1], fmt)
+    else:
+        wq, sinv[1] = fp8_weight
     acc = nm.dec(yq, fmt) @ nm.dec(wq, fmt).T
     out = acc * nm.dq(sinv[0], sinv[1])
     if b is not None:
@@ -171,11 +197,17 @@ def ln_linear_bwd(dy, ctx: Ctx, gstate: ScalingState, recipe: Recipe, *,
 
 
 def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, state: ScalingState, recipe: Recipe, *,
-               exact: bool = False, update: bool = True, gelu_approx: str = "tanh"):
+               exact: bool = False, update: bool = True, gelu_approx: str = "tanh", fp8_weights=None):
     """LayerNormMLP forward. Returns (Y, ctx, aux); aux holds mu, rsigma, the
-    fp32 pre-cast LN output y and GELU output a, and the bf16 H."""
+    fp32 pre-cast LN output y and GELU output a, and the bf16 H.
+
+    fp8_weights: None, or ((W1 codes, scale_inv), (W2 codes, scale_inv)) of
+    weights kept in FP8 (see quantize_weight); then w1 and w2 are unused, slots
+    1 and 3 record no amax, and their scale_inv come from the weights."""
     nm = _Numerics(exact)
     fmt = recipe.fwd_fmt()
+    if fp8_weights is not None and exact:
+        raise ValueError("exact=True has no FP8-stored weights")
     X = _in(x)
     G = _in(gamma)
     y, mu, rs = _ln.forward(X, G, _in(beta))
@@ -183,14 +215,17 @@ def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, state: ScalingState, recipe: Reci
         xc = X - X.mean(axis=1, keepdims=True)
         y = xc / np.sqrt((xc * xc).mean(axis=1, keepdims=True) + _ln.EPS) * G + _in(beta)
     y = nm.f32(y)
-    W1, W2 = _in(w1), _in(w2)
     state.record(0, nm.amax(y))
     yq = nm.cast(y, state.scale[0], fmt)
-    state.record(1, nm.amax(W1.astype(np.float32)))
-    w1q = nm.cast(W1, state.scale[1], fmt)
-    state.record(3, nm.amax(W2.astype(np.float32)))
-    w2q = nm.cast(W2, state.scale[3], fmt)
     sinv = state.scale_inv.copy()
+    if fp8_weights is None:
+        W1, W2 = _in(w1), _in(w2)
+        state.record(1, nm.amax(W1.astype(np.float32)))
+        w1q = nm.cast(W1, state.scale[1], fmt)
+        state.record(3, nm.amax(W2.astype(np.float32)))
+        w2q = nm.cast(W2, state.scale[3], fmt)
+    else:
+        (w1q, sinv[1]), (w2q, sinv[3]) = fp8_weights
     h = nm.dec(yq, fmt) @ nm.dec(w1q, fmt).T * nm.dq(sinv[0], sinv[1])
     if b1 is not None:
         h = h + _in(b1)[None, :]
