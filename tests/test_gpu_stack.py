@@ -10,12 +10,16 @@ around a synthetic attention output (attention itself is not on the path):
 and the backward in reverse with synthetic dQKV ~ N(0, 0.01) and the residual
 gradient flowing through. Every module call defers its state update; after the
 step one ``amax_history_update_many`` launch updates all layers' forward and
-backward states. The checks, per step and layer: every module output and
-gradient against the oracle module fed the same inputs and the same pre-step
-state (1e-2 relative Frobenius); the states after the one-launch update equal,
-bit for bit, the oracle state machine fed the amaxes the GPU recorded, and equal
-separate per-set updates. The residual adds are test plumbing (torch on the
-GPU side, numpy on the oracle side, both rounding to bf16).
+backward states. The oracle runs the whole stack on its own (its own residual
+stream and its own state machines); the GPU modules take the oracle stream's
+values as inputs, so no oracle input comes from the GPU. The checks, per step
+and layer: every module output and gradient against the oracle module (1e-2
+relative Frobenius); the recorded amaxes and the states after the one-launch
+update against the oracle's own, bit for bit where both sides reduce the same
+bf16 values (weights, Linear inputs, dY) and within a stated relative bound
+where the amax is of an fp32 intermediate; and the update kernel alone, bit for
+bit, against the oracle rule applied to the GPU's pre-update state. The residual
+adds round to bf16 in numpy.
 """
 import numpy as np
 import pytest
@@ -64,6 +68,24 @@ def _to_bits(v):
     return to_bf16_bits(np.asarray(v, np.float64))
 
 
+def _close_state(meta, st, rtol):
+    """GPU state against the oracle's own within rtol (amaxes of fp32 intermediates)."""
+    for name in ("scale", "scale_inv", "amax_history"):
+        g = host(getattr(meta, name)).astype(np.float64)
+        o = getattr(st, name).astype(np.float64)
+        if not np.allclose(g, o, rtol=rtol, atol=0):
+            return False
+    return True
+
+
+# Slots whose amax is max|t| of a tensor both sides hold bit for bit (weights, the bf16 inputs
+# of Linear and of every backward) are compared bit for bit; the others (LayerNorm output, GELU
+# output, dH: fp32 values computed in a different order) within a relative tolerance.
+EXACT = {"fq": [False, True], "fp": [True, True], "fm": [False, True, False, True], "bq": [True], "bp": [True],
+         "bm": [True, False]}
+RTOL = {"fq": 1e-5, "fp": 0.0, "fm": 2e-2, "bq": 0.0, "bp": 0.0, "bm": 2e-2}
+
+
 @pytest.mark.parametrize("layers,M,steps", [(4, 512, 3)])
 def test_block_stack_with_one_state_update_launch(L, layers, M, steps):
     D, F, NQKV = 768, 3072, 2304
@@ -84,72 +106,85 @@ def test_block_stack_with_one_state_update_launch(L, layers, M, steps):
     M_ = [dict(fq=L.ScalingMeta(2, 16), fp=L.ScalingMeta(2, 16), fm=L.ScalingMeta(4, 16),
                bq=L.ScalingMeta(1, 16), bp=L.ScalingMeta(1, 16), bm=L.ScalingMeta(2, 16)) for _ in range(layers)]
     order = ["fq", "fp", "fm", "bq", "bp", "bm"]
+    # the oracle's own states, run next to the GPU's from the same initial state
+    O_ = [{k: ScalingState(m[k].n, 16) for k in order} for m in M_]
     dts = {"fq": [E4, E4], "fp": [E4, E4], "fm": [E4] * 4, "bq": [E5], "bp": [E5], "bm": [E5, E5]}
     ofmts = {"fq": [ff] * 2, "fp": [ff] * 2, "fm": [ff] * 4, "bq": [gf], "bp": [gf], "bm": [gf] * 2}
     for step in range(steps):
-        pre = [{k: _state(m[k]) for k in order} for m in M_]
+        # the residual stream is the oracle's: both sides get its values at every layer
         h = bf16_to_f32(synth.activations(M, D, dist="outliers", step=step)).astype(np.float64)
         saved = []
         for l in range(layers):
-            p, d, m, st = P[l], dev[l], M_[l], pre[l]
+            p, d, m, o = P[l], dev[l], M_[l], O_[l]
             hb = _to_bits(h)
             attn = synth.activations(M, D, step=step, tid=synth.TID["attn"], layer=l)
             xq = bf16_dev(hb)
             qkv, cq = L.ln_linear_fwd(xq, d["qkv"]["gamma"], d["qkv"]["beta"], d["qkv"]["w"], d["qkv"]["b"], m["fq"], rec,
                                       defer_update=True)
             oq_y, ocq, _ = omod.ln_linear_fwd(hb, p["qkv"]["gamma"], p["qkv"]["beta"], p["qkv"]["w"], p["qkv"]["b"],
-                                              st["fq"].copy(), orec, update=False)
+                                              o["fq"], orec, update=False)
             assert rel_fro(host(qkv), oq_y) < TOL, (step, l, "qkv")
             xa = bf16_dev(attn)
             pr, cp = L.ln_linear_fwd(xa, None, None, d["proj"]["w"], d["proj"]["b"], m["fp"], rec, defer_update=True)
-            op_y, ocp, _ = omod.ln_linear_fwd(attn, None, None, p["proj"]["w"], p["proj"]["b"], st["fp"].copy(), orec,
+            op_y, ocp, _ = omod.ln_linear_fwd(attn, None, None, p["proj"]["w"], p["proj"]["b"], o["fp"], orec,
                                               update=False)
             assert rel_fro(host(pr), op_y) < TOL, (step, l, "proj")
-            h = _bf16_add(h, host(pr))
+            h = _bf16_add(h, op_y)
             hb2 = _to_bits(h)
             xm = bf16_dev(hb2)
             y, cm = L.ln_mlp_fwd(xm, d["mlp"]["gamma"], d["mlp"]["beta"], d["mlp"]["w1"], d["mlp"]["b1"], d["mlp"]["w2"],
                                  d["mlp"]["b2"], m["fm"], rec, defer_update=True)
             om_y, ocm, _ = omod.ln_mlp_fwd(hb2, p["mlp"]["gamma"], p["mlp"]["beta"], p["mlp"]["w1"], p["mlp"]["b1"],
-                                           p["mlp"]["w2"], p["mlp"]["b2"], st["fm"].copy(), orec, update=False)
+                                           p["mlp"]["w2"], p["mlp"]["b2"], o["fm"], orec, update=False)
             assert rel_fro(host(y), om_y) < TOL, (step, l, "mlp")
-            h = _bf16_add(h, host(y))
+            h = _bf16_add(h, om_y)
             saved.append((xq, cq, ocq, xa, cp, ocp, xm, cm, ocm))
         dh = bf16_to_f32(synth.grad(M, D, step=step)).astype(np.float64)
         for l in reversed(range(layers)):
-            p, d, m, st = P[l], dev[l], M_[l], pre[l]
+            p, d, m, o = P[l], dev[l], M_[l], O_[l]
             xq, cq, ocq, xa, cp, ocp, xm, cm, ocm = saved[l]
             g = L.ln_mlp_bwd(bf16_dev(_to_bits(dh)), xm, d["mlp"]["gamma"], cm, m["bm"], rec, defer_update=True)
-            og = omod.ln_mlp_bwd(_to_bits(dh), ocm, st["bm"].copy(), orec, update=False)
+            og = omod.ln_mlp_bwd(_to_bits(dh), ocm, o["bm"], orec, update=False)
             for k in ("dx", "dw1", "dw2", "dgamma"):
                 assert rel_fro(host(getattr(g, k)), og[k]) < TOL, (step, l, "mlp", k)
-            dh = _bf16_add(dh, host(g.dx))
+            dh = _bf16_add(dh, og["dx"])
             gp = L.ln_linear_bwd(bf16_dev(_to_bits(dh)), xa, None, cp, m["bp"], rec, defer_update=True)
-            ogp = omod.ln_linear_bwd(_to_bits(dh), ocp, st["bp"].copy(), orec, update=False)
+            ogp = omod.ln_linear_bwd(_to_bits(dh), ocp, o["bp"], orec, update=False)
             assert rel_fro(host(gp.dw), ogp["dw"]) < TOL, (step, l, "proj dw")
             dqkv = synth.grad(M, NQKV, step=step, layer=l, tid=synth.TID["attn"])
             gq = L.ln_linear_bwd(bf16_dev(dqkv), xq, d["qkv"]["gamma"], cq, m["bq"], rec, defer_update=True)
-            ogq = omod.ln_linear_bwd(dqkv, ocq, st["bq"].copy(), orec, update=False)
+            ogq = omod.ln_linear_bwd(dqkv, ocq, o["bq"], orec, update=False)
             for k in ("dx", "dw", "dgamma"):
                 assert rel_fro(host(getattr(gq, k)), ogq[k]) < TOL, (step, l, "qkv", k)
-            dh = _bf16_add(dh, host(gq.dx))
+            dh = _bf16_add(dh, ogq["dx"])
         L.sync_status()
-        # one launch for every layer's six states; a copy updated set by set must agree
-        copies = [{k: _state(m[k]) for k in order} for m in M_]
+        # the recorded amaxes: bit for bit where both sides reduce the same values
+        for l in range(layers):
+            for k in order:
+                ga = host(M_[l][k].amax_cur).astype(np.float32)
+                oa = O_[l][k].amax_cur
+                for i in range(len(ga)):
+                    if EXACT[k][i]:
+                        assert ga[i].view(np.uint32) == oa[i].view(np.uint32), (step, l, k, i)
+                    else:
+                        assert abs(float(ga[i]) - float(oa[i])) <= RTOL[k] * float(oa[i]), (step, l, k, i)
+        # one launch for every layer's six states
+        pre = [{k: _state(m[k]) for k in order} for m in M_]
         metas = [m[k] for m in M_ for k in order]
         L.amax_history_update_many(metas, rec, [dts[k] for _ in M_ for k in order])
         L.sync_status()
         for l in range(layers):
             for k in order:
-                ost = copies[l][k].copy()
-                ost.update(ofmts[k])
-                assert _bits_equal(M_[l][k], ost), (step, l, k)
-                # the teacher-forced oracle: the pre-step state fed the amaxes the GPU recorded
+                O_[l][k].update(ofmts[k])
+                # against the oracle's own state machine
+                if all(EXACT[k]):
+                    assert _bits_equal(M_[l][k], O_[l][k]), (step, l, k)
+                else:
+                    assert _close_state(M_[l][k], O_[l][k], RTOL[k]), (step, l, k)
+                # the update kernel on its own: the GPU's pre-update state through the oracle rule
                 tf = pre[l][k].copy()
-                for i in range(tf.n):
-                    tf.record(i, copies[l][k].amax_cur[i])
                 tf.update(ofmts[k])
-                assert _bits_equal(M_[l][k], tf), (step, l, k, "teacher-forced")
+                assert _bits_equal(M_[l][k], tf), (step, l, k, "update rule")
 
 
 def test_update_many_equals_separate_updates(L):
