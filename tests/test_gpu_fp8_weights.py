@@ -66,7 +66,8 @@ def test_linear_fwd_with_fp8_weight(L, M, ln):
     p = synth.linear_params(N, K, ln=ln, layer=1, bias_std=0.02)
     fw = L.quantize_weight(bf16_dev(p["w"]), rec)
     codes0 = fw.codes.clone()
-    wcodes, wsinv = host(fw.codes), np.float32(host(fw.scale_inv)[0])
+    wcodes, wsinv, _ = omod.quantize_weight(p["w"], orec)  # the oracle's own conversion
+    assert np.array_equal(host(fw.codes), wcodes)
     meta = L.ScalingMeta(2, 16)
     gmeta = L.ScalingMeta(1, 16)
     g = bf16_dev(p["gamma"]) if ln else None
@@ -107,7 +108,8 @@ def test_mlp_fwd_with_fp8_weights(L, M, fused):
     ff = orec.fwd_fmt()
     p = synth.mlp_params(D, F, layer=3, bias_std=0.02)
     f1, f2 = L.quantize_weight(bf16_dev(p["w1"]), rec), L.quantize_weight(bf16_dev(p["w2"]), rec)
-    ow = ((host(f1.codes), np.float32(host(f1.scale_inv)[0])), (host(f2.codes), np.float32(host(f2.scale_inv)[0])))
+    ow = (omod.quantize_weight(p["w1"], orec)[:2], omod.quantize_weight(p["w2"], orec)[:2])
+    assert np.array_equal(host(f1.codes), ow[0][0]) and np.array_equal(host(f2.codes), ow[1][0])
     meta = L.ScalingMeta(4, 16)
     dev = {k: bf16_dev(v) for k, v in p.items()}
     for step in range(2):
