@@ -288,6 +288,111 @@ class MlpRun:
         self.graphs = graphs
 
 
+def stack_flops_per_step(layers, m, d, f):
+    """Six GEMMs per module (forward, data and weight gradients): QKV d -> 3d, proj d -> d, MLP d -> f -> d."""
+    return layers * 6.0 * m * d * (3 * d + d + 2 * f)
+
+
+class StackRun:
+    """A stack of transformer-block FP8 modules as one training step: per layer
+    LayerNormLinear d -> 3d (QKV), Linear d -> d (attention-output projection, fed
+    a synthetic attention output) and LayerNormMLP d -> f -> d, forward over the
+    layers then backward in reverse, every module with its state update deferred
+    and one state-update launch for all layers' sets at the end of the step.
+
+    Each layer's inputs (h ~ N(0,1) with 0.1% x50 outliers, attention output ~
+    N(0,1), dQKV and dY ~ N(0, 0.01)) are device-resident, generated once; the
+    layers are not chained through residual adds (attention and residuals are
+    not part of this path), so the step's work is exactly the modules'. The whole
+    step is one captured CUDA graph."""
+
+    def __init__(self, L, torch, dev, layers, m, d, f, fmt, hist, seed):
+        self.L, self.torch, self.layers, self.m, self.d, self.f = L, torch, layers, m, d, f
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+
+        def randn(*shape, std=1.0, outliers=False):
+            t = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32) * std
+            if outliers:
+                t = torch.where(torch.rand(*shape, generator=g, device=dev) < 1e-3, t * 50, t)
+            return t.to(torch.bfloat16)
+
+        def ones_plus(n):
+            return (1 + 0.1 * torch.randn(n, generator=g, device=dev)).to(torch.bfloat16)
+
+        self.rec = L.Recipe(fmt, hist)
+        E4, E5 = L.E4M3, L.E5M2
+        self.layer = []
+        for _ in range(layers):
+            lay = dict(
+                wqkv=randn(3 * d, d, std=0.02), bqkv=torch.zeros(3 * d, dtype=torch.bfloat16, device=dev),
+                g1=ones_plus(d), be1=randn(d, std=0.1),
+                wproj=randn(d, d, std=0.02), bproj=torch.zeros(d, dtype=torch.bfloat16, device=dev),
+                g2=ones_plus(d), be2=randn(d, std=0.1),
+                w1=randn(f, d, std=0.02), b1=torch.zeros(f, dtype=torch.bfloat16, device=dev),
+                w2=randn(d, f, std=0.02), b2=torch.zeros(d, dtype=torch.bfloat16, device=dev),
+                h=randn(m, d, outliers=True), attn=randn(m, d), dqkv=randn(m, 3 * d, std=0.01),
+                dy=randn(m, d, std=0.01),
+                fq=L.ScalingMeta(2, hist, device=dev), fp=L.ScalingMeta(2, hist, device=dev),
+                fm=L.ScalingMeta(4, hist, device=dev), bq=L.ScalingMeta(1, hist, device=dev),
+                bp=L.ScalingMeta(1, hist, device=dev), bm=L.ScalingMeta(2, hist, device=dev),
+                cq=L.linear_ctx(m, d, 3 * d, device=dev), cp=L.linear_ctx(m, d, d, ln=False, device=dev),
+                cm=L.mlp_ctx(m, d, f, device=dev),
+                gq=L.linear_grads(m, d, 3 * d, device=dev), gp=L.linear_grads(m, d, d, ln=False, device=dev),
+                gm=L.mlp_grads(m, d, f, device=dev))
+            self.layer.append(lay)
+        # module outputs the stack does not consume share one buffer per shape
+        self.yq = torch.empty(m, 3 * d, dtype=torch.bfloat16, device=dev)
+        self.yd = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
+        self.order = ["fq", "fp", "fm", "bq", "bp", "bm"]
+        dts = {"fq": [E4] * 2, "fp": [E4] * 2, "fm": [E4] * 4, "bq": [E5], "bp": [E5], "bm": [E5] * 2}
+        self.metas = [lay[k] for lay in self.layer for k in self.order]
+        self.dtypes = [dts[k] for _ in self.layer for k in self.order]
+        self.graphs = None
+
+    def _call(self):
+        L, rec = self.L, self.rec
+        for lay in self.layer:
+            L.ln_linear_fwd(lay["h"], lay["g1"], lay["be1"], lay["wqkv"], lay["bqkv"], lay["fq"], rec, y=self.yq,
+                            ctx=lay["cq"], defer_update=True)
+            L.ln_linear_fwd(lay["attn"], None, None, lay["wproj"], lay["bproj"], lay["fp"], rec, y=self.yd,
+                            ctx=lay["cp"], defer_update=True)
+            L.ln_mlp_fwd(lay["h"], lay["g2"], lay["be2"], lay["w1"], lay["b1"], lay["w2"], lay["b2"], lay["fm"], rec,
+                         y=self.yd, ctx=lay["cm"], defer_update=True)
+        for lay in reversed(self.layer):
+            L.ln_mlp_bwd(lay["dy"], lay["h"], lay["g2"], lay["cm"], lay["bm"], rec, grads=lay["gm"], defer_update=True)
+            L.ln_linear_bwd(lay["dy"], lay["attn"], None, lay["cp"], lay["bp"], rec, grads=lay["gp"],
+                            defer_update=True)
+            L.ln_linear_bwd(lay["dqkv"], lay["h"], lay["g1"], lay["cq"], lay["bq"], rec, grads=lay["gq"],
+                            defer_update=True)
+        L.amax_history_update_many(self.metas, rec, self.dtypes)
+
+    def step(self, i):
+        if self.graphs is not None:
+            self.graphs[0].replay()
+        else:
+            self._call()
+
+    def capture(self):
+        torch = self.torch
+        sds = [m.state_dict() for m in self.metas]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            c0 = self.L.launch_count()
+            self._call()
+            self.launches_per_step = self.L.launch_count() - c0
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            self._call()
+        torch.cuda.synchronize()
+        for m, sd in zip(self.metas, sds):
+            m.load_state_dict(sd)
+        self.graphs = [gr]
+
+
 def timed_steps(torch, run, steps, warmup, flush, barrier):
     """W untimed warm-up steps, then K steps each bracketed by CUDA events on the
     launching (current) stream, an L2 flush between them outside the events.
@@ -541,6 +646,34 @@ def run_gpu(args):
         d2048["frac_of_fp8_peak"] = d2048["value"] / world / fp8_peak
         del run2
 
+    # ---- the scale-up stack: 12 layers of d 2048 (QKV, projection, MLP 8192) over 16384 tokens,
+    # amax_history_len 1024, the whole step one CUDA graph with one state-update launch
+    stack = None
+    if not args.no_stack:
+        ls, ms_, ds, fs, hs = 12, 16384, 2048, 8192, 1024
+        torch.cuda.empty_cache()
+        srun = StackRun(L, torch, dev, ls, ms_, ds, fs, FMT, hs, seed=977 + rank)
+        if args.graph:
+            srun.capture()
+        ks = max(3, min(args.steps, 20))
+        sms, slaunch = timed_steps(torch, srun, ks, 3, flush, barrier)
+        sms = max_over_ranks(sms)
+        L.sync_status()
+        stack = {"value": stack_flops_per_step(ls, ms_, ds, fs) * ks * world / (sms / 1e3) / 1e12,
+                 "unit": "TFLOP/s", "ms_per_step": sms / ks, "steps": ks, "gpu_launches": slaunch,
+                 "frac_of_fp8_peak": None, "cuda_graph": bool(args.graph),
+                 "config": {"workload": f"transformer-block FP8 module stack fwd+bwd: {ls} layers x (LayerNormLinear "
+                                        f"{ds}->{3 * ds}, Linear {ds}->{ds}, LayerNormMLP {ds}->{fs}->{ds}), {ms_} "
+                                        f"tokens, {FMT.upper()}, amax_history_len {hs}, one state-update launch for "
+                                        f"all {6 * ls} state sets",
+                            "layers": ls, "tokens": ms_, "d_model": ds, "ffn": fs, "amax_history_len": hs,
+                            "inputs": "per layer, device-resident: h N(0,1) + 0.1% x50, attention output N(0,1), "
+                                      "dQKV and dY N(0, 0.01); layers not chained (no residual adds)",
+                            "flops": "six GEMMs per module"}}
+        stack["frac_of_fp8_peak"] = stack["value"] / world / fp8_peak
+        del srun
+        torch.cuda.empty_cache()
+
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -556,7 +689,8 @@ def run_gpu(args):
                 "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)", "data": "synthetic",
                 "config": dict(workload(), cuda_graph=bool(args.graph)), "frac_of_fp8_peak": value / world / fp8_peak,
                 "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline,
-                "per_kernel": per_kernel, "hbm_peak_gbs": hbm, "cpu_baseline": cpu, "d2048": d2048}
+                "per_kernel": per_kernel, "hbm_peak_gbs": hbm, "cpu_baseline": cpu, "d2048": d2048,
+                "stack2048x12": stack}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -573,6 +707,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-d2048", action="store_true")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 12-layer d 2048 stack step")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph (1) or call (0)")
     args = ap.parse_args()
     if args.warmup < 3:

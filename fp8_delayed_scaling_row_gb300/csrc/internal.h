@@ -14,7 +14,7 @@ namespace lnfp8 {
 lnfp8_status validate_meta(const lnfp8_meta* m, int expect_n, const char* who);
 lnfp8_status meta_init_launch(const lnfp8_meta* m, cudaStream_t st);
 // one state-update launch for up to kMaxUpdateSets tensor sets (each validated by the caller)
-constexpr int kMaxUpdateSets = 64;
+constexpr int kMaxUpdateSets = 128;  // the table travels as a ~7.7 KB kernel parameter
 lnfp8_status update_many_launch(const lnfp8_meta* const* metas, const uint64_t* e5m2_masks, float* const* sinv_before,
                                 int count, int margin, cudaStream_t st);
 lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, float* sinv_before,

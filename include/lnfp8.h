@@ -159,7 +159,7 @@ lnfp8_status amax_history_update(const lnfp8_meta* meta, const lnfp8_recipe* rec
                                  const int* dtype_per_tensor, float* scale_inv_before,
                                  lnfp8_stream stream);
 
-/* The same update for `count` tensor sets (0..64; e.g. every layer of a model
+/* The same update for `count` tensor sets (0..128; e.g. every layer of a model
  * after the step, its module calls having run with defer_update) in ONE kernel
  * launch. metas: HOST array [count]; dtypes: HOST array, the sets' per-slot
  * lnfp8_dtype values one after another (sum of the n's entries);

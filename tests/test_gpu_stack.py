@@ -187,11 +187,12 @@ def test_block_stack_with_one_state_update_launch(L, layers, M, steps):
                 assert _bits_equal(M_[l][k], tf), (step, l, k, "update rule")
 
 
-def test_update_many_equals_separate_updates(L):
-    rec = L.Recipe("hybrid", 8)
+@pytest.mark.parametrize("ns,hist", [((1, 2, 4, 3), 8), (tuple(1 + k % 4 for k in range(128)), 1024)])
+def test_update_many_equals_separate_updates(L, ns, hist):
+    rec = L.Recipe("hybrid", hist)
     rng = np.random.default_rng(3)
-    metas = [L.ScalingMeta(n, 8) for n in (1, 2, 4, 3)]
-    twins = [L.ScalingMeta(m.n, 8) for m in metas]
+    metas = [L.ScalingMeta(n, hist) for n in ns]
+    twins = [L.ScalingMeta(m.n, hist) for m in metas]
     dts = [[L.E4M3] * m.n if i % 2 == 0 else [L.E5M2] * m.n for i, m in enumerate(metas)]
     for step in range(5):
         for m, t in zip(metas, twins):
@@ -210,3 +211,5 @@ def test_update_many_equals_separate_updates(L):
         for sn, b in zip(snaps, before):
             assert torch.equal(sn, b), step
     L.amax_history_update_many([], rec, [])  # nothing to do
+    with pytest.raises(L.LnFp8Error):  # more sets than one launch takes
+        L.amax_history_update_many(metas + metas[:1] * (129 - len(metas)), rec, dts + dts[:1] * (129 - len(metas)))
