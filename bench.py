@@ -67,51 +67,76 @@ def _num(d, *keys):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """nvidia-smi sampling of SM clocks and throttle reasons. The sampler starts
+    before the timed region and keeps only the samples taken between mark_start()
+    and mark_stop() (by nvidia-smi's own timestamps)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, tag: str = ""):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}{tag}.csv")
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(self.idx)], stdout=self.fh,
+                                          "-lms", "50", "-i", str(self.idx)], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        deadline = time.time() + 10.0  # nvidia-smi needs a moment before its first sample
+        while time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _when(ts):
+        base, _, frac = ts.partition(".")
+        return time.mktime(time.strptime(base, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac else 0.0)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)  # one more sample past the end of the region
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                t = self._when(f[0])
+                if self.t0 is not None and not (self.t0 - 0.05 <= t <= (self.t1 or t) + 0.05):
+                    continue
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+                pw.append(float(f[4]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def gemm_sources_sha1():
@@ -373,16 +398,17 @@ class StackRun:
         else:
             self._call()
 
-    def capture(self):
+    def capture(self, warm=True):
         torch = self.torch
         sds = [m.state_dict() for m in self.metas]
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            c0 = self.L.launch_count()
-            self._call()
-            self.launches_per_step = self.L.launch_count() - c0
-        torch.cuda.current_stream().wait_stream(s)
+        if warm:  # one direct step on a side stream before the first capture
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                c0 = self.L.launch_count()
+                self._call()
+                self.launches_per_step = self.L.launch_count() - c0
+            torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr):
@@ -393,7 +419,7 @@ class StackRun:
         self.graphs = [gr]
 
 
-def timed_steps(torch, run, steps, warmup, flush, barrier):
+def timed_steps(torch, run, steps, warmup, flush, barrier, clocks=None):
     """W untimed warm-up steps, then K steps each bracketed by CUDA events on the
     launching (current) stream, an L2 flush between them outside the events.
     Returns (device ms summed over the K steps, library kernel launches in them)."""
@@ -401,6 +427,8 @@ def timed_steps(torch, run, steps, warmup, flush, barrier):
         run.step(i)
     torch.cuda.synchronize()
     barrier()
+    if clocks is not None:
+        clocks.mark_start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     n0 = run.L.launch_count()
     for i in range(steps):
@@ -410,6 +438,8 @@ def timed_steps(torch, run, steps, warmup, flush, barrier):
         ev[i][1].record()
     n1 = run.L.launch_count()
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark_stop()
     barrier()
     launches = n1 - n0
     if run.graphs is not None:
@@ -527,6 +557,55 @@ def end_to_end(torch, run, steps, dev, barrier, max_over_ranks, world, graph=Tru
                       "overlapping the neighbouring steps' compute (two device buffer sets)"}
 
 
+def run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak):
+    """The scale-up stack step (StackRun), timed like the main workload, with its own
+    clock record and per-kernel times."""
+    ls, ms_, ds, fs, hs = args.stack_layers, 16384, 2048, 8192, 1024
+    torch.cuda.empty_cache()
+    srun = StackRun(L, torch, dev, ls, ms_, ds, fs, FMT, hs, seed=977 + rank)
+    if args.graph:
+        srun.capture()
+    ks = max(3, min(args.steps, 40))
+    sclk = ClockSampler(local, "_stack")
+    sclk.start()
+    sms, slaunch = timed_steps(torch, srun, ks, 3, flush, barrier, sclk)
+    sclk = sclk.stop()
+    sms = max_over_ranks(sms)
+    L.sync_status()
+    stack = {"value": stack_flops_per_step(ls, ms_, ds, fs) * ks * world / (sms / 1e3) / 1e12,
+             "unit": "TFLOP/s", "ms_per_step": sms / ks, "steps": ks, "gpu_launches": slaunch,
+             "frac_of_fp8_peak": None, "cuda_graph": bool(args.graph), "clocks": sclk,
+             "config": {"workload": f"transformer-block FP8 module stack fwd+bwd: {ls} layers x (LayerNormLinear "
+                                    f"{ds}->{3 * ds}, Linear {ds}->{ds}, LayerNormMLP {ds}->{fs}->{ds}), {ms_} "
+                                    f"tokens, {FMT.upper()}, amax_history_len {hs}, one state-update launch for "
+                                    f"all {6 * ls} state sets",
+                        "layers": ls, "tokens": ms_, "d_model": ds, "ffn": fs, "amax_history_len": hs,
+                        "inputs": "per layer, device-resident: h N(0,1) + 0.1% x50, attention output N(0,1), "
+                                  "dQKV and dY N(0, 0.01); layers not chained (no residual adds)",
+                        "flops": "six GEMMs per module"}}
+    stack["frac_of_fp8_peak"] = stack["value"] / world / fp8_peak
+    # per-kernel times of the same step (the library's event pairs as graph nodes)
+    if args.graph:
+        L.profile_enable(True)
+        srun.capture(warm=False)
+        for _ in range(3):
+            flush.zero_()
+            srun.step(0)
+            L.profile_sample()
+        sprof = L.profile_collect()
+        L.profile_enable(False)
+        tot = sum(v[0] for v in sprof.values()) or 1.0
+        stack["per_kernel"] = {k: {"ms_per_step": v[0] / 3, "launches_per_step": v[1] / 3, "share": v[0] / tot}
+                               for k, v in sorted(sprof.items(), key=lambda kv: -kv[1][0])}
+        gk = [v for k, v in sprof.items() if k.startswith("gemm")]
+        if gk:
+            stack["gemm_family_tflops"] = stack_flops_per_step(ls, ms_, ds, fs) / (sum(v[0] for v in gk) / 3 / 1e3) / 1e12
+    del srun
+    torch.cuda.empty_cache()
+
+    return stack
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -553,6 +632,13 @@ def run_gpu(args):
         return float(t.item())
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.stack_only:  # diagnostic: the stack step alone (e.g. a one-layer case to profile)
+        pk, _ = peaks()
+        fp8_peak = (_num(pk, "bf16_tflops", "bf16_tflops_burst") or FALLBACK["bf16_tflops"]) * FP8_PER_BF16
+        stack = run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak)
+        if rank == 0:
+            print(json.dumps({"stack": stack}), flush=True)
+        return 0
     n_sets = min(args.steps + args.warmup, 8)
     run = MlpRun(L, torch, dev, M_TOK, D_MODEL, FFN, FMT, HIST, "outliers", n_sets, seed=1234 + 7919 * rank)
     if args.graph:
@@ -561,7 +647,7 @@ def run_gpu(args):
     # ---- main timed region (device time, CUDA events, L2 flushed between steps)
     clocks = ClockSampler(local)
     clocks.start()
-    ms, gpu_launches = timed_steps(torch, run, args.steps, args.warmup, flush, barrier)
+    ms, gpu_launches = timed_steps(torch, run, args.steps, args.warmup, flush, barrier, clocks)
     clk = clocks.stop()
     L.sync_status()
     ms = max_over_ranks(ms)
@@ -646,33 +732,8 @@ def run_gpu(args):
         d2048["frac_of_fp8_peak"] = d2048["value"] / world / fp8_peak
         del run2
 
-    # ---- the scale-up stack: 12 layers of d 2048 (QKV, projection, MLP 8192) over 16384 tokens,
-    # amax_history_len 1024, the whole step one CUDA graph with one state-update launch
-    stack = None
-    if not args.no_stack:
-        ls, ms_, ds, fs, hs = 12, 16384, 2048, 8192, 1024
-        torch.cuda.empty_cache()
-        srun = StackRun(L, torch, dev, ls, ms_, ds, fs, FMT, hs, seed=977 + rank)
-        if args.graph:
-            srun.capture()
-        ks = max(3, min(args.steps, 20))
-        sms, slaunch = timed_steps(torch, srun, ks, 3, flush, barrier)
-        sms = max_over_ranks(sms)
-        L.sync_status()
-        stack = {"value": stack_flops_per_step(ls, ms_, ds, fs) * ks * world / (sms / 1e3) / 1e12,
-                 "unit": "TFLOP/s", "ms_per_step": sms / ks, "steps": ks, "gpu_launches": slaunch,
-                 "frac_of_fp8_peak": None, "cuda_graph": bool(args.graph),
-                 "config": {"workload": f"transformer-block FP8 module stack fwd+bwd: {ls} layers x (LayerNormLinear "
-                                        f"{ds}->{3 * ds}, Linear {ds}->{ds}, LayerNormMLP {ds}->{fs}->{ds}), {ms_} "
-                                        f"tokens, {FMT.upper()}, amax_history_len {hs}, one state-update launch for "
-                                        f"all {6 * ls} state sets",
-                            "layers": ls, "tokens": ms_, "d_model": ds, "ffn": fs, "amax_history_len": hs,
-                            "inputs": "per layer, device-resident: h N(0,1) + 0.1% x50, attention output N(0,1), "
-                                      "dQKV and dY N(0, 0.01); layers not chained (no residual adds)",
-                            "flops": "six GEMMs per module"}}
-        stack["frac_of_fp8_peak"] = stack["value"] / world / fp8_peak
-        del srun
-        torch.cuda.empty_cache()
+    stack = None if args.no_stack else run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local,
+                                                    rank, fp8_peak)
 
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0
     cpu = None
@@ -700,7 +761,7 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=512, help="tokens per oracle step of the cpu_baseline leg")
@@ -708,6 +769,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-d2048", action="store_true")
     ap.add_argument("--no-stack", action="store_true", help="skip the 12-layer d 2048 stack step")
+    ap.add_argument("--stack-only", action="store_true", help="run only the stack step (prints its own line)")
+    ap.add_argument("--stack-layers", type=int, default=12)
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph (1) or call (0)")
     args = ap.parse_args()
     if args.warmup < 3:

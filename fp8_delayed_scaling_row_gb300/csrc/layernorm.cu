@@ -9,10 +9,14 @@
 // fp32/bf16 LayerNorm output never reaches HBM.
 //
 // Both kernels are HBM-bound. A group of TPR threads owns one row (TPR = 32 is
-// a warp per row; wider rows use 64..256 threads so that a thread keeps at
-// most 4 x 16-byte vectors of the row in registers). Loads are 128-bit,
-// consecutive threads read consecutive 16-byte chunks, and row sums are warp
-// shuffles (plus one shared-memory exchange when TPR > 32).
+// a warp per row; wider rows use 64..256 threads so that a thread holds at most
+// 4 x 16-byte vectors of the row). Consecutive threads read consecutive 16-byte
+// chunks, and row sums are warp shuffles (plus one shared-memory exchange when
+// TPR > 32). The loads run ahead of the arithmetic through a per-thread ring
+// in shared memory: each thread copies (cp.async, 16 bytes) the chunks of the
+// rows it will normalise RING - 2 iterations later, so the bytes in flight per
+// SM no longer depend on registers. A thread only ever reads the ring slots it
+// filled itself, and refills a slot two iterations after it last read it.
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,6 +24,24 @@ namespace lnfp8 {
 namespace {
 
 constexpr int kThreads = 256;
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Ring depth (slots) per thread: deeper for short per-thread chunks of a row.
+__host__ __device__ constexpr int fwd_ring(int nv) { return nv <= 2 ? 6 : 4; }
+__host__ __device__ constexpr int bwd_ring(int nv) { return nv <= 2 ? 5 : (nv == 3 ? 4 : 3); }
 
 __device__ __forceinline__ void unpack8(uint4 u, float* v) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -56,13 +78,16 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
               const uint16_t* __restrict__ beta, float eps, int64_t M, int D,
               const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
               float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg) {
+  constexpr int RING = fwd_ring(NV);
+  constexpr int P = RING - 2;  // rows in flight ahead of the one being normalised
   __shared__ float xch[kThreads / 32];
   __shared__ uint32_t ared[kThreads / 32];
-  extern __shared__ uint4 sgb[];  // gamma then beta, D/8 16-byte vectors each
+  extern __shared__ uint4 sgb[];  // gamma then beta (D/8 16-byte vectors each), then the ring
   constexpr int GPB = kThreads / TPR;  // row groups per block
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
   const int nvec = D >> 3;
+  uint4* ring = sgb + 2 * nvec;  // [RING][NV][kThreads]
   pdl_wait();
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < nvec; i += kThreads) {
@@ -75,22 +100,33 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   const int64_t stride = (int64_t)gridDim.x * GPB;
   uint32_t am = 0;
 
-  auto load_row = [&](int64_t row, uint4* raw) {
+  // one commit group per iteration (empty past the last row) keeps the group count regular
+  auto issue = [&](int64_t r, int slot) {
+    if (r < M) {
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int c = (gt + TPR * j) * 8;
-      raw[j] = make_uint4(0, 0, 0, 0);
-      if (row < M && c < D) raw[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
+      for (int j = 0; j < NV; ++j) {
+        const int c = (gt + TPR * j) * 8;
+        if (c < D) cp_async16(&ring[(slot * NV + j) * kThreads + threadIdx.x], x + r * D + c);
+      }
     }
+    cp_async_commit();
   };
 
   int64_t row = (int64_t)blockIdx.x * GPB + g;
-  uint4 raw[NV];
-  load_row(row, raw);
+#pragma unroll
+  for (int k = 0; k < P; ++k) issue(row + k * stride, k);
+  int slot = 0;
   // every thread of the block runs the same trip count (group_sum may use barriers)
   for (; row - g < M; row += stride) {
-    uint4 nxt[NV];
-    load_row(row + stride, nxt);  // the next row's loads are in flight during this row's math
+    issue(row + P * stride, slot + P < RING ? slot + P : slot + P - RING);
+    cp_async_wait<P>();  // this iteration's group has landed
+    uint4 raw[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      raw[j] = (row < M && c < D) ? ring[(slot * NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+    }
+    slot = slot + 1 == RING ? 0 : slot + 1;
     const bool active = row < M;
     float sum = 0.f;
 #pragma unroll
@@ -144,9 +180,8 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
         rs_out[row] = rs;
       }
     }
-#pragma unroll
-    for (int j = 0; j < NV; ++j) raw[j] = nxt[j];
   }
+  cp_async_wait<0>();
   block_amax_commit(am, ared, amax_cur);
 }
 
@@ -156,14 +191,21 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
               const uint16_t* __restrict__ gamma, const float* __restrict__ mu_in,
               const float* __restrict__ rs_in, int64_t M, int D, uint16_t* __restrict__ dx,
               float* dgamma, float* dbeta) {
+  constexpr int RING = bwd_ring(NV);
+  constexpr int P = RING - 2;  // rows in flight ahead of the one being processed
   __shared__ float xch[kThreads / 32];
-  extern __shared__ float colred[];  // [2][D] block partials of dgamma, dbeta, then gamma [D/8 uint4]
+  // [2][D] block partials of dgamma, dbeta; gamma [D/8 uint4]; the ring of x and dY chunks
+  // [RING][2 NV][kThreads] uint4; then the ring of mu, rsigma [RING][2][kThreads] fp32
+  extern __shared__ float colred[];
   uint4* sg = reinterpret_cast<uint4*>(colred + 2 * D);
   constexpr int GPB = kThreads / TPR;
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
   const float inv_d = 1.0f / (float)D;
   const int nvec = D >> 3;
+  uint4* ring = sg + nvec;
+  float* rstat = reinterpret_cast<float*>(ring + RING * 2 * NV * kThreads);
+  const int64_t stride = (int64_t)gridDim.x * GPB;
   pdl_wait();
   pdl_launch_dependents();
 
@@ -171,26 +213,49 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
   for (int i = threadIdx.x; i < nvec; i += kThreads) sg[i] = reinterpret_cast<const uint4*>(gamma)[i];
   __syncthreads();
 
+  auto issue = [&](int64_t r, int slot) {
+    if (r < M) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int c = (gt + TPR * j) * 8;
+        if (c < D) {
+          cp_async16(&ring[(slot * 2 * NV + j) * kThreads + threadIdx.x], x + r * D + c);
+          cp_async16(&ring[(slot * 2 * NV + NV + j) * kThreads + threadIdx.x], dy + r * D + c);
+        }
+      }
+      cp_async4(&rstat[(slot * 2 + 0) * kThreads + threadIdx.x], mu_in + r);
+      cp_async4(&rstat[(slot * 2 + 1) * kThreads + threadIdx.x], rs_in + r);
+    }
+    cp_async_commit();
+  };
+
   float accg[NV][8], accb[NV][8];
 #pragma unroll
   for (int j = 0; j < NV; ++j)
 #pragma unroll
     for (int i = 0; i < 8; ++i) accg[j][i] = accb[j][i] = 0.f;
 
-  for (int64_t row = (int64_t)blockIdx.x * GPB + g; row - g < M; row += (int64_t)gridDim.x * GPB) {
+  int64_t row = (int64_t)blockIdx.x * GPB + g;
+#pragma unroll
+  for (int k = 0; k < P; ++k) issue(row + k * stride, k);
+  int slot = 0;
+  for (; row - g < M; row += stride) {
+    issue(row + P * stride, slot + P < RING ? slot + P : slot + P - RING);
+    cp_async_wait<P>();  // this iteration's group has landed
     const bool active = row < M;
-    const float mu = active ? mu_in[row] : 0.f;
-    const float rs = active ? rs_in[row] : 0.f;
+    const float mu = active ? rstat[(slot * 2 + 0) * kThreads + threadIdx.x] : 0.f;
+    const float rs = active ? rstat[(slot * 2 + 1) * kThreads + threadIdx.x] : 0.f;
     uint4 rx[NV], rd[NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int c = (gt + TPR * j) * 8;
       rx[j] = rd[j] = make_uint4(0, 0, 0, 0);
       if (active && c < D) {
-        rx[j] = *reinterpret_cast<const uint4*>(x + row * D + c);
-        rd[j] = *reinterpret_cast<const uint4*>(dy + row * D + c);
+        rx[j] = ring[(slot * 2 * NV + j) * kThreads + threadIdx.x];
+        rd[j] = ring[(slot * 2 * NV + NV + j) * kThreads + threadIdx.x];
       }
     }
+    slot = slot + 1 == RING ? 0 : slot + 1;
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
@@ -235,6 +300,7 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     }
   }
 
+  cp_async_wait<0>();
   // block reduction of the column partials: the row groups add their partials
   // into shared memory one group at a time (plain 16-byte accesses, no bank
   // conflicts), then one atomic per column per block
@@ -285,7 +351,7 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
                              const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int D,
                              const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
                              float* ydbg) {
-  const size_t smem = (size_t)D * 2 * sizeof(uint16_t);
+  const size_t smem = (size_t)D * 2 * sizeof(uint16_t) + (size_t)fwd_ring(rsh.nv) * rsh.nv * kThreads * 16;
   const int64_t gpb = kThreads / rsh.tpr;
 #define LNF(TPR, NV)                                                                                    \
   do {                                                                                                  \
@@ -341,7 +407,8 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
   const RowShape rsh = row_shape(D, 3);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: D = %lld > 8192", (long long)D);
   const int64_t gpb = kThreads / rsh.tpr;
-  const size_t smem = 2 * D * sizeof(float) + D * sizeof(uint16_t);
+  const size_t smem = 2 * D * sizeof(float) + D * sizeof(uint16_t) +
+                      (size_t)bwd_ring(rsh.nv) * (2 * rsh.nv * 16 + 2 * 4) * kThreads;
   LaunchScope ls("ln_bwd", st);
 #define LNB(TPR, NV)                                                                                   \
   do {                                                                                                 \
