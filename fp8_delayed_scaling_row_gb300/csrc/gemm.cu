@@ -110,7 +110,21 @@ struct KParams {
   int splits, kb_per_split;
   float* ws;
   unsigned* flags;
+  int group_m;  // M pairs per raster group (see tile_mn)
 };
+
+// Output tile t of a [num_m2 x num_n] grid of CTA-pair tiles in grouped raster
+// order: M pairs fastest within a group of G pairs, then N, then the next
+// group. The clusters in flight at any time then touch about G panels of A
+// and ncl / G panels of B, so a G chosen to keep G A-panels in L2 reads A from
+// DRAM once and B num_m2 / G times (G = num_m2 is plain M-fastest order).
+__device__ __forceinline__ int2 tile_mn(int t, int num_m2, int num_n, int G) {
+  const int span = G * num_n;
+  const int grp = t / span, r = t - grp * span;
+  const int m0 = grp * G;
+  const int gs = min(G, num_m2 - m0);
+  return make_int2(m0 + r % gs, r / gs);
+}
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -430,9 +444,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const int num_m2 = (p.num_m + CL - 1) / CL;
   const int S = p.splits;
   const int num_units = num_m2 * p.num_n * S;
-  // unit u: tile u / S (M pair fastest), K piece u % S
-  auto unit_m = [&](int u) { return ((u / S) % num_m2) * CL + rank; };
-  auto unit_n = [&](int u) { return (u / S) / num_m2; };
+  // unit u: tile u / S (grouped raster order), K piece u % S
+  auto unit_m = [&](int u) { return tile_mn(u / S, num_m2, p.num_n, p.group_m).x * CL + rank; };
+  auto unit_n = [&](int u) { return tile_mn(u / S, num_m2, p.num_n, p.group_m).y; };
   auto unit_kb0 = [&](int u) { return (u % S) * p.kb_per_split; };
   auto unit_kb1 = [&](int u) { return min(p.num_kb, (u % S + 1) * p.kb_per_split); };
   constexpr uint16_t kPair = (1u << CL) - 1u;
@@ -1011,6 +1025,15 @@ lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st) {
 // Splitting is considered for the bf16-store epilogue with a workspace only,
 // when all units fit in one round (the exchange then overlaps no other
 // tile's work, so it is paid once), and taken when it saves more than a tenth.
+// M pairs per raster group (tile_mn): as many A panels (tile rows x K codes) as
+// fit in 48 MB of the L2 cache; the rest holds the B panels in flight and the
+// outputs. Small problems get one group, which is plain M-fastest order.
+int raster_group(int64_t num_m2, int64_t panel_bytes) {
+  constexpr int64_t kBudget = 48ll << 20;
+  const int64_t g = panel_bytes > 0 ? kBudget / panel_bytes : num_m2;
+  return (int)max64(1, min64(g, max64(num_m2, 1)));
+}
+
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split, bool kmajor) {
   GemmPlan pl;
   const int64_t num_m = (M + BM - 1) / BM;
@@ -1085,6 +1108,7 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.num_m = (int)num_m;
   kp.num_n = (int)num_n;
   kp.num_kb = (int)((g.K + BK - 1) / BK);
+  kp.group_m = raster_group((num_m + (bn >= 192 ? 1 : 0)) / (bn >= 192 ? 2 : 1), (bn >= 192 ? 256 : 128) * g.K);
   // 256-wide tiles run the 2-SM MMA (M = 256 over the CTA pair, N = 256);
   // 128-wide tiles the 1-SM MMA (M = 128; N = 128 per instruction for MN-major B)
   kp.idesc = bn >= 192 ? make_idesc(256, bn, g.a_dtype, g.b_dtype, a_mn, b_mn)
@@ -1186,6 +1210,7 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
     pr.num_n = (int)((g.N + 255) / 256);
     pr.num_kb = (int)((g.K + BK - 1) / BK);
     pr.units = pr.num_m2 * pr.num_n * splits;
+    pr.group_m = fwd ? pr.num_m2 : raster_group(pr.num_m2, 256 * g.K);  // the forward keeps its N-fastest order
     pr.idesc = make_idesc(256, 256, g.a_dtype, g.b_dtype, a_mn, b_mn);
     pr.sinv_a = g.sinv_a;
     pr.sinv_b = g.sinv_b;

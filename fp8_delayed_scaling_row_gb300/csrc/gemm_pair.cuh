@@ -45,6 +45,7 @@ struct PairCfg {
 
 struct PairProb {
   int M, N, num_m2, num_n, num_kb, units;
+  int group_m;  // M pairs per raster group (tile_mn); the forward (DEP) order is N fastest
   uint32_t idesc;
   const float* sinv_a;
   const float* sinv_b;
@@ -206,10 +207,18 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
   sc.init(p, cid, ncl);
   // tile coordinates: primary unit u = tile; secondary unit v = tile * splits1 + piece
   constexpr bool DEP = PEPI == EPI_GELU;  // forward: FC2 depends on this launch's FC1 output
-  auto p_m = [&](int u) { return (DEP ? u / p.p0.num_n : u % p.p0.num_m2) * CL + rank; };
-  auto p_n = [&](int u) { return DEP ? u % p.p0.num_n : u / p.p0.num_m2; };
-  auto s_m = [&](int v) { return (DEP ? (v / p.splits1) / p.p1.num_n : (v / p.splits1) % p.p1.num_m2) * CL + rank; };
-  auto s_n = [&](int v) { return DEP ? (v / p.splits1) % p.p1.num_n : (v / p.splits1) / p.p1.num_m2; };
+  auto p_m = [&](int u) {
+    return (DEP ? u / p.p0.num_n : tile_mn(u, p.p0.num_m2, p.p0.num_n, p.p0.group_m).x) * CL + rank;
+  };
+  auto p_n = [&](int u) { return DEP ? u % p.p0.num_n : tile_mn(u, p.p0.num_m2, p.p0.num_n, p.p0.group_m).y; };
+  auto s_m = [&](int v) {
+    const int t = v / p.splits1;
+    return (DEP ? t / p.p1.num_n : tile_mn(t, p.p1.num_m2, p.p1.num_n, p.p1.group_m).x) * CL + rank;
+  };
+  auto s_n = [&](int v) {
+    const int t = v / p.splits1;
+    return DEP ? t % p.p1.num_n : tile_mn(t, p.p1.num_m2, p.p1.num_n, p.p1.group_m).y;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
