@@ -84,3 +84,93 @@ def test_single_process_is_a_no_op():
     assert torch.equal(t.view(torch.int32), before.view(torch.int32))
     with pytest.raises(TypeError):
         dp.allreduce_amax_(torch.zeros(3, dtype=torch.float64))
+
+
+# ---- the LayerNormMLP step itself, rows split over two ranks
+MLP_M, MLP_D, MLP_F, MLP_STEPS = 48, 32, 64, 4
+
+
+def _mlp_inputs(step):
+    from fp8_delayed_scaling_row_gb300 import synth
+    x = synth.activations(2 * MLP_M, MLP_D, dist="outliers", step=step)
+    dy = synth.grad(2 * MLP_M, MLP_D, step=step)
+    return x, dy
+
+
+def _mlp_step(x, dy, p, fs, bs, rec, exchange):
+    """One oracle LayerNormMLP forward + backward with the states' updates after
+    `exchange` (the data-parallel hook) has combined the recorded amaxes."""
+    from oracle import modules as omod
+    _, ctx, _ = omod.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], fs, rec, update=False)
+    g = omod.ln_mlp_bwd(dy, ctx, bs, rec, update=False)
+    exchange(fs, bs, g)
+    fs.update([rec.fwd_fmt()] * 4)
+    bs.update([rec.bwd_fmt()] * 2)
+    return g
+
+
+def _mlp_worker(rank, world, port, out):
+    from fp8_delayed_scaling_row_gb300 import synth
+    from oracle.delayed_scaling import Recipe
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rec = Recipe("hybrid", 3)
+    p = synth.mlp_params(MLP_D, MLP_F, bias_std=0.02)
+    fs, bs = ScalingState(4, 3), ScalingState(2, 3)
+
+    def exchange(fs, bs, g):
+        for st in (fs, bs):
+            cur = torch.from_numpy(st.amax_cur.copy())
+            dp.allreduce_amax_(cur)
+            st.amax_cur[:] = cur.numpy()
+        ts = [torch.from_numpy(np.ascontiguousarray(g[k], dtype=np.float64)) for k in ("dw1", "dw2", "dgamma", "dbeta")]
+        dp.allreduce_grads_(ts)
+        for k, t in zip(("dw1", "dw2", "dgamma", "dbeta"), ts):
+            g[k] = t.numpy()
+
+    grads = []
+    for step in range(MLP_STEPS):
+        x, dy = _mlp_inputs(step)
+        rows = slice(rank * MLP_M, (rank + 1) * MLP_M)
+        g = _mlp_step(x[rows], dy[rows], p, fs, bs, rec, exchange)
+        grads.append({k: g[k] for k in ("dw1", "dw2", "dgamma", "dbeta")})
+    out.put((rank, fs.copy(), bs.copy(), grads))
+    dist.destroy_process_group()
+
+
+def test_two_ranks_of_a_layernorm_mlp_keep_one_process_state():
+    """Each rank runs the oracle LayerNormMLP on half of the rows. Every amax of
+    the step is a maximum over rows, so with the MAX exchange each rank's forward
+    and backward states equal, bit for bit, those of one process over all rows;
+    the summed weight and LayerNorm gradients equal that process's gradients up
+    to the bf16 rounding of each half (1e-2 relative Frobenius, the parity bound)."""
+    from fp8_delayed_scaling_row_gb300 import synth
+    from oracle.delayed_scaling import Recipe
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_mlp_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=300) for _ in procs), key=lambda r: r[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    rec = Recipe("hybrid", 3)
+    p = synth.mlp_params(MLP_D, MLP_F, bias_std=0.02)
+    fs, bs = ScalingState(4, 3), ScalingState(2, 3)
+    ref = []
+    for step in range(MLP_STEPS):
+        x, dy = _mlp_inputs(step)
+        g = _mlp_step(x, dy, p, fs, bs, rec, lambda *a: None)
+        ref.append(g)
+    assert (fs.scale != 1).all() and (bs.scale != 1).all()  # the scales moved
+    for rank, rfs, rbs, grads in res:
+        for a, b in ((rfs, fs), (rbs, bs)):
+            for name in ("scale", "scale_inv", "amax_history"):
+                assert np.array_equal(getattr(a, name).view(np.uint32), getattr(b, name).view(np.uint32)), (rank, name)
+        for step in range(MLP_STEPS):
+            for k in ("dw1", "dw2", "dgamma", "dbeta"):
+                got, want = grads[step][k], np.asarray(ref[step][k], np.float64)
+                assert np.linalg.norm(got - want) <= 1e-2 * np.linalg.norm(want), (rank, step, k)
