@@ -52,6 +52,49 @@ __device__ __forceinline__ void unpack8(uint4 u, float* v) {
   }
 }
 
+// Packed fp32 pairs: two values in one 64-bit register, for the f32x2 add,
+// sub, mul and fma of the sm_100-family cores (one instruction per pair).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// bf16 pair (low, high halves of a 32-bit word) -> fp32 pair
+__device__ __forceinline__ uint64_t bf2(uint32_t w) {
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// max(m, |y|) with NaN winning (the amax order: NaN > Inf > finite)
+__device__ __forceinline__ float absmax_nan(float m, float y) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(y)));
+  return r;
+}
+
 // Sum over the TPR threads of a row group. `xch` holds kThreads/32 floats.
 template <int TPR>
 __device__ __forceinline__ float group_sum(float v, float* xch) {
@@ -82,7 +125,9 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   constexpr int P = RING - 2;  // rows in flight ahead of the one being normalised
   __shared__ float xch[kThreads / 32];
   __shared__ uint32_t ared[kThreads / 32];
-  extern __shared__ uint4 sgb[];  // gamma then beta (D/8 16-byte vectors each), then the ring
+  // gamma then beta as bf16 (D/8 16-byte vectors each: a warp's loads of consecutive vectors
+  // are conflict-free), then the ring
+  extern __shared__ uint4 sgb[];
   constexpr int GPB = kThreads / TPR;  // row groups per block
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
@@ -98,7 +143,7 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   const float s = *scale_p;
   const float inv_d = 1.0f / (float)D;
   const int64_t stride = (int64_t)gridDim.x * GPB;
-  uint32_t am = 0;
+  float amf = 0.f;
 
   // one commit group per iteration (empty past the last row) keeps the group count regular
   auto issue = [&](int64_t r, int slot) {
@@ -120,55 +165,64 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   for (; row - g < M; row += stride) {
     issue(row + P * stride, slot + P < RING ? slot + P : slot + P - RING);
     cp_async_wait<P>();  // this iteration's group has landed
-    uint4 raw[NV];
+    // each chunk of 8 values unpacked once into four fp32 pairs
+    uint64_t v2[NV][4];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int c = (gt + TPR * j) * 8;
-      raw[j] = (row < M && c < D) ? ring[(slot * NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+      const uint4 u = (row < M && c < D) ? ring[(slot * NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+      v2[j][0] = bf2(u.x);
+      v2[j][1] = bf2(u.y);
+      v2[j][2] = bf2(u.z);
+      v2[j][3] = bf2(u.w);
     }
     slot = slot + 1 == RING ? 0 : slot + 1;
     const bool active = row < M;
-    float sum = 0.f;
+    uint64_t s2 = 0;  // (0.f, 0.f)
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s2 = add2(s2, v2[j][q]);
+    const float2 sp = up2(s2);
+    const float mu = group_sum<TPR>(sp.x + sp.y, xch) * inv_d;
+    const uint64_t mu2 = pk2(mu, mu);
+    uint64_t q2 = 0;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      float v[8];
-      unpack8(raw[j], v);
+      if ((gt + TPR * j) * 8 < D) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sum += v[i];
-    }
-    const float mu = group_sum<TPR>(sum, xch) * inv_d;
-    float sq = 0.f;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int c = (gt + TPR * j) * 8;
-      if (c < D) {
-        float v[8];
-        unpack8(raw[j], v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float d = v[i] - mu;
-          sq += d * d;
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t d = sub2(v2[j][q], mu2);
+          q2 = fma2(d, d, q2);
         }
       }
     }
-    const float var = group_sum<TPR>(sq, xch) * inv_d;
+    const float2 qp = up2(q2);
+    const float var = group_sum<TPR>(qp.x + qp.y, xch) * inv_d;
     const float rs = 1.0f / sqrtf(var + eps);
     if (active) {
+      const uint64_t rs2 = pk2(rs, rs), sc2 = pk2(s, s);
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
-        const int cv = gt + TPR * j;
-        const int c = cv * 8;
+        const int c = (gt + TPR * j) * 8;
         if (c >= D) continue;
-        float v[8], gm[8], bt[8], y[8];
-        unpack8(raw[j], v);
-        unpack8(sgb[cv], gm);
-        unpack8(sgb[nvec + cv], bt);
+        const uint4 gu = sgb[gt + TPR * j], bu = sgb[nvec + gt + TPR * j];
+        const uint64_t gq[4] = {bf2(gu.x), bf2(gu.y), bf2(gu.z), bf2(gu.w)};
+        const uint64_t bq[4] = {bf2(bu.x), bf2(bu.y), bf2(bu.z), bf2(bu.w)};
+        float y[8];
+        uint32_t c16[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          y[i] = fmaf((v[i] - mu) * rs, gm[i], bt[i]);
-          am = max(am, abs_bits(y[i]));
+        for (int q = 0; q < 4; ++q) {
+          // y = (x - mu) * rsigma * gamma + beta, the same rounded steps as one value at a time
+          const uint64_t y2 = fma2(mul2(sub2(v2[j][q], mu2), rs2), gq[q], bq[q]);
+          const float2 yv = up2(y2);
+          y[2 * q] = yv.x;
+          y[2 * q + 1] = yv.y;
+          amf = absmax_nan(absmax_nan(amf, yv.x), yv.y);
+          const float2 z = up2(mul2(y2, sc2));
+          c16[q] = cvt_fp8x2<DT>(z.x, z.y);
         }
-        *reinterpret_cast<uint2*>(out + row * D + c) = cvt_fp8x8<DT>(y, s);
+        *reinterpret_cast<uint2*>(out + row * D + c) = make_uint2(c16[0] | (c16[1] << 16), c16[2] | (c16[3] << 16));
         if (ydbg) {
           float4* d4 = reinterpret_cast<float4*>(ydbg + row * D + c);
           d4[0] = make_float4(y[0], y[1], y[2], y[3]);
@@ -182,7 +236,7 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
     }
   }
   cp_async_wait<0>();
-  block_amax_commit(am, ared, amax_cur);
+  block_amax_commit(__float_as_uint(amf) & 0x7FFFFFFFu, ared, amax_cur);
 }
 
 template <int TPR, int NV>
@@ -194,7 +248,7 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
   constexpr int RING = bwd_ring(NV);
   constexpr int P = RING - 2;  // rows in flight ahead of the one being processed
   __shared__ float xch[kThreads / 32];
-  // [2][D] block partials of dgamma, dbeta; gamma [D/8 uint4]; the ring of x and dY chunks
+  // [2][D] block partials of dgamma, dbeta; gamma [D/8 uint4] bf16; the ring of x and dY chunks
   // [RING][2 NV][kThreads] uint4; then the ring of mu, rsigma [RING][2][kThreads] fp32
   extern __shared__ float colred[];
   uint4* sg = reinterpret_cast<uint4*>(colred + 2 * D);
@@ -229,11 +283,12 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     cp_async_commit();
   };
 
-  float accg[NV][8], accb[NV][8];
+  // dgamma, dbeta partials of this thread's columns as fp32 pairs
+  uint64_t accg[NV][4], accb[NV][4];
 #pragma unroll
   for (int j = 0; j < NV; ++j)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) accg[j][i] = accb[j][i] = 0.f;
+    for (int q = 0; q < 4; ++q) accg[j][q] = accb[j][q] = 0;
 
   int64_t row = (int64_t)blockIdx.x * GPB + g;
 #pragma unroll
@@ -245,58 +300,48 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     const bool active = row < M;
     const float mu = active ? rstat[(slot * 2 + 0) * kThreads + threadIdx.x] : 0.f;
     const float rs = active ? rstat[(slot * 2 + 1) * kThreads + threadIdx.x] : 0.f;
-    uint4 rx[NV], rd[NV];
+    const uint64_t mu2 = pk2(mu, mu), rs2 = pk2(rs, rs);
+    // xhat = (x - mu) * rsigma and g = dy * gamma, kept for the second pass
+    uint64_t xh[NV][4], gg[NV][4];
+    uint64_t s1 = 0, s2 = 0;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int c = (gt + TPR * j) * 8;
-      rx[j] = rd[j] = make_uint4(0, 0, 0, 0);
-      if (active && c < D) {
-        rx[j] = ring[(slot * 2 * NV + j) * kThreads + threadIdx.x];
-        rd[j] = ring[(slot * 2 * NV + NV + j) * kThreads + threadIdx.x];
+      const bool ok = active && c < D;
+      const uint4 ux = ok ? ring[(slot * 2 * NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+      const uint4 ud = ok ? ring[(slot * 2 * NV + NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+      const uint4 ug = c < D ? sg[gt + TPR * j] : make_uint4(0, 0, 0, 0);
+      const uint32_t wx[4] = {ux.x, ux.y, ux.z, ux.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
+      const uint64_t gq[4] = {bf2(ug.x), bf2(ug.y), bf2(ug.z), bf2(ug.w)};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t xv = bf2(wx[q]), dv = bf2(wd[q]);
+        xh[j][q] = mul2(sub2(xv, mu2), rs2);
+        gg[j][q] = mul2(dv, gq[q]);
+        s1 = add2(s1, gg[j][q]);
+        s2 = fma2(gg[j][q], xh[j][q], s2);
+        accg[j][q] = fma2(dv, xh[j][q], accg[j][q]);
+        accb[j][q] = add2(accb[j][q], dv);
       }
     }
     slot = slot + 1 == RING ? 0 : slot + 1;
-    float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int cv = gt + TPR * j;
-      float xv[8], dv[8], gm[8];
-      unpack8(rx[j], xv);
-      unpack8(rd[j], dv);
-      unpack8(cv < nvec ? sg[cv] : make_uint4(0, 0, 0, 0), gm);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float xh = (xv[i] - mu) * rs;
-        const float gg = dv[i] * gm[i];
-        s1 += gg;
-        s2 += gg * xh;
-        accg[j][i] = fmaf(dv[i], xh, accg[j][i]);
-        accb[j][i] += dv[i];
-      }
-    }
-    const float mean_g = group_sum<TPR>(s1, xch) * inv_d;
-    const float mean_gx = group_sum<TPR>(s2, xch) * inv_d;
+    const float2 s1p = up2(s1), s2p = up2(s2);
+    const float mean_g = group_sum<TPR>(s1p.x + s1p.y, xch) * inv_d;
+    const float mean_gx = group_sum<TPR>(s2p.x + s2p.y, xch) * inv_d;
     if (!active) continue;
+    const uint64_t mg2 = pk2(mean_g, mean_g), nmgx2 = pk2(-mean_gx, -mean_gx);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int cv = gt + TPR * j;
-      const int c = cv * 8;
+      const int c = (gt + TPR * j) * 8;
       if (c >= D) continue;
-      float xv[8], dv[8], gm[8], o[8];
-      unpack8(rx[j], xv);
-      unpack8(rd[j], dv);
-      unpack8(sg[cv], gm);
+      uint32_t w[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float xh = (xv[i] - mu) * rs;
-        o[i] = rs * (dv[i] * gm[i] - mean_g - xh * mean_gx);
+      for (int q = 0; q < 4; ++q) {
+        // dx = rsigma * (g - mean(g) - xhat * mean(g * xhat))
+        const float2 o = up2(mul2(fma2(xh[j][q], nmgx2, sub2(gg[j][q], mg2)), rs2));
+        w[q] = pack_bf16x2(o.x, o.y);
       }
-      uint4 pk;
-      pk.x = pack_bf16x2(o[0], o[1]);
-      pk.y = pack_bf16x2(o[2], o[3]);
-      pk.z = pack_bf16x2(o[4], o[5]);
-      pk.w = pack_bf16x2(o[6], o[7]);
-      *reinterpret_cast<uint4*>(dx + row * D + c) = pk;
+      *reinterpret_cast<uint4*>(dx + row * D + c) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 
@@ -314,10 +359,12 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
       float4* pg = reinterpret_cast<float4*>(colred + c);
       float4* pb = reinterpret_cast<float4*>(colred + D + c);
       const float4 g0 = pg[0], g1 = pg[1], b0 = pb[0], b1 = pb[1];
-      pg[0] = make_float4(g0.x + accg[j][0], g0.y + accg[j][1], g0.z + accg[j][2], g0.w + accg[j][3]);
-      pg[1] = make_float4(g1.x + accg[j][4], g1.y + accg[j][5], g1.z + accg[j][6], g1.w + accg[j][7]);
-      pb[0] = make_float4(b0.x + accb[j][0], b0.y + accb[j][1], b0.z + accb[j][2], b0.w + accb[j][3]);
-      pb[1] = make_float4(b1.x + accb[j][4], b1.y + accb[j][5], b1.z + accb[j][6], b1.w + accb[j][7]);
+      const float2 a0 = up2(accg[j][0]), a1 = up2(accg[j][1]), a2 = up2(accg[j][2]), a3 = up2(accg[j][3]);
+      const float2 e0 = up2(accb[j][0]), e1 = up2(accb[j][1]), e2 = up2(accb[j][2]), e3 = up2(accb[j][3]);
+      pg[0] = make_float4(g0.x + a0.x, g0.y + a0.y, g0.z + a1.x, g0.w + a1.y);
+      pg[1] = make_float4(g1.x + a2.x, g1.y + a2.y, g1.z + a3.x, g1.w + a3.y);
+      pb[0] = make_float4(b0.x + e0.x, b0.y + e0.y, b0.z + e1.x, b0.w + e1.y);
+      pb[1] = make_float4(b1.x + e2.x, b1.y + e2.y, b1.z + e3.x, b1.w + e3.y);
     }
   }
   __syncthreads();
