@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -77,7 +78,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int, tag: str = ""):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}{tag}.csv")
+        # raw samples; LNFP8_CLOCKS_DIR keeps them somewhere lasting (the JSON line has the summary)
+        self.path = os.path.join(os.environ.get("LNFP8_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"lnfp8_clocks_rank{gpu_index}{tag}.csv")
         self.t0 = self.t1 = None
 
     def start(self):
