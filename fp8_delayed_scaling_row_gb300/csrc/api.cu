@@ -253,7 +253,7 @@ extern "C" {
 
 const char* lnfp8_last_error(void) { return g_msg; }
 
-int lnfp8_version(void) { return 200; }
+int lnfp8_version(void) { return 300; }
 
 long long lnfp8_launch_count(void) { return g_launches.load(); }
 
@@ -553,6 +553,11 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
     if (a->K > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: K > 8192 with LayerNorm", who);
   }
   const bool w8 = a->w_scale_inv != nullptr;  // weight stored as FP8 codes
+  OPT(a->residual, who);
+  if (a->residual) {
+    if (!ln) return set_error(LNFP8_ERR_INVALID_ARG, "%s: residual needs the LayerNorm (gamma)", who);
+    if (a->M > 0) REQ(a->x_sum, who);
+  }
   if (!w8) REQ(a->w, who);
   REQ(a->wq, who);
   OPT(a->bias, who);
@@ -572,7 +577,7 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
   if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
   if (ln)
     TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,
-                      a->rsigma, a->ln_out_debug, st));
+                      a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum));
   else
     TRY(cast_launch(a->x, false, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, nullptr, nullptr, st));
   GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, m.scale_inv + 0,
@@ -656,6 +661,8 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   TRY(check_recipe(&a->recipe, &a->meta, who));
   REQ(a->gamma, who);
   REQ(a->beta, who);
+  OPT(a->residual, who);
+  if (a->residual && a->M > 0) REQ(a->x_sum, who);
   const bool w8 = a->w1_scale_inv != nullptr;  // weights stored as FP8 codes
   if (w8 != (a->w2_scale_inv != nullptr))
     return set_error(LNFP8_ERR_INVALID_ARG, "%s: w1_scale_inv and w2_scale_inv must be given together", who);
@@ -691,7 +698,7 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   else if (fused)
     TRY(zero_launch({{a->gemm_ws, ready_bytes}}, st));
   TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
-                    a->rsigma, a->ln_out_debug, st));
+                    a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum));
   GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0,
                           w8 ? a->w1_scale_inv : m.scale_inv + 1);
   f1.epi = EPI_GELU;

@@ -35,7 +35,8 @@ lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, con
 
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
-                           uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st);
+                           uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st,
+                           const uint16_t* resid = nullptr, uint16_t* hsum = nullptr);
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
                            float* dbeta, cudaStream_t st, bool clear = true);

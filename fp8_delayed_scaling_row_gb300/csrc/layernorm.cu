@@ -115,13 +115,18 @@ __device__ __forceinline__ float group_sum(float v, float* xch) {
   }
 }
 
-template <int TPR, int NV, int DT>
+// RES: the row is h = bf16(x + resid) (a residual add fused ahead of the
+// LayerNorm); h is written to hsum (the new residual stream, which the backward
+// reads as its x) and normalised.
+template <int TPR, int NV, int DT, bool RES>
 __global__ void __launch_bounds__(kThreads)
 ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
               const uint16_t* __restrict__ beta, float eps, int64_t M, int D,
               const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
-              float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg) {
-  constexpr int RING = fwd_ring(NV);
+              float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg,
+              const uint16_t* __restrict__ resid, uint16_t* __restrict__ hsum) {
+  constexpr int NVR = RES ? 2 * NV : NV;  // 16-byte chunks per row and thread in the ring
+  constexpr int RING = fwd_ring(NVR);
   constexpr int P = RING - 2;  // rows in flight ahead of the one being normalised
   __shared__ float xch[kThreads / 32];
   __shared__ uint32_t ared[kThreads / 32];
@@ -132,7 +137,7 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   const int g = threadIdx.x / TPR;
   const int gt = threadIdx.x % TPR;
   const int nvec = D >> 3;
-  uint4* ring = sgb + 2 * nvec;  // [RING][NV][kThreads]
+  uint4* ring = sgb + 2 * nvec;  // [RING][NVR][kThreads]: x chunks, then (RES) residual chunks
   pdl_wait();
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < nvec; i += kThreads) {
@@ -151,7 +156,10 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int c = (gt + TPR * j) * 8;
-        if (c < D) cp_async16(&ring[(slot * NV + j) * kThreads + threadIdx.x], x + r * D + c);
+        if (c < D) {
+          cp_async16(&ring[(slot * NVR + j) * kThreads + threadIdx.x], x + r * D + c);
+          if (RES) cp_async16(&ring[(slot * NVR + NV + j) * kThreads + threadIdx.x], resid + r * D + c);
+        }
       }
     }
     cp_async_commit();
@@ -170,7 +178,20 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int c = (gt + TPR * j) * 8;
-      const uint4 u = (row < M && c < D) ? ring[(slot * NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+      const bool ok = row < M && c < D;
+      uint4 u = ok ? ring[(slot * NVR + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+      if (RES) {
+        const uint4 ur = ok ? ring[(slot * NVR + NV + j) * kThreads + threadIdx.x] : make_uint4(0, 0, 0, 0);
+        const uint32_t wx[4] = {u.x, u.y, u.z, u.w}, wr[4] = {ur.x, ur.y, ur.z, ur.w};
+        uint32_t wh[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 hv = up2(add2(bf2(wx[q]), bf2(wr[q])));
+          wh[q] = pack_bf16x2(hv.x, hv.y);
+        }
+        u = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        if (ok) *reinterpret_cast<uint4*>(hsum + row * D + c) = u;
+      }
       v2[j][0] = bf2(u.x);
       v2[j][1] = bf2(u.y);
       v2[j][2] = bf2(u.z);
@@ -393,19 +414,20 @@ int64_t resident_blocks(K kernel, size_t smem) {
   return (int64_t)n * num_sms();
 }
 
-template <int DT>
+template <int DT, bool RES>
 lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
                              const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int D,
                              const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
-                             float* ydbg) {
-  const size_t smem = (size_t)D * 2 * sizeof(uint16_t) + (size_t)fwd_ring(rsh.nv) * rsh.nv * kThreads * 16;
+                             float* ydbg, const uint16_t* resid, uint16_t* hsum) {
+  const int nvr = RES ? 2 * rsh.nv : rsh.nv;
+  const size_t smem = (size_t)D * 2 * sizeof(uint16_t) + (size_t)fwd_ring(nvr) * nvr * kThreads * 16;
   const int64_t gpb = kThreads / rsh.tpr;
 #define LNF(TPR, NV)                                                                                    \
   do {                                                                                                  \
-    auto k = ln_fwd_kernel<TPR, NV, DT>;                                                                \
+    auto k = ln_fwd_kernel<TPR, NV, DT, RES>;                                                           \
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                        \
-    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg) != cudaSuccess) \
+    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg, resid, hsum) != cudaSuccess) \
       return check_launch("ln_fwd_cast launch");                                                        \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
@@ -432,14 +454,22 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
 
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
-                           uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st) {
+                           uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st,
+                           const uint16_t* resid, uint16_t* hsum) {
   if (M == 0) return LNFP8_OK;
   const RowShape rsh = row_shape(D, 4);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: D = %lld > 8192", (long long)D);
   LaunchScope ls("ln_fwd_cast", st);
+  const bool res = resid != nullptr;
   if (dtype == LNFP8_E4M3)
-    return ln_fwd_dispatch<LNFP8_E4M3>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
-  return ln_fwd_dispatch<LNFP8_E5M2>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu, rsigma, ydbg);
+    return res ? ln_fwd_dispatch<LNFP8_E4M3, true>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
+                                                   rsigma, ydbg, resid, hsum)
+               : ln_fwd_dispatch<LNFP8_E4M3, false>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
+                                                    rsigma, ydbg, nullptr, nullptr);
+  return res ? ln_fwd_dispatch<LNFP8_E5M2, true>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
+                                                 rsigma, ydbg, resid, hsum)
+             : ln_fwd_dispatch<LNFP8_E5M2, false>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
+                                                  rsigma, ydbg, nullptr, nullptr);
 }
 
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,

@@ -60,7 +60,7 @@ class CLnLinearFwd(C.Structure):
     _fields_ = [("M", _I64), ("K", _I64), ("N", _I64), ("x", _P), ("gamma", _P), ("beta", _P), ("eps", C.c_float),
                 ("w", _P), ("bias", _P), ("y", _P), ("xq", _P), ("wq", _P), ("mu", _P), ("rsigma", _P),
                 ("sinv_saved", _P), ("meta", CMeta), ("recipe", CRecipe), ("defer_update", C.c_int),
-                ("ln_out_debug", _P), ("w_scale_inv", _P)]
+                ("ln_out_debug", _P), ("w_scale_inv", _P), ("residual", _P), ("x_sum", _P)]
 
 
 class CLnLinearBwd(C.Structure):
@@ -75,7 +75,8 @@ class CLnMlpFwd(C.Structure):
                 ("w1", _P), ("b1", _P), ("w2", _P), ("b2", _P), ("y", _P), ("lnq", _P), ("mu", _P), ("rsigma", _P),
                 ("w1q", _P), ("w2q", _P), ("h", _P), ("aq", _P), ("sinv_saved", _P), ("meta", CMeta),
                 ("recipe", CRecipe), ("defer_update", C.c_int), ("ln_out_debug", _P), ("act_debug", _P),
-                ("gemm_ws", _P), ("gemm_ws_bytes", _I64), ("w1_scale_inv", _P), ("w2_scale_inv", _P)]
+                ("gemm_ws", _P), ("gemm_ws_bytes", _I64), ("w1_scale_inv", _P), ("w2_scale_inv", _P),
+                ("residual", _P), ("x_sum", _P)]
 
 
 class CLnMlpBwd(C.Structure):
@@ -363,6 +364,7 @@ class LinearCtx:
     rsigma: torch.Tensor | None
     sinv_saved: torch.Tensor
     ln_out_debug: torch.Tensor | None = None
+    x_sum: torch.Tensor | None = None  # h = bf16(x + residual) of a forward with a residual (the backward's x)
 
 
 def _e(shape, dtype, dev):
@@ -379,9 +381,11 @@ def linear_ctx(M, K, N, *, ln=True, device="cuda", debug=False, weight_codes=Tru
 
 
 def ln_linear_fwd(x, gamma, beta, w, bias, meta: ScalingMeta, recipe: Recipe, *, eps=1e-5, y=None,
-                  ctx: LinearCtx | None = None, defer_update=False, debug=False, stream=None):
+                  ctx: LinearCtx | None = None, defer_update=False, debug=False, residual=None, stream=None):
     """LayerNormLinear (gamma given) or Linear (gamma None) forward; returns (y, ctx).
-    w is a bf16 weight (cast every call) or an FP8Weight (its codes are used as they are)."""
+    w is a bf16 weight (cast every call) or an FP8Weight (its codes are used as they are).
+    residual: optional bf16 [M, K]; the input becomes h = bf16(x + residual), returned as
+    ctx.x_sum (pass it as the backward's x)."""
     M, K = x.shape
     N = w.shape[0]
     dev = x.device
@@ -390,12 +394,15 @@ def ln_linear_fwd(x, gamma, beta, w, bias, meta: ScalingMeta, recipe: Recipe, *,
                                                  weight_codes=not w8)
     if w8:
         ctx.wq = w.codes
+    if residual is not None and ctx.x_sum is None:
+        ctx.x_sum = _e((M, K), torch.bfloat16, dev)
     y = y if y is not None else _e((M, N), torch.bfloat16, dev)
     a = CLnLinearFwd(M=M, K=K, N=N, x=_ptr(x), gamma=_ptr(gamma), beta=_ptr(beta), eps=eps,
                      w=None if w8 else _ptr(w), bias=_ptr(bias), y=_ptr(y), xq=_ptr(ctx.xq), wq=_ptr(ctx.wq),
                      mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma), sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(),
                      recipe=recipe.c(), defer_update=int(defer_update), ln_out_debug=_ptr(ctx.ln_out_debug),
-                     w_scale_inv=_ptr(w.scale_inv) if w8 else None)
+                     w_scale_inv=_ptr(w.scale_inv) if w8 else None, residual=_ptr(residual),
+                     x_sum=_ptr(ctx.x_sum) if residual is not None else None)
     _check(_c_lin_fwd(C.byref(a), _stream(stream)))
     return y, ctx
 
@@ -464,6 +471,7 @@ class MlpCtx:
     ln_out_debug: torch.Tensor | None = None
     act_debug: torch.Tensor | None = None
     gemm_ws: torch.Tensor | None = None  # FC1 tiles' readiness counters (FC1 and FC2 in one launch)
+    x_sum: torch.Tensor | None = None  # h = bf16(x + residual) of a forward with a residual (the backward's x)
 
 
 def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False, weight_codes=True) -> MlpCtx:
@@ -482,9 +490,10 @@ def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False, weight_codes=Tr
 
 
 def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, meta: ScalingMeta, recipe: Recipe, *, eps=1e-5, y=None,
-               ctx: MlpCtx | None = None, defer_update=False, debug=False, stream=None):
+               ctx: MlpCtx | None = None, defer_update=False, debug=False, residual=None, stream=None):
     """LayerNormMLP forward; returns (y, ctx). w1 and w2 are both bf16 weights (cast
-    every call) or both FP8Weight (their codes are used as they are)."""
+    every call) or both FP8Weight (their codes are used as they are). residual: optional
+    bf16 [M, D]; the input becomes h = bf16(x + residual), returned as ctx.x_sum."""
     M, D = x.shape
     F = w1.shape[0]
     dev = x.device
@@ -494,6 +503,8 @@ def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, meta: ScalingMeta, recipe: Recipe
     ctx = ctx if ctx is not None else mlp_ctx(M, D, F, device=dev, debug=debug, weight_codes=not w8)
     if w8:
         ctx.w1q, ctx.w2q = w1.codes, w2.codes
+    if residual is not None and ctx.x_sum is None:
+        ctx.x_sum = _e((M, D), torch.bfloat16, dev)
     y = y if y is not None else _e((M, D), torch.bfloat16, dev)
     a = CLnMlpFwd(M=M, D=D, F=F, x=_ptr(x), gamma=_ptr(gamma), beta=_ptr(beta), eps=eps,
                   w1=None if w8 else _ptr(w1), b1=_ptr(b1), w2=None if w8 else _ptr(w2), b2=_ptr(b2), y=_ptr(y),
@@ -502,7 +513,8 @@ def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, meta: ScalingMeta, recipe: Recipe
                   sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(), recipe=recipe.c(), defer_update=int(defer_update),
                   ln_out_debug=_ptr(ctx.ln_out_debug), act_debug=_ptr(ctx.act_debug), gemm_ws=_ptr(ctx.gemm_ws),
                   gemm_ws_bytes=ctx.gemm_ws.numel() if ctx.gemm_ws is not None else 0,
-                  w1_scale_inv=_ptr(w1.scale_inv) if w8 else None, w2_scale_inv=_ptr(w2.scale_inv) if w8 else None)
+                  w1_scale_inv=_ptr(w1.scale_inv) if w8 else None, w2_scale_inv=_ptr(w2.scale_inv) if w8 else None,
+                  residual=_ptr(residual), x_sum=_ptr(ctx.x_sum) if residual is not None else None)
     _check(_c_mlp_fwd(C.byref(a), _stream(stream)))
     return y, ctx
 

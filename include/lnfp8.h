@@ -275,6 +275,12 @@ typedef struct {
    * the forward casts no weight and records no weight amax, the GEMM uses
    * w_scale_inv[0] for the weight and sinv_saved[1] receives it. */
   const float* w_scale_inv;
+  /* Residual add fused ahead of the LayerNorm (requires gamma): NULL, or [M, K]
+   * bf16 r; then the module's input is h = bf16(x + r) (fp32 add, round to
+   * nearest even), which the call writes to x_sum ([M, K] bf16, required with
+   * residual) and normalises. The backward takes x_sum as its x. */
+  const uint16_t* residual;
+  uint16_t* x_sum;
 } lnfp8_ln_linear_fwd_args;
 
 typedef struct {
@@ -307,7 +313,10 @@ typedef struct {
  *   out = (xq . wq^T) * (scale_inv[0] * scale_inv[1]) + bias  (bf16);
  * then the forward state update unless defer_update. With w_scale_inv set
  * (weights stored in FP8, TE tutorial closing list: fp8_model_init), wq is the
- * given codes and w_scale_inv[0] takes the place of scale_inv[1]. */
+ * given codes and w_scale_inv[0] takes the place of scale_inv[1]. With
+ * residual set, x is first replaced by h = bf16(x + residual) (the residual
+ * connection ahead of the block's LayerNorm, TE tutorial code block 2), fused
+ * into the LayerNorm kernel and written to x_sum. */
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* args, lnfp8_stream stream);
 
 /* LayerNormLinear backward: dyq = fp8(dy * gscale[0]) (E5M2 under HYBRID);
@@ -381,6 +390,11 @@ typedef struct {
    * and sinv_saved[1], sinv_saved[3] receive these values. */
   const float* w1_scale_inv;
   const float* w2_scale_inv;
+  /* Residual add fused ahead of the LayerNorm: NULL, or [M, D] bf16 r; then the
+   * input is h = bf16(x + r), written to x_sum ([M, D] bf16, required with
+   * residual) and normalised; the backward takes x_sum as its x. */
+  const uint16_t* residual;
+  uint16_t* x_sum;
 } lnfp8_ln_mlp_fwd_args;
 
 typedef struct {
@@ -419,7 +433,9 @@ typedef struct {
  *   y = LN(x) -> lnq = fp8(y*scale[0]); w1q = fp8(W1*scale[1]); w2q = fp8(W2*scale[3]);
  *   h = bf16((lnq . w1q^T) * sinv[0]*sinv[1] + b1);
  *   a = gelu_tanh(h) (fp32); aq = fp8(a * scale[2]);
- *   out = bf16((aq . w2q^T) * sinv[2]*sinv[3] + b2); then the state update. */
+ *   out = bf16((aq . w2q^T) * sinv[2]*sinv[3] + b2); then the state update.
+ * With residual set, x is first replaced by h = bf16(x + residual) (fused into
+ * the LayerNorm kernel, written to x_sum), as in ln_linear_fwd. */
 lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* args, lnfp8_stream stream);
 
 /* Bytes of args->gemm_ws with which ln_mlp_fwd runs FC1 (+GELU) and FC2 as one

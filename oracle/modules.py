@@ -126,8 +126,15 @@ def quantize_weight(w, recipe: Recipe, state: ScalingState | None = None):
     return codes, np.float32(st.scale_inv[0]), st
 
 
+def _residual_sum(X, residual, nm):
+    """The residual connection ahead of a block's LayerNorm (TE tutorial code
+    block 2, the plain-PyTorch block: x = x + a; x + mlp(ln2(x))): the module's
+    input is the bf16 sum of the two bf16 tensors."""
+    return nm.bf16(X + _in(residual))
+
+
 def ln_linear_fwd(x, gamma, beta, w, b, state: ScalingState, recipe: Recipe, *,
-                  exact: bool = False, update: bool = True, fp8_weight=None):
+                  exact: bool = False, update: bool = True, fp8_weight=None, residual=None):
     """LayerNormLinear (gamma given) or Linear (gamma None) forward.
 
     fp8_weight: None, or (codes, scale_inv) of a weight kept in FP8 (see
@@ -141,6 +148,11 @@ def ln_linear_fwd(x, gamma, beta, w, b, state: ScalingState, recipe: Recipe, *,
         raise ValueError("exact=True has no FP8-stored weight")
     X = _in(x)
     aux = {}
+    if residual is not None:
+        if gamma is None:
+            raise ValueError("the residual add precedes a LayerNorm")
+        X = _residual_sum(X, residual, nm)
+        aux["x_sum"] = X
     if gamma is not None:
         y, mu, rs = _ln.forward(X, _in(gamma), _in(beta))
         if exact:
@@ -197,7 +209,8 @@ def ln_linear_bwd(dy, ctx: Ctx, gstate: ScalingState, recipe: Recipe, *,
 
 
 def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, state: ScalingState, recipe: Recipe, *,
-               exact: bool = False, update: bool = True, gelu_approx: str = "tanh", fp8_weights=None):
+               exact: bool = False, update: bool = True, gelu_approx: str = "tanh", fp8_weights=None,
+               residual=None):
     """LayerNormMLP forward. Returns (Y, ctx, aux); aux holds mu, rsigma, the
     fp32 pre-cast LN output y and GELU output a, and the bf16 H.
 
@@ -209,6 +222,8 @@ def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, state: ScalingState, recipe: Reci
     if fp8_weights is not None and exact:
         raise ValueError("exact=True has no FP8-stored weights")
     X = _in(x)
+    if residual is not None:
+        X = _residual_sum(X, residual, nm)
     G = _in(gamma)
     y, mu, rs = _ln.forward(X, G, _in(beta))
     if exact:
@@ -241,6 +256,8 @@ def ln_mlp_fwd(x, gamma, beta, w1, b1, w2, b2, state: ScalingState, recipe: Reci
         state.update([fmt] * 4, recipe.amax_compute_algo, recipe.margin)
     ctx = Ctx(x=X, gamma=G, yq=yq, wq=[w1q, w2q], sinv=sinv, h=H, aq=aq, fmt=fmt)
     aux = dict(mu=mu, rsigma=rs, y=y, a=a, h=H)
+    if residual is not None:
+        aux["x_sum"] = X
     return Y, ctx, aux
 
 

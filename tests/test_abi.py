@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.version() == 200
+    assert lib.version() == 300
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first

@@ -8,7 +8,9 @@ around a synthetic attention output (attention itself is not on the path):
     h   = h + LayerNormMLP(h)           768 -> 3072 -> 768
 
 and the backward in reverse with synthetic dQKV ~ N(0, 0.01) and the residual
-gradient flowing through. Every module call defers its state update; after the
+gradient flowing through. On the GPU side the residual adds in front of the
+MLP's and the next layer's LayerNorm run fused into those LayerNorm kernels
+(their x_sum must equal the oracle's residual stream bit for bit). Every module call defers its state update; after the
 step one ``amax_history_update_many`` launch updates all layers' forward and
 backward states. The oracle runs the whole stack on its own (its own residual
 stream and its own state machines); the GPU modules take the oracle stream's
@@ -68,6 +70,10 @@ def _to_bits(v):
     return to_bf16_bits(np.asarray(v, np.float64))
 
 
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
 def _close_state(meta, st, rtol):
     """GPU state against the oracle's own within rtol (amaxes of fp32 intermediates)."""
     for name in ("scale", "scale_inv", "amax_history"):
@@ -114,13 +120,20 @@ def test_block_stack_with_one_state_update_launch(L, layers, M, steps):
         # the residual stream is the oracle's: both sides get its values at every layer
         h = bf16_to_f32(synth.activations(M, D, dist="outliers", step=step)).astype(np.float64)
         saved = []
+        prev = None  # (residual stream before the last MLP add, that MLP's output) as bf16 bits
         for l in range(layers):
             p, d, m, o = P[l], dev[l], M_[l], O_[l]
             hb = _to_bits(h)
             attn = synth.activations(M, D, step=step, tid=synth.TID["attn"], layer=l)
-            xq = bf16_dev(hb)
-            qkv, cq = L.ln_linear_fwd(xq, d["qkv"]["gamma"], d["qkv"]["beta"], d["qkv"]["w"], d["qkv"]["b"], m["fq"], rec,
-                                      defer_update=True)
+            if prev is None:
+                xq = bf16_dev(hb)
+                qkv, cq = L.ln_linear_fwd(xq, d["qkv"]["gamma"], d["qkv"]["beta"], d["qkv"]["w"], d["qkv"]["b"],
+                                          m["fq"], rec, defer_update=True)
+            else:  # the previous MLP's residual add fused into this LayerNorm
+                qkv, cq = L.ln_linear_fwd(bf16_dev(prev[0]), d["qkv"]["gamma"], d["qkv"]["beta"], d["qkv"]["w"],
+                                          d["qkv"]["b"], m["fq"], rec, defer_update=True, residual=bf16_dev(prev[1]))
+                assert np.array_equal(_bits(cq.x_sum), hb), (step, l, "qkv residual")
+                xq = cq.x_sum
             oq_y, ocq, _ = omod.ln_linear_fwd(hb, p["qkv"]["gamma"], p["qkv"]["beta"], p["qkv"]["w"], p["qkv"]["b"],
                                               o["fq"], orec, update=False)
             assert rel_fro(host(qkv), oq_y) < TOL, (step, l, "qkv")
@@ -131,13 +144,17 @@ def test_block_stack_with_one_state_update_launch(L, layers, M, steps):
             assert rel_fro(host(pr), op_y) < TOL, (step, l, "proj")
             h = _bf16_add(h, op_y)
             hb2 = _to_bits(h)
-            xm = bf16_dev(hb2)
-            y, cm = L.ln_mlp_fwd(xm, d["mlp"]["gamma"], d["mlp"]["beta"], d["mlp"]["w1"], d["mlp"]["b1"], d["mlp"]["w2"],
-                                 d["mlp"]["b2"], m["fm"], rec, defer_update=True)
+            # the projection's residual add fused into the MLP's LayerNorm
+            y, cm = L.ln_mlp_fwd(bf16_dev(hb), d["mlp"]["gamma"], d["mlp"]["beta"], d["mlp"]["w1"], d["mlp"]["b1"],
+                                 d["mlp"]["w2"], d["mlp"]["b2"], m["fm"], rec, defer_update=True,
+                                 residual=bf16_dev(_to_bits(op_y)))
+            assert np.array_equal(_bits(cm.x_sum), hb2), (step, l, "mlp residual")
+            xm = cm.x_sum
             om_y, ocm, _ = omod.ln_mlp_fwd(hb2, p["mlp"]["gamma"], p["mlp"]["beta"], p["mlp"]["w1"], p["mlp"]["b1"],
                                            p["mlp"]["w2"], p["mlp"]["b2"], o["fm"], orec, update=False)
             assert rel_fro(host(y), om_y) < TOL, (step, l, "mlp")
             h = _bf16_add(h, om_y)
+            prev = (hb2, _to_bits(om_y))
             saved.append((xq, cq, ocq, xa, cp, ocp, xm, cm, ocm))
         dh = bf16_to_f32(synth.grad(M, D, step=step)).astype(np.float64)
         for l in reversed(range(layers)):

@@ -1,7 +1,8 @@
-"""Pins of the oracle's FP8-stored weights (fp8_model_init, TE tutorial closing
-list): the one-time conversion against what the FP8 formats fix, and the
-modules' FP8-weight branch against the bf16-weight branch and the exact fp64
-layer."""
+"""Pins of the oracle's module variants. FP8-stored weights (fp8_model_init, TE
+tutorial closing list): the one-time conversion against what the FP8 formats
+fix, and the modules' FP8-weight branch against the bf16-weight branch and the
+exact fp64 layer. The residual add ahead of a LayerNorm module: against torch's
+own bf16 addition, and a zero residual against no residual."""
 import numpy as np
 import pytest
 
@@ -108,3 +109,39 @@ def test_exact_mode_refuses_fp8_weight():
     with pytest.raises(ValueError):
         omod.ln_linear_fwd(np.zeros((2, 16)), None, None, None, None, ScalingState(2, 1), Recipe(), exact=True,
                            fp8_weight=(np.zeros((16, 16), np.uint8), np.float32(1)))
+
+
+# ---- the residual add ahead of a LayerNorm module
+def _bf16_bits_sum_torch(a_bits, b_bits):
+    """bf16 + bf16 -> bf16 by torch's own bf16 addition (an independent rounding)."""
+    import torch
+    ta = torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(b_bits.view(np.int16)).view(torch.bfloat16)
+    return (ta + tb).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_residual_sum_matches_torch_bf16_addition_and_zero_is_identity():
+    M, D, F = 24, 32, 64
+    p = synth.mlp_params(D, F, layer=4, bias_std=0.02)
+    x = synth.activations(M, D, dist="outliers", step=3)
+    r = synth.activations(M, D, step=5, tid=synth.TID["attn"])
+    rec = Recipe("hybrid", 4)
+    h = _bf16_bits_sum_torch(x, r)
+    y1, c1, a1 = omod.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], ScalingState(4, 4), rec,
+                                 update=False, residual=r)
+    y2, c2, _ = omod.ln_mlp_fwd(h, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], ScalingState(4, 4), rec,
+                                update=False)
+    assert np.array_equal(a1["x_sum"], bf16_to_f32(h)) and np.array_equal(y1, y2) and np.array_equal(c1.x, c2.x)
+    z = np.zeros_like(x)
+    y3, _, _ = omod.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], ScalingState(4, 4), rec,
+                               update=False, residual=z)
+    y4, _, _ = omod.ln_mlp_fwd(x, p["gamma"], p["beta"], p["w1"], p["b1"], p["w2"], p["b2"], ScalingState(4, 4), rec,
+                               update=False)
+    assert np.array_equal(y3, y4)
+    pl = synth.linear_params(48, D, layer=2, bias_std=0.02)
+    ly1, _, la = omod.ln_linear_fwd(x, pl["gamma"], pl["beta"], pl["w"], pl["b"], ScalingState(2, 4), rec, update=False,
+                                    residual=r)
+    ly2, _, _ = omod.ln_linear_fwd(h, pl["gamma"], pl["beta"], pl["w"], pl["b"], ScalingState(2, 4), rec, update=False)
+    assert np.array_equal(ly1, ly2) and np.array_equal(la["x_sum"], bf16_to_f32(h))
+    with pytest.raises(ValueError):  # a residual needs the LayerNorm it precedes
+        omod.ln_linear_fwd(x, None, None, pl["w"], pl["b"], ScalingState(2, 4), rec, residual=r)
