@@ -328,11 +328,13 @@ class StackRun:
     layers then backward in reverse, every module with its state update deferred
     and one state-update launch for all layers' sets at the end of the step.
 
-    Each layer's inputs (h ~ N(0,1) with 0.1% x50 outliers, attention output ~
-    N(0,1), dQKV and dY ~ N(0, 0.01)) are device-resident, generated once; the
-    layers are not chained through residual adds (attention and residuals are
-    not part of this path), so the step's work is exactly the modules'. The whole
-    step is one captured CUDA graph."""
+    The forward is chained as a pre-LN block: the MLP's LayerNorm takes the
+    residual stream plus the projection's output, the next layer's QKV LayerNorm
+    the stream plus the MLP's output, both adds fused into those LayerNorm
+    kernels. Device-resident inputs, generated once: the first layer's h ~ N(0,1)
+    with 0.1% x50 outliers, each layer's attention output ~ N(0,1), dQKV and dY
+    ~ N(0, 0.01) (the backward is not chained: attention is not on this path).
+    The whole step is one captured CUDA graph."""
 
     def __init__(self, L, torch, dev, layers, m, d, f, fmt, hist, seed):
         self.L, self.torch, self.layers, self.m, self.d, self.f = L, torch, layers, m, d, f
@@ -359,8 +361,7 @@ class StackRun:
                 g2=ones_plus(d), be2=randn(d, std=0.1),
                 w1=randn(f, d, std=0.02), b1=torch.zeros(f, dtype=torch.bfloat16, device=dev),
                 w2=randn(d, f, std=0.02), b2=torch.zeros(d, dtype=torch.bfloat16, device=dev),
-                h=randn(m, d, outliers=True), attn=randn(m, d), dqkv=randn(m, 3 * d, std=0.01),
-                dy=randn(m, d, std=0.01),
+                attn=randn(m, d), dqkv=randn(m, 3 * d, std=0.01), dy=randn(m, d, std=0.01),
                 fq=L.ScalingMeta(2, hist, device=dev), fp=L.ScalingMeta(2, hist, device=dev),
                 fm=L.ScalingMeta(4, hist, device=dev), bq=L.ScalingMeta(1, hist, device=dev),
                 bp=L.ScalingMeta(1, hist, device=dev), bm=L.ScalingMeta(2, hist, device=dev),
@@ -369,9 +370,12 @@ class StackRun:
                 gq=L.linear_grads(m, d, 3 * d, device=dev), gp=L.linear_grads(m, d, d, ln=False, device=dev),
                 gm=L.mlp_grads(m, d, f, device=dev))
             self.layer.append(lay)
-        # module outputs the stack does not consume share one buffer per shape
+        self.h0 = randn(m, d, outliers=True)
+        # the QKV output is not consumed (attention is synthetic); projection and MLP outputs
+        # feed the next LayerNorm's fused residual add
         self.yq = torch.empty(m, 3 * d, dtype=torch.bfloat16, device=dev)
-        self.yd = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
+        self.yp = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
+        self.ym = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
         self.order = ["fq", "fp", "fm", "bq", "bp", "bm"]
         dts = {"fq": [E4] * 2, "fp": [E4] * 2, "fm": [E4] * 4, "bq": [E5], "bp": [E5], "bm": [E5] * 2}
         self.metas = [lay[k] for lay in self.layer for k in self.order]
@@ -380,18 +384,22 @@ class StackRun:
 
     def _call(self):
         L, rec = self.L, self.rec
+        x, r = self.h0, None  # the stream before the last add, and what is added to it
         for lay in self.layer:
-            L.ln_linear_fwd(lay["h"], lay["g1"], lay["be1"], lay["wqkv"], lay["bqkv"], lay["fq"], rec, y=self.yq,
-                            ctx=lay["cq"], defer_update=True)
-            L.ln_linear_fwd(lay["attn"], None, None, lay["wproj"], lay["bproj"], lay["fp"], rec, y=self.yd,
+            L.ln_linear_fwd(x, lay["g1"], lay["be1"], lay["wqkv"], lay["bqkv"], lay["fq"], rec, y=self.yq,
+                            ctx=lay["cq"], defer_update=True, residual=r)
+            lay["hq"] = lay["cq"].x_sum if r is not None else x  # this layer's stream (the QKV input)
+            L.ln_linear_fwd(lay["attn"], None, None, lay["wproj"], lay["bproj"], lay["fp"], rec, y=self.yp,
                             ctx=lay["cp"], defer_update=True)
-            L.ln_mlp_fwd(lay["h"], lay["g2"], lay["be2"], lay["w1"], lay["b1"], lay["w2"], lay["b2"], lay["fm"], rec,
-                         y=self.yd, ctx=lay["cm"], defer_update=True)
+            L.ln_mlp_fwd(lay["hq"], lay["g2"], lay["be2"], lay["w1"], lay["b1"], lay["w2"], lay["b2"], lay["fm"], rec,
+                         y=self.ym, ctx=lay["cm"], defer_update=True, residual=self.yp)
+            x, r = lay["cm"].x_sum, self.ym
         for lay in reversed(self.layer):
-            L.ln_mlp_bwd(lay["dy"], lay["h"], lay["g2"], lay["cm"], lay["bm"], rec, grads=lay["gm"], defer_update=True)
+            L.ln_mlp_bwd(lay["dy"], lay["cm"].x_sum, lay["g2"], lay["cm"], lay["bm"], rec, grads=lay["gm"],
+                         defer_update=True)
             L.ln_linear_bwd(lay["dy"], lay["attn"], None, lay["cp"], lay["bp"], rec, grads=lay["gp"],
                             defer_update=True)
-            L.ln_linear_bwd(lay["dqkv"], lay["h"], lay["g1"], lay["cq"], lay["bq"], rec, grads=lay["gq"],
+            L.ln_linear_bwd(lay["dqkv"], lay["hq"], lay["g1"], lay["cq"], lay["bq"], rec, grads=lay["gq"],
                             defer_update=True)
         L.amax_history_update_many(self.metas, rec, self.dtypes)
 
@@ -583,8 +591,9 @@ def run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local,
                                     f"tokens, {FMT.upper()}, amax_history_len {hs}, one state-update launch for "
                                     f"all {6 * ls} state sets",
                         "layers": ls, "tokens": ms_, "d_model": ds, "ffn": fs, "amax_history_len": hs,
-                        "inputs": "per layer, device-resident: h N(0,1) + 0.1% x50, attention output N(0,1), "
-                                  "dQKV and dY N(0, 0.01); layers not chained (no residual adds)",
+                        "inputs": "device-resident: first layer's h N(0,1) + 0.1% x50; per layer attention output "
+                                  "N(0,1), dQKV and dY N(0, 0.01); forward chained as a pre-LN block (residual adds "
+                                  "fused into the next LayerNorm), backward per layer",
                         "flops": "six GEMMs per module"}}
     stack["frac_of_fp8_peak"] = stack["value"] / world / fp8_peak
     # per-kernel times of the same step (the library's event pairs as graph nodes)
