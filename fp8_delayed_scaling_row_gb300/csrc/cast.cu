@@ -166,6 +166,141 @@ cast_kernel(const CastT t0, const CastT t1) {
   block_amax_commit(am, ared, amax_cur);
 }
 
+// ------------------------------------------------------------------ row-streaming form
+// For bf16 input without a transposed copy: TPR threads per row, each owning NV
+// 16-byte column chunks of every row it visits, rows taken by a persistent
+// grid stride. Each thread copies the chunks of the rows it will convert
+// RING - 2 iterations ahead into its own slots of a shared-memory ring
+// (cp.async) and reads only its own slots. Column sums stay in registers
+// (fp32 pairs) until the end, then the row groups add them into shared memory
+// in turn and the block adds one partial per column to `colsum`.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t bf2(uint32_t w) {
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ float absmax_nan(float m, float y) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(y)));
+  return r;
+}
+__host__ __device__ constexpr int rows_ring(int nv) { return nv <= 2 ? 6 : 4; }
+constexpr int64_t kRowsMinElems = 1ll << 24;  // smallest tensor the row form takes
+
+template <int TPR, int NV, int DT>
+__global__ void __launch_bounds__(kThreads)
+cast_rows_kernel(const uint16_t* __restrict__ in, int64_t rows, int cols, const float* __restrict__ scale_p,
+                 float* amax_cur, uint8_t* __restrict__ out, float* colsum) {
+  constexpr int RING = rows_ring(NV);
+  constexpr int P = RING - 2;
+  constexpr int GPB = kThreads / TPR;
+  extern __shared__ uint4 rring[];  // [RING][NV][kThreads], then (column sums) [cols] fp32
+  __shared__ uint32_t ared[kThreads / 32];
+  float* colred = reinterpret_cast<float*>(rring + RING * NV * kThreads);
+  const int g = threadIdx.x / TPR;
+  const int gt = threadIdx.x % TPR;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (colsum) {
+    for (int c = threadIdx.x; c < cols; c += kThreads) colred[c] = 0.f;
+  }
+  const float s = *scale_p;
+  const uint64_t s2 = pk2(s, s);
+  const int64_t stride = (int64_t)gridDim.x * GPB;
+  float am = 0.f;
+  uint64_t cs[NV][4];
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cs[j][q] = 0;
+
+  auto issue = [&](int64_t r, int slot) {
+    if (r < rows) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int c = (gt + TPR * j) * 8;
+        if (c < cols) cp_async16(&rring[(slot * NV + j) * kThreads + threadIdx.x], in + r * cols + c);
+      }
+    }
+    cp_async_commit();
+  };
+  int64_t row = (int64_t)blockIdx.x * GPB + g;
+#pragma unroll
+  for (int k = 0; k < P; ++k) issue(row + k * stride, k);
+  int slot = 0;
+  for (; row < rows; row += stride) {
+    issue(row + P * stride, slot + P < RING ? slot + P : slot + P - RING);
+    cp_async_wait<P>();
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = (gt + TPR * j) * 8;
+      if (c >= cols) continue;
+      const uint4 u = rring[(slot * NV + j) * kThreads + threadIdx.x];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t c16[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t v = bf2(w[q]);
+        cs[j][q] = add2(cs[j][q], v);
+        const float2 vv = up2(v);
+        am = absmax_nan(absmax_nan(am, vv.x), vv.y);
+        const float2 z = up2(mul2(v, s2));
+        c16[q] = cvt_fp8x2<DT>(z.x, z.y);
+      }
+      *reinterpret_cast<uint2*>(out + row * cols + c) = make_uint2(c16[0] | (c16[1] << 16), c16[2] | (c16[3] << 16));
+    }
+    slot = slot + 1 == RING ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+  if (colsum) {
+    for (int turn = 0; turn < GPB; ++turn) {
+      __syncthreads();
+      if (g != turn) continue;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int c = (gt + TPR * j) * 8;
+        if (c >= cols) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 v = up2(cs[j][q]);
+          colred[c + 2 * q] += v.x;
+          colred[c + 2 * q + 1] += v.y;
+        }
+      }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < cols; c += kThreads) atomicAdd(colsum + c, colred[c]);
+  }
+  block_amax_commit(__float_as_uint(am) & 0x7FFFFFFFu, ared, amax_cur);
+}
+
 }  // namespace
 
 namespace {
@@ -195,12 +330,72 @@ lnfp8_status cast_dispatch(dim3 grid, int dtype, const CastT& a, const CastT& b,
 
 }  // namespace
 
+namespace {
+// Threads per row and 16-byte chunks per thread of the row-streaming form, or {0, 0}.
+struct RowsShape { int tpr, nv; };
+RowsShape rows_shape(int64_t cols) {
+  if (cols > 8192) return {0, 0};
+  const int64_t vecs = (cols + 7) / 8;
+  for (int tpr = 32; tpr <= 256; tpr *= 2) {
+    const int64_t nv = (vecs + tpr - 1) / tpr;
+    if (nv <= 4 || tpr == 256) return nv <= 4 ? RowsShape{tpr, (int)nv} : RowsShape{0, 0};
+  }
+  return {0, 0};
+}
+
+template <int DT>
+lnfp8_status rows_dispatch(RowsShape rs, const uint16_t* in, int64_t rows, int64_t cols, const float* scale,
+                           float* amax_cur, uint8_t* out, float* colsum, cudaStream_t st) {
+  const size_t smem = (size_t)rows_ring(rs.nv) * rs.nv * kThreads * 16 + (colsum ? (size_t)cols * 4 : 0);
+  const int64_t gpb = kThreads / rs.tpr;
+#define CRK(TPR, NV)                                                                                   \
+  do {                                                                                                 \
+    auto k = cast_rows_kernel<TPR, NV, DT>;                                                            \
+    if (smem + 1024 > 48 * 1024 &&                                                                            \
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) \
+      return check_launch("fp8_quantize: smem attribute");                                             \
+    int nb = 0;                                                                                        \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, kThreads, smem) != cudaSuccess || nb < 1) nb = 1; \
+    const int64_t blocks = min64((rows + gpb - 1) / gpb, (int64_t)nb * num_sms());                     \
+    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, in, rows, (int)cols, scale, amax_cur, out, colsum) != cudaSuccess) \
+      return check_launch("fp8_quantize launch");                                                      \
+  } while (0)
+  switch (rs.tpr * 10 + rs.nv) {
+    case 321: CRK(32, 1); break;
+    case 322: CRK(32, 2); break;
+    case 323: CRK(32, 3); break;
+    case 324: CRK(32, 4); break;
+    case 642: CRK(64, 2); break;
+    case 643: CRK(64, 3); break;
+    case 644: CRK(64, 4); break;
+    case 1282: CRK(128, 2); break;
+    case 1283: CRK(128, 3); break;
+    case 1284: CRK(128, 4); break;
+    case 2562: CRK(256, 2); break;
+    case 2563: CRK(256, 3); break;
+    case 2564: CRK(256, 4); break;
+    default: return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8_quantize: unsupported row width");
+  }
+#undef CRK
+  return check_launch("fp8_quantize");
+}
+}  // namespace
+
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st, bool clear_colsum) {
   if (clear_colsum && colsum && cols > 0 && cudaMemsetAsync(colsum, 0, cols * sizeof(float), st) != cudaSuccess)
     return check_launch("fp8_quantize: clearing colsum");
   if (rows == 0 || cols == 0) return LNFP8_OK;
+  // large bf16 tensors without a transposed copy stream through the row form (on small ones
+  // its per-block column reduction costs more than it saves)
+  const RowsShape rs = rows_shape(cols);
+  if (!in_fp32 && !out_t && out && rs.tpr && rows * cols >= kRowsMinElems) {
+    LaunchScope ls(colsum ? "cast_colsum" : "cast", st);
+    return dtype == LNFP8_E4M3
+               ? rows_dispatch<LNFP8_E4M3>(rs, static_cast<const uint16_t*>(in), rows, cols, scale, amax_cur, out, colsum, st)
+               : rows_dispatch<LNFP8_E5M2>(rs, static_cast<const uint16_t*>(in), rows, cols, scale, amax_cur, out, colsum, st);
+  }
   // enough CTAs that each SM keeps several row tiles of loads in flight
   const Grid2 g = cast_grid(rows, cols, 8LL * num_sms());
   if (g.strips > 0x7FFFFFFF || g.ysplit > 65535)

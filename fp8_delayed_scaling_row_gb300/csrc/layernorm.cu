@@ -425,7 +425,7 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
 #define LNF(TPR, NV)                                                                                    \
   do {                                                                                                  \
     auto k = ln_fwd_kernel<TPR, NV, DT, RES>;                                                           \
-    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (smem + 1024 > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                        \
     if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg, resid, hsum) != cudaSuccess) \
       return check_launch("ln_fwd_cast launch");                                                        \
@@ -490,7 +490,7 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
 #define LNB(TPR, NV)                                                                                   \
   do {                                                                                                 \
     auto k = ln_bwd_kernel<TPR, NV>;                                                                   \
-    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (smem + 1024 > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                       \
     if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta) != cudaSuccess) \
       return check_launch("ln_bwd launch");                                                            \

@@ -130,7 +130,7 @@ lnfp8_status meta_init_launch(const lnfp8_meta* m, cudaStream_t st) {
 lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, float* sinv_before,
                            cudaStream_t st) {
   const size_t smem = (size_t)m->history_len * sizeof(float);
-  if (smem > 48 * 1024) {
+  if (smem + 1024 > 48 * 1024) {
     if (cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return check_launch("amax_history_update: smem attribute");
   }
@@ -157,7 +157,7 @@ lnfp8_status update_many_launch(const lnfp8_meta* const* metas, const uint64_t* 
   tab.margin = margin;
   if (!slots) return LNFP8_OK;
   const size_t smem = (size_t)maxL * sizeof(float);
-  if (smem > 48 * 1024) {
+  if (smem + 1024 > 48 * 1024) {
     if (cudaFuncSetAttribute(update_many_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return check_launch("amax_history_update_many: smem attribute");
   }

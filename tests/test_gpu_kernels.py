@@ -61,6 +61,45 @@ def test_quantize_matches_oracle_bit_exact(L, rows, cols, dt, in_fp32):
     assert np.allclose(host(colsum), cs, rtol=1e-4, atol=1e-4 * np.abs(xv).sum(axis=0).max())
 
 
+@pytest.mark.parametrize("rows,cols,dt,with_colsum", [
+    (300, 272, 0, True), (2048, 768, 1, False), (2048, 8208, 1, True),       # strip form
+    (1 << 20, 16, 0, True), (45000, 384, 1, True), (32768, 544, 0, False),  # row form, 32 threads a row
+    (16384, 1024, 1, True), (8192, 2048, 0, True), (4096, 4096, 1, False),  # 1-4 chunks each
+    (2736, 6144, 0, True), (2048, 8192, 1, True)])                          # 64-256 threads a row
+def test_quantize_bf16_rows_without_transpose_bit_exact(L, rows, cols, dt, with_colsum):
+    # bf16 input and no transposed copy: tensors of 2^24 elements or more with rows of up to
+    # 8192 columns take the row-streaming form (every threads-per-row / chunks-per-thread
+    # shape of it here), smaller or wider ones the strip form
+    rng = np.random.default_rng(rows * 5 + cols + dt)
+    x = (rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-6, 6, (rows, 1)))).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    xv = synth.bf16_bits_to_f32(bits)
+    scale = np.float32(ofp8.FP8_MAX[FMT[dt]] / max(np.abs(xv).max(), 1e-30) * 0.7)
+    amax = _scalar(0.0)
+    out = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    colsum = torch.full((cols,), 123.0, device="cuda") if with_colsum else None
+    L.fp8_quantize(bf16_dev(bits), dt, _scalar(float(scale)), amax, out=out, colsum=colsum)
+    assert np.array_equal(host(out), ofp8.quantize(xv, scale, FMT[dt]))
+    assert host(amax)[0] == ofp8.amax(xv)
+    if with_colsum:
+        cs = xv.astype(np.float64).sum(axis=0)
+        assert np.allclose(host(colsum), cs, rtol=1e-4, atol=1e-4 * np.abs(xv).sum(axis=0).max())
+
+
+def test_quantize_bf16_rows_special_values(L):
+    x = np.tile(np.array([[0.0, -0.0, 1e30, -1e30, np.inf, -np.inf, np.nan, 3.0] * 4], dtype=np.float32), (1 << 19, 1))
+    bits = synth.f32_to_bf16_bits(x)
+    amax = _scalar(5.0)
+    out = torch.empty(x.shape[0], 32, dtype=torch.uint8, device="cuda")
+    L.fp8_quantize(bf16_dev(bits), 0, _scalar(1.0), amax, out=out)
+    got = host(out)
+    ref = ofp8.quantize(synth.bf16_bits_to_f32(bits), 1.0, ofp8.E4M3)
+    nan = np.isnan(x)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.isnan(ofp8.decode(got[nan], ofp8.E4M3)).all()
+    assert np.isnan(host(amax)[0])
+
+
 def test_quantize_special_values_and_accumulating_amax(L):
     x = np.array([[0.0, -0.0, 1e30, -1e30, np.inf, -np.inf, np.nan, 3.0] * 2], dtype=np.float32)
     amax = _scalar(5.0)  # an earlier cast of the same step already saw 5
