@@ -381,6 +381,15 @@ lnfp8_status amax_history_update_many(const lnfp8_meta* metas, int count, const 
     ptrs[k] = &metas[k];
     masks[k] = mask;
   }
+  // one CTA per slot updates it in place: a set listed twice (or two sets sharing state) would race
+  for (int k = 0; k < count; ++k)
+    for (int q = k + 1; q < count; ++q) {
+      const lnfp8_meta &a = metas[k], &b = metas[q];
+      const uintptr_t pa = reinterpret_cast<uintptr_t>(a.amax_cur), pb = reinterpret_cast<uintptr_t>(b.amax_cur);
+      const bool overlap = pa < pb + 4u * (uintptr_t)b.n && pb < pa + 4u * (uintptr_t)a.n;
+      if (overlap || a.scale == b.scale || a.amax_history == b.amax_history)
+        return set_error(LNFP8_ERR_INVALID_ARG, "%s: sets %d and %d share state", who, k, q);
+    }
   return update_many_launch(ptrs, masks, scale_inv_before, count, recipe->margin, (cudaStream_t)stream);
 }
 

@@ -164,8 +164,9 @@ lnfp8_status amax_history_update(const lnfp8_meta* meta, const lnfp8_recipe* rec
  * launch. metas: HOST array [count]; dtypes: HOST array, the sets' per-slot
  * lnfp8_dtype values one after another (sum of the n's entries);
  * scale_inv_before: HOST array [count] of optional device pointers (each [n] or
- * NULL), or NULL. The results equal count separate amax_history_update calls
- * bit for bit. */
+ * NULL), or NULL. The sets must not share state (a set listed twice, or two
+ * sets whose amax_cur ranges overlap, is refused with LNFP8_ERR_INVALID_ARG).
+ * The results equal count separate amax_history_update calls bit for bit. */
 lnfp8_status amax_history_update_many(const lnfp8_meta* metas, int count, const lnfp8_recipe* recipe,
                                       const int* dtypes, float* const* scale_inv_before,
                                       lnfp8_stream stream);

@@ -230,3 +230,5 @@ def test_update_many_equals_separate_updates(L, ns, hist):
     L.amax_history_update_many([], rec, [])  # nothing to do
     with pytest.raises(L.LnFp8Error):  # more sets than one launch takes
         L.amax_history_update_many(metas + metas[:1] * (129 - len(metas)), rec, dts + dts[:1] * (129 - len(metas)))
+    with pytest.raises(L.LnFp8Error):  # a set listed twice would race with itself
+        L.amax_history_update_many([metas[0], metas[1], metas[0]], rec, [dts[0], dts[1], dts[0]])
