@@ -124,3 +124,31 @@ def test_state_update_rejects_bad_arguments(lib):
     m0 = _meta(0, 16)
     assert lib._c_meta_init(ctypes.byref(m0), None) == 1
     assert lib._c_selftest(10, None) == 1
+
+
+def test_update_many_and_new_entry_points_reject_bad_arguments(lib):
+    rec = lib.CRecipe(1, 16, 0, 0)
+    a, b = lib.CMeta(FAKE, FAKE, FAKE, FAKE, 2, 16), lib.CMeta(FAKE + 256, FAKE + 256, FAKE + 256, FAKE + 256, 2, 16)
+    dts = (ctypes.c_int * 6)(0, 0, 0, 0, 0, 0)
+    # the same set twice would have two CTAs update one slot
+    arr = (lib.CMeta * 3)(a, b, a)
+    assert lib._c_update_many(arr, 3, ctypes.byref(rec), dts, None, None) == 1 and "share state" in lib.last_error()
+    # overlapping amax_cur ranges
+    c = lib.CMeta(FAKE + 512, FAKE + 512, FAKE + 512, FAKE + 4, 2, 16)
+    arr = (lib.CMeta * 2)(a, c)
+    assert lib._c_update_many(arr, 2, ctypes.byref(rec), dts, None, None) == 1
+    assert lib._c_update_many(arr, 129, ctypes.byref(rec), dts, None, None) == 1
+    assert lib._c_update_many(arr, -1, ctypes.byref(rec), dts, None, None) == 1
+    bad = (ctypes.c_int * 4)(0, 7, 0, 0)  # not an FP8 dtype
+    arr = (lib.CMeta * 2)(a, b)
+    assert lib._c_update_many(arr, 2, ctypes.byref(rec), bad, None, None) == 1
+    # the weight conversion takes a one-slot state
+    assert lib._c_wquant(FAKE, 64, 32, ctypes.byref(a), ctypes.byref(rec), 0, FAKE, None) == 1
+    # a residual needs the LayerNorm it precedes
+    la = lib.CLnLinearFwd(M=64, K=256, N=512, x=FAKE, gamma=None, beta=None, eps=1e-5, w=FAKE, bias=None, y=FAKE,
+                          xq=FAKE, wq=FAKE, mu=None, rsigma=None, sinv_saved=FAKE, meta=lib.CMeta(FAKE, FAKE, FAKE, FAKE, 2, 16),
+                          recipe=rec, defer_update=0, residual=FAKE, x_sum=FAKE)
+    assert lib._c_lin_fwd(ctypes.byref(la), None) == 1 and "residual" in lib.last_error()
+    # FP8 weights of an MLP come in pairs
+    m = _mlp_args(lib, w1_scale_inv=FAKE)
+    assert lib._c_mlp_fwd(ctypes.byref(m), None) == 1 and "together" in lib.last_error()
