@@ -120,15 +120,22 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
+        with open(self.path) as f:
+            return self.summarize(f, self.t0, self.t1)
+
+    @classmethod
+    def summarize(cls, lines, t0=None, t1=None):
+        """Median SM clock, max clock and power, and the throttle reasons seen, over the
+        samples taken between t0 and t1 (50 ms of slack on both sides; all when t0 is None)."""
         sm, smax, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 10:
                 continue
             try:
-                t = self._when(f[0])
-                if self.t0 is not None and not (self.t0 - 0.05 <= t <= (self.t1 or t) + 0.05):
+                t = cls._when(f[0])
+                if t0 is not None and not (t0 - 0.05 <= t <= (t1 or t) + 0.05):
                     continue
                 sm.append(float(f[2]))
                 smax.append(float(f[3]))

@@ -1,0 +1,40 @@
+"""Host-side logic of bench.py (CPU): the FLOP counts against the workloads'
+figures worked out by hand, and the clock-record summary."""
+import os
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_flop_counts():
+    # LayerNormMLP fwd+bwd: six GEMMs of 2*M*D*F each
+    assert bench.flops_per_step(8192, 768, 3072) == 6 * 2 * 8192 * 768 * 3072
+    assert abs(bench.flops_per_step() / 1e9 - 231.928) < 1e-3
+    # one transformer-block layer at d 2048 over 16384 tokens: QKV 1236.9, projection 412.3, MLP 3298.5 GFLOP
+    per_layer = bench.stack_flops_per_step(1, 16384, 2048, 8192) / 1e9
+    assert abs(per_layer - (1236.95 + 412.32 + 3298.53)) < 0.05
+    assert abs(bench.stack_flops_per_step(12, 16384, 2048, 8192) / 1e12 - 59.38) < 0.01
+
+
+def _line(ts, sm, reasons=("Not Active",) * 4):
+    return ", ".join([ts, "0", str(sm), "2070", "500.0", "0x0"] + list(reasons)) + "\n"
+
+
+def test_clock_summary_keeps_samples_inside_the_region():
+    base = time.mktime(time.strptime("2026/12/02 10:00:00", "%Y/%m/%d %H:%M:%S"))
+    lines = [_line("2026/12/02 10:00:00.000", 1000),                      # before the region
+             _line("2026/12/02 10:00:01.000", 2070),
+             _line("2026/12/02 10:00:01.500", 2000, ("Not Active", "Not Active", "Not Active", "Active")),
+             _line("2026/12/02 10:00:02.000", 1900),
+             _line("2026/12/02 10:00:05.000", 500),                       # after it
+             "garbage line\n"]
+    out = bench.ClockSampler.summarize(lines, base + 0.9, base + 2.1)
+    assert out["samples"] == 3 and out["sm_mhz"] == 2000 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"]
+    everything = bench.ClockSampler.summarize(lines)
+    assert everything["samples"] == 5 and everything["sm_mhz"] == 1900
+    assert bench.ClockSampler.summarize([])["sm_mhz"] is None
