@@ -3,6 +3,8 @@ tutorial closing list): the one-time conversion against what the FP8 formats
 fix, and the modules' FP8-weight branch against the bf16-weight branch and the
 exact fp64 layer. The residual add ahead of a LayerNorm module: against torch's
 own bf16 addition, and a zero residual against no residual."""
+import os
+
 import numpy as np
 import pytest
 
@@ -145,3 +147,20 @@ def test_residual_sum_matches_torch_bf16_addition_and_zero_is_identity():
     assert np.array_equal(ly1, ly2) and np.array_equal(la["x_sum"], bf16_to_f32(h))
     with pytest.raises(ValueError):  # a residual needs the LayerNorm it precedes
         omod.ln_linear_fwd(x, None, None, pl["w"], pl["b"], ScalingState(2, 4), rec, residual=r)
+
+
+def test_quantize_weight_hand_worked_cases():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "fp8_weight_cases.txt")
+    n = 0
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        fmt_name, margin, w, scale, codes, _ = [f.strip() for f in line.split("|", 5)]
+        W = np.array([[float(v) for v in row.split()] for row in w.split(";")], dtype=np.float32)
+        rec = Recipe(fmt_name if fmt_name != "e4m3" else "hybrid", 16, margin=int(margin))
+        got, sinv, st = omod.quantize_weight(synth.f32_to_bf16_bits(W), rec)
+        assert st.scale[0] == np.float32(float(scale)), line
+        assert sinv == np.float32(np.float32(1.0) / np.float32(float(scale))), line
+        assert [int(c, 16) for c in codes.split()] == got.ravel().tolist(), line
+        n += 1
+    assert n == 4
