@@ -64,8 +64,10 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 128;  // bytes (= FP8 elements) of K per pipeline stage
 constexpr int kEpiWarps = 16;  // two groups of 8, one per accumulator buffer
-// CTAs per cluster: a pair of CTAs works on two M tiles of the same N tile and
-// each loads half of the shared B tile, multicast to both.
+// CTAs per cluster: a pair of CTAs works on two M tiles of the same N tile.
+// With the 2-SM MMA each CTA loads its own A rows and half of the B tile;
+// otherwise each CTA loads its own A rows and the whole B tile. No load
+// writes into the peer's shared memory.
 constexpr int CL = 2;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warpgroup 0 (producer, MMA, two idle warps), 16 epilogue warps
 
@@ -185,16 +187,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-// Multicast variant: the box lands at the same shared-memory offset, and
-// signals the same barrier offset, in every CTA of the cluster named by mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-
 // 2-SM forms: the load may signal a barrier in the peer CTA; the MMA / commit
 // are issued by the pair's leader for both CTAs.
 __device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar_cluster) {
@@ -273,12 +265,6 @@ __device__ __forceinline__ void mma_commit_cg2_mc(uint32_t bar, uint16_t mask) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
-}
-// Arrive on the barrier at this offset in every CTA of the mask once the MMAs complete.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-               "h"(mask)
-               : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
@@ -396,8 +382,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      // released by the MMAs of both CTAs of the pair (1-SM), or once by the pair's leader (2-SM)
-      mbar_init(empty_bar(s), TWO ? 1 : CL);
+      // released once: by this CTA's own MMAs (1-SM), or by the pair's leader for both CTAs (2-SM)
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -411,7 +397,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // the peer multicasts into this CTA's ring and barriers: both must be initialised
+  // with the 2-SM MMA the peer's loads and commits signal this CTA's barriers:
+  // both CTAs' barriers must be initialised first
   cluster_sync();
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -479,13 +466,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
             if (!A_MN) tma_load_2d(a_dst, &tmA, kb * BK, m_blk * BM, fb);
             else       tma_load_2d(a_dst, &tmA, m_blk * BM, kb * BK, fb);
-            // this CTA's half of the B tile, multicast to both CTAs of the pair
-            if (!B_MN) {
-              tma_load_2d_mc(b_dst + rank * (BN / CL) * BK, &tmB, kb * BK, n_blk * BN + rank * (BN / CL), fb, kPair);
-            } else if (BN == 256) {
-              tma_load_2d_mc(b_dst + rank * 128 * BK, &tmB, n_blk * BN + rank * 128, kb * BK, fb, kPair);
-            } else {
-              tma_load_2d_mc(b_dst + rank * (BK / CL) * 128, &tmB, n_blk * BN, kb * BK + rank * (BK / CL), fb, kPair);
+            // the whole B tile into this CTA's own ring, as the two half boxes of
+            // the B tensor map ([BN/2 rows] K-major; [128 n] x [BK/2 k] MN-major)
+#pragma unroll
+            for (int h = 0; h < CL; ++h) {
+              if (!B_MN)          tma_load_2d(b_dst + h * (BN / CL) * BK, &tmB, kb * BK, n_blk * BN + h * (BN / CL), fb);
+              else if (BN == 256) tma_load_2d(b_dst + h * 128 * BK, &tmB, n_blk * BN + h * 128, kb * BK, fb);
+              else                tma_load_2d(b_dst + h * (BK / CL) * 128, &tmB, n_blk * BN, kb * BK + h * (BK / CL), fb);
             }
           }
           ++issued;
@@ -540,7 +527,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
           }
           if constexpr (TWO) mma_commit_cg2_mc(empty_bar(stage), kPair);  // frees the stage in both CTAs
-          else mma_commit_mc(empty_bar(stage), kPair);
+          else mma_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -887,7 +874,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     else
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS) : "memory");
   }
-  // neither CTA leaves while its peer may still multicast into it or arrive on its barriers
+  // neither CTA leaves while its peer may still arrive on its barriers (2-SM MMA)
   cluster_sync();
 }
 
@@ -1090,7 +1077,8 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   CUtensorMap ta, tb;
   const int64_t K = g.K > 0 ? g.K : 1;  // a zero-K product never loads; keep the map valid
   bool ok = a_mn ? make_operand_map(&ta, g.a, g.M, K, BK) : make_operand_map(&ta, g.a, K, g.M, BM);
-  // each CTA of a pair loads half of the B tile: [bn/2 rows] K-major, [128 n] or [BK/2 k rows] MN-major
+  // the B box is half of the B tile ([bn/2 rows] K-major, [128 n] or [BK/2 k rows] MN-major): a CTA of a
+  // 2-SM pair loads one half, a single-SM CTA both
   ok = ok && (b_mn ? make_operand_map(&tb, g.b, g.N, K, bn == 256 ? BK : BK / CL)
                    : make_operand_map(&tb, g.b, K, g.N, bn / CL));  // 128 or 96 rows per CTA of a pair
   // epilogue boxes: 32 x 32 per warp; unused maps are copies of a valid one

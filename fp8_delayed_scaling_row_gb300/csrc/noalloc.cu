@@ -14,6 +14,8 @@
 //
 // The pages have no counterpart of this entry point; it changes no numerics:
 // it runs exactly the kernels of ln_linear_bwd on the same stream.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -29,27 +31,58 @@ constexpr size_t kScratchBytes = size_t(16) << 20;
 
 __device__ __align__(256) unsigned char g_linear_bwd_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// The driver's cuCtxGetCurrent, looked up through the runtime (the library
+// links no driver library at build time).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  return fn;
+}
 
-// Device address of the scratch array on the current device. In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device with that device current, and cached.
+CUcontext current_context() {
+  CUcontext c = nullptr;
+  const CtxGetCurrentFn fn = ctx_get_current();
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+constexpr int kMaxDevices = 64;
+struct ScratchSlot {
+  CUcontext ctx;  // the context the address belongs to
+  void* addr;
+};
+std::mutex g_scratch_mu;
+ScratchSlot g_scratch[kMaxDevices] = {};
+
+// Device address of the scratch array in the current device's current
+// context. In host code the array's name is only a host-side stand-in, so the
+// address is looked up with that device current: once per device, and again
+// whenever the current context is not the one the address was taken in (a
+// caller that runs its own context on the device).
 lnfp8_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("ln_linear_bwd_noalloc: cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return set_error(LNFP8_ERR_UNSUPPORTED, "ln_linear_bwd_noalloc: device ordinal %d >= %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchSlot& slot = g_scratch[dev];
+  const CUcontext ctx = current_context();
+  if (!slot.addr || ctx == nullptr || ctx != slot.ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_linear_bwd_scratch);
     if (e != cudaSuccess || p == nullptr)
       return set_error(LNFP8_ERR_CUDA, "ln_linear_bwd_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+    slot.addr = p;
+    slot.ctx = current_context();  // the lookup made the device's context current if none was
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return LNFP8_OK;
 }
 

@@ -348,7 +348,11 @@ int64_t lnfp8_ln_linear_bwd_workspace_size(int64_t M, int64_t K, int64_t N);
  * nothing and runs the same kernels as ln_linear_bwd.
  *   - The first call on each device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture. A call made under another CUDA context on the same
+ *     device than the one of the previous calls looks the address up again
+ *     (also before any capture). After cudaDeviceReset the library may still
+ *     hold the old address: do not call this entry point again in a process
+ *     that has reset the device.
  *   - All calls share the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero (both buffers are fully written
  *     before they are read). Calls whose work overlaps on the GPU (other

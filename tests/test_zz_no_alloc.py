@@ -1,14 +1,24 @@
 """ln_linear_bwd_noalloc: the LayerNormLinear backward for callers that cannot
 allocate device memory (GPU).
 
-Such a caller passes inputs and outputs only; the dY codes and the LayerNorm
-output gradient live in the library's own fixed scratch array. The test checks,
-through the C ABI, that two calls in a row give the same results as
-ln_linear_bwd with caller-provided scratch, within the tolerance the other
-parity tests use, and that a problem larger than the scratch is refused before
-anything runs. This file is collected last on purpose.
+Some callers may not call cudaMalloc: a plug-in that a host framework hands
+only the tensors of one layer, or a runtime whose device memory is fixed before
+start-up. Such a caller passes inputs and outputs only; the dY codes and the
+LayerNorm-output gradient live in the library's own fixed scratch array. The
+tests check, through the C ABI:
+  * two calls in a row give the same results as ln_linear_bwd with
+    caller-provided scratch, within the tolerance the other parity tests use,
+    and the same delayed-scaling state bit for bit;
+  * the call takes no device memory: the GPU's free memory is the same
+    before and after the second call;
+  * a problem larger than the scratch is refused before anything is enqueued
+    (real buffers of the declared sizes, whose contents stay untouched).
+
+The file is named so that pytest collects it last: if it fails, a run that
+stops at the first failure (-x) has already run every other test. It passes
+both alone in a fresh process and after the other tests (its first call on the
+device does the one-time address lookup either way).
 """
-import numpy as np
 import pytest
 
 from fp8_delayed_scaling_row_gb300 import synth
@@ -32,6 +42,11 @@ def _copy_meta(L, src):
     return m
 
 
+def _free_bytes():
+    torch.cuda.synchronize()
+    return torch.cuda.mem_get_info()[0]
+
+
 @pytest.mark.parametrize("M,K,N,ln", [(256, 768, 2304, True), (300, 192, 400, True), (250, 256, 128, False)])
 def test_noalloc_backward_matches_the_allocating_one_twice_in_a_row(L, M, K, N, ln):
     rec = L.Recipe("hybrid", 16)
@@ -47,9 +62,13 @@ def test_noalloc_backward_matches_the_allocating_one_twice_in_a_row(L, M, K, N, 
         ref_meta = _copy_meta(L, bm)
         ref = L.ln_linear_bwd(dy, x, gamma, ctx, ref_meta, rec)
         out = L.linear_grads(M, K, N, ln=ln)
+        free0 = _free_bytes()
         L.ln_linear_bwd_noalloc(dy, x, gamma, ctx, bm, rec, dx=out.dx, dw=out.dw, dbias=out.dbias,
                                 dgamma=out.dgamma, dbeta=out.dbeta)
         L.sync_status()
+        free1 = _free_bytes()
+        if step == 1:  # the first call may load the kernels' code; the second reuses everything
+            assert free1 == free0, f"device memory changed by {free0 - free1} bytes"
         for name in ("dx", "dw", "dbias") + (("dgamma", "dbeta") if ln else ()):
             got, want = host(getattr(out, name)), host(getattr(ref, name))
             assert rel_fro(got, want) < TOL, (step, name)
@@ -58,12 +77,32 @@ def test_noalloc_backward_matches_the_allocating_one_twice_in_a_row(L, M, K, N, 
 
 
 def test_noalloc_backward_refuses_problems_larger_than_its_scratch(L):
-    M, K, N = 8192, 1024, 2048  # 16 MiB of dY codes + 16 MiB of LayerNorm gradient: too large
-    a = L.CLnLinearBwd(M=M, K=K, N=N, dy=0x10000, x=0x10000, gamma=0x10000, xq=0x10000, wq=0x10000, mu=0x10000,
-                       rsigma=0x10000, sinv_saved=0x10000, dx=0x10000, dw=0x10000, dbias=None, dgamma=0x10000,
-                       dbeta=0x10000, dyq=None, dln=None, meta=L.CMeta(0x10000, 0x10000, 0x10000, 0x10000, 1, 16),
-                       recipe=L.CRecipe(1, 16, 0, 0), defer_update=0)
-    import ctypes
-    st = L._c_lin_bwd_noalloc(ctypes.byref(a), None)
-    assert st == L.ERR_UNSUPPORTED_SHAPE
-    assert "scratch" in L.last_error()
+    # 9 MiB of dY codes + 8 MiB of LayerNorm-output gradient: one MiB over the 16 MiB scratch
+    M, K, N = 4096, 1024, 2304
+    rec = L.Recipe("hybrid", 16)
+    dev = "cuda"
+    x = torch.zeros(M, K, dtype=torch.bfloat16, device=dev)
+    dy = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
+    gamma = torch.ones(K, dtype=torch.bfloat16, device=dev)
+    ctx = L.linear_ctx(M, K, N, ln=True, device=dev)
+    for t in (ctx.xq, ctx.wq, ctx.mu, ctx.rsigma, ctx.sinv_saved):
+        t.zero_()
+    bm = L.ScalingMeta(1, 16)
+    sentinel = 0x3F80  # bf16 1.0
+    dx = torch.full((M, K), 1.0, dtype=torch.bfloat16, device=dev)
+    dw = torch.full((N, K), 1.0, dtype=torch.bfloat16, device=dev)
+    dbias = torch.full((N,), 7.0, device=dev)
+    dgamma = torch.full((K,), 7.0, device=dev)
+    dbeta = torch.full((K,), 7.0, device=dev)
+    state0 = {k: v.clone() for k, v in bm.state_dict().items()}
+    torch.cuda.synchronize()
+    with pytest.raises(L.LnFp8Error) as e:
+        L.ln_linear_bwd_noalloc(dy, x, gamma, ctx, bm, rec, dx=dx, dw=dw, dbias=dbias, dgamma=dgamma, dbeta=dbeta)
+    assert e.value.status == L.ERR_UNSUPPORTED_SHAPE
+    assert "scratch" in str(e.value)
+    torch.cuda.synchronize()
+    # refused before anything was enqueued: outputs and state untouched
+    assert (dx.view(torch.int16) == sentinel).all() and (dw.view(torch.int16) == sentinel).all()
+    assert (dbias == 7.0).all() and (dgamma == 7.0).all() and (dbeta == 7.0).all()
+    for k, v in bm.state_dict().items():
+        assert torch.equal(v, state0[k]), k
