@@ -39,12 +39,17 @@ def flops_per_step(m=M_TOK, d=D_MODEL, f=FFN):
     return 12.0 * m * d * f
 
 
-def workload(m=M_TOK, d=D_MODEL, f=FFN, fmt=FMT, hist=HIST, dist="outliers"):
-    return {"workload": f"LayerNormMLP fwd+bwd, {m} tokens x {d} -> {f} -> {d}, {fmt.upper()} "
-                        f"(E4M3 fwd / E5M2 grads), amax_history_len {hist}, fresh X and dY each step",
+FORMAT_TEXT = {"hybrid": "HYBRID (E4M3 fwd / E5M2 grads)", "e4m3": "E4M3 everywhere", "e5m2": "E5M2 everywhere"}
+DIST_TEXT = {"outliers": "N(0,1) + 0.1% entries x50", "normal": "N(0,1)", "t3": "Student-t(3)"}
+
+
+def workload(m=M_TOK, d=D_MODEL, f=FFN, fmt=FMT, hist=HIST, dist="outliers", n_sets=8, inputs="host"):
+    src = "seeded host generator" if inputs == "host" else "the device's generator"
+    return {"workload": f"LayerNormMLP fwd+bwd, {m} tokens x {d} -> {f} -> {d}, {FORMAT_TEXT[fmt]}, "
+                        f"amax_history_len {hist}, {n_sets} pre-drawn X / dY batches cycled over the steps",
             "tokens": m, "d_model": d, "ffn": f, "fp8_format": fmt, "amax_history_len": hist,
-            "x_dist": {"outliers": "N(0,1) + 0.1% entries x50", "normal": "N(0,1)", "t3": "Student-t(3)"}[dist],
-            "dy_dist": "N(0, 0.01)", "weights": "N(0, 0.02), bias 0",
+            "x_dist": DIST_TEXT[dist], "dy_dist": "N(0, 0.01)", "weights": "N(0, 0.02), bias 0",
+            "inputs": f"{n_sets} batches drawn once by the {src}, device-resident, step i uses batch i mod {n_sets}",
             "l2": "flushed (256 MiB write) between timed steps", "parallelism": "replicas (one per GPU)"}
 
 
@@ -242,11 +247,25 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- GPU arm
+def device_draw(torch, g, shape, dist="normal", std=1.0):
+    """bf16 tensor on the device: N(0,1) (x50 on 0.1% of entries for "outliers") or
+    Student-t(3) = N / sqrt(chi2_3 / 3), times std."""
+    z = torch.randn(*shape, generator=g, device=g.device, dtype=torch.float32)
+    if dist == "outliers":
+        z = torch.where(torch.rand(*shape, generator=g, device=g.device) < 1e-3, z * 50, z)
+    elif dist == "t3":
+        chi2 = sum(torch.randn(*shape, generator=g, device=g.device, dtype=torch.float32) ** 2 for _ in range(3))
+        z = z / torch.sqrt(chi2 / 3.0)
+    return (z * std).to(torch.bfloat16)
+
+
 class MlpRun:
     """Device-resident workload: weights, state, saved tensors, gradient buffers,
-    and P pre-generated input batches cycled over the steps."""
+    and n_sets input batches drawn once and cycled over the steps (inputs="host":
+    the seeded host generator, also kept in pinned-able host arrays for the end-to-end
+    leg; "device": the device's generator, for the large sweep points)."""
 
-    def __init__(self, L, torch, dev, m, d, f, fmt, hist, dist, n_sets, seed):
+    def __init__(self, L, torch, dev, m, d, f, fmt, hist, dist, n_sets, seed, inputs="host", params=None):
         from fp8_delayed_scaling_row_gb300 import synth
         import numpy as np
 
@@ -254,19 +273,24 @@ class MlpRun:
             return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
         self.L, self.torch, self.m, self.d, self.f = L, torch, m, d, f
-        p = synth.mlp_params(d, f, seed=seed)
-        self.p = {k: bf(v) for k, v in p.items()}
+        self.p = params if params is not None else {k: bf(v) for k, v in synth.mlp_params(d, f, seed=seed).items()}
         self.rec = L.Recipe(fmt, hist)
         self.fm, self.bm = L.ScalingMeta(4, hist, device=dev), L.ScalingMeta(2, hist, device=dev)
         self.ctx = L.mlp_ctx(m, d, f, device=dev)
         self.grads = L.mlp_grads(m, d, f, device=dev)
         self.y = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
         self.xs_host, self.dys_host = [], []
-        for i in range(n_sets):
-            self.xs_host.append(synth.activations(m, d, dist=dist, seed=seed, step=i))
-            self.dys_host.append(synth.grad(m, d, seed=seed, step=i))
-        self.xs = [bf(x) for x in self.xs_host]
-        self.dys = [bf(x) for x in self.dys_host]
+        if inputs == "host":
+            for i in range(n_sets):
+                self.xs_host.append(synth.activations(m, d, dist=dist, seed=seed, step=i))
+                self.dys_host.append(synth.grad(m, d, seed=seed, step=i))
+            self.xs = [bf(x) for x in self.xs_host]
+            self.dys = [bf(x) for x in self.dys_host]
+        else:
+            g = torch.Generator(device=dev)
+            g.manual_seed(seed)
+            self.xs = [device_draw(torch, g, (m, d), dist) for _ in range(n_sets)]
+            self.dys = [device_draw(torch, g, (m, d), "normal", 0.01) for _ in range(n_sets)]
         self.graphs = None
 
     def step(self, i, x=None, dy=None):
@@ -343,7 +367,16 @@ class StackRun:
     ~ N(0, 0.01) (the backward is not chained: attention is not on this path).
     The whole step is one captured CUDA graph."""
 
-    def __init__(self, L, torch, dev, layers, m, d, f, fmt, hist, seed):
+    PARAMS = ("wqkv", "bqkv", "g1", "be1", "wproj", "bproj", "g2", "be2", "w1", "b1", "w2", "b2")
+
+    def __init__(self, L, torch, dev, layers, m, d, f, fmt, hist, seed, host_params=None, host_inputs=None,
+                 keep_outputs=False):
+        """host_params: None (weights drawn on the device), or per layer a dict of
+        bf16 bit patterns (numpy uint16) under the names in PARAMS; host_inputs: None,
+        or a dict of bf16 bit patterns h0 [m, d], attn [m, d], dqkv [m, 3d], dy [m, d]
+        shared by every layer (the parity tests feed seeded host inputs this way);
+        keep_outputs: every layer writes its QKV, projection and MLP outputs to buffers
+        of its own (lay["yq"], lay["yp"], lay["ym"]) instead of sharing one set."""
         self.L, self.torch, self.layers, self.m, self.d, self.f = L, torch, layers, m, d, f
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
@@ -357,18 +390,30 @@ class StackRun:
         def ones_plus(n):
             return (1 + 0.1 * torch.randn(n, generator=g, device=dev)).to(torch.bfloat16)
 
+        def from_bits(bits):
+            import numpy as np
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        shared = None if host_inputs is None else {k: from_bits(v) for k, v in host_inputs.items()}
         self.rec = L.Recipe(fmt, hist)
         E4, E5 = L.E4M3, L.E5M2
         self.layer = []
-        for _ in range(layers):
-            lay = dict(
-                wqkv=randn(3 * d, d, std=0.02), bqkv=torch.zeros(3 * d, dtype=torch.bfloat16, device=dev),
-                g1=ones_plus(d), be1=randn(d, std=0.1),
-                wproj=randn(d, d, std=0.02), bproj=torch.zeros(d, dtype=torch.bfloat16, device=dev),
-                g2=ones_plus(d), be2=randn(d, std=0.1),
-                w1=randn(f, d, std=0.02), b1=torch.zeros(f, dtype=torch.bfloat16, device=dev),
-                w2=randn(d, f, std=0.02), b2=torch.zeros(d, dtype=torch.bfloat16, device=dev),
-                attn=randn(m, d), dqkv=randn(m, 3 * d, std=0.01), dy=randn(m, d, std=0.01),
+        for li in range(layers):
+            if host_params is None:
+                lay = dict(
+                    wqkv=randn(3 * d, d, std=0.02), bqkv=torch.zeros(3 * d, dtype=torch.bfloat16, device=dev),
+                    g1=ones_plus(d), be1=randn(d, std=0.1),
+                    wproj=randn(d, d, std=0.02), bproj=torch.zeros(d, dtype=torch.bfloat16, device=dev),
+                    g2=ones_plus(d), be2=randn(d, std=0.1),
+                    w1=randn(f, d, std=0.02), b1=torch.zeros(f, dtype=torch.bfloat16, device=dev),
+                    w2=randn(d, f, std=0.02), b2=torch.zeros(d, dtype=torch.bfloat16, device=dev))
+            else:
+                lay = {k: from_bits(host_params[li][k]) for k in self.PARAMS}
+            if shared is None:
+                lay.update(attn=randn(m, d), dqkv=randn(m, 3 * d, std=0.01), dy=randn(m, d, std=0.01))
+            else:
+                lay.update(attn=shared["attn"], dqkv=shared["dqkv"], dy=shared["dy"])
+            lay.update(
                 fq=L.ScalingMeta(2, hist, device=dev), fp=L.ScalingMeta(2, hist, device=dev),
                 fm=L.ScalingMeta(4, hist, device=dev), bq=L.ScalingMeta(1, hist, device=dev),
                 bp=L.ScalingMeta(1, hist, device=dev), bm=L.ScalingMeta(2, hist, device=dev),
@@ -377,12 +422,17 @@ class StackRun:
                 gq=L.linear_grads(m, d, 3 * d, device=dev), gp=L.linear_grads(m, d, d, ln=False, device=dev),
                 gm=L.mlp_grads(m, d, f, device=dev))
             self.layer.append(lay)
-        self.h0 = randn(m, d, outliers=True)
+        self.h0 = randn(m, d, outliers=True) if shared is None else shared["h0"]
         # the QKV output is not consumed (attention is synthetic); projection and MLP outputs
         # feed the next LayerNorm's fused residual add
         self.yq = torch.empty(m, 3 * d, dtype=torch.bfloat16, device=dev)
         self.yp = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
         self.ym = torch.empty(m, d, dtype=torch.bfloat16, device=dev)
+        for i, lay in enumerate(self.layer):
+            own = keep_outputs and i < layers - 1  # the last layer writes the shared set
+            lay["yq"] = torch.empty_like(self.yq) if own else self.yq
+            lay["yp"] = torch.empty_like(self.yp) if own else self.yp
+            lay["ym"] = torch.empty_like(self.ym) if own else self.ym
         self.order = ["fq", "fp", "fm", "bq", "bp", "bm"]
         dts = {"fq": [E4] * 2, "fp": [E4] * 2, "fm": [E4] * 4, "bq": [E5], "bp": [E5], "bm": [E5] * 2}
         self.metas = [lay[k] for lay in self.layer for k in self.order]
@@ -393,14 +443,14 @@ class StackRun:
         L, rec = self.L, self.rec
         x, r = self.h0, None  # the stream before the last add, and what is added to it
         for lay in self.layer:
-            L.ln_linear_fwd(x, lay["g1"], lay["be1"], lay["wqkv"], lay["bqkv"], lay["fq"], rec, y=self.yq,
+            L.ln_linear_fwd(x, lay["g1"], lay["be1"], lay["wqkv"], lay["bqkv"], lay["fq"], rec, y=lay["yq"],
                             ctx=lay["cq"], defer_update=True, residual=r)
             lay["hq"] = lay["cq"].x_sum if r is not None else x  # this layer's stream (the QKV input)
-            L.ln_linear_fwd(lay["attn"], None, None, lay["wproj"], lay["bproj"], lay["fp"], rec, y=self.yp,
+            L.ln_linear_fwd(lay["attn"], None, None, lay["wproj"], lay["bproj"], lay["fp"], rec, y=lay["yp"],
                             ctx=lay["cp"], defer_update=True)
             L.ln_mlp_fwd(lay["hq"], lay["g2"], lay["be2"], lay["w1"], lay["b1"], lay["w2"], lay["b2"], lay["fm"], rec,
-                         y=self.ym, ctx=lay["cm"], defer_update=True, residual=self.yp)
-            x, r = lay["cm"].x_sum, self.ym
+                         y=lay["ym"], ctx=lay["cm"], defer_update=True, residual=lay["yp"])
+            x, r = lay["cm"].x_sum, lay["ym"]
         for lay in reversed(self.layer):
             L.ln_mlp_bwd(lay["dy"], lay["cm"].x_sum, lay["g2"], lay["cm"], lay["bm"], rec, grads=lay["gm"],
                          defer_update=True)
@@ -551,7 +601,9 @@ def end_to_end(torch, run, steps, dev, barrier, max_over_ranks, world, graph=Tru
     for b in range(2):
         done[b].record(comp)
         out_read[b].record(comp)
-    for i in range(3):
+    # warm-up: every pinned host batch and both device sets take part once before the
+    # timed region, so first-use costs of the host buffers stay outside it
+    for i in range(max(3, len(xh))):
         issue(i)
     torch.cuda.synchronize()
     barrier()
@@ -575,32 +627,50 @@ def end_to_end(torch, run, steps, dev, barrier, max_over_ranks, world, graph=Tru
                       "overlapping the neighbouring steps' compute (two device buffer sets)"}
 
 
-def run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak):
-    """The scale-up stack step (StackRun), timed like the main workload, with its own
-    clock record and per-kernel times."""
-    ls, ms_, ds, fs, hs = args.stack_layers, 16384, 2048, 8192, 1024
+def stack_hbm_bytes(layers, m, d, f):
+    """Algorithmic bytes per stack step of the HBM-bound kernel kinds (each tensor read
+    or written once): LayerNorm forward (x, and with the fused residual add r and the sum
+    h, read/written as bf16; codes written; mu, rsigma), LayerNorm backward (dLN, x read,
+    dX written), the gradient casts with column sums (dY of the MLP and the projection,
+    dQKV), the plain casts (QKV and projection weights, the projection's input) and the
+    MLP weight pair."""
+    row = 8 * m
+    return {
+        "ln_fwd_cast": (3 * m * d + row) + (2 * layers - 1) * (7 * m * d + row),
+        "ln_bwd": 2 * layers * (6 * m * d + row),
+        "cast_colsum": layers * (3 * (m * d + m * d + 3 * m * d) + 4 * (d + d + 3 * d)),
+        "cast": layers * (3 * (3 * d * d + d * d) + 3 * m * d),
+        "cast_pair": layers * 3 * 2 * f * d,
+    }
+
+
+def run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak, hbm,
+              layers, m, d, f, hist, seed, k_max=40):
+    """A transformer-block module stack step (StackRun), timed like the main workload,
+    with its own clock record, per-kernel times and the HBM-bound kinds' fractions."""
     torch.cuda.empty_cache()
-    srun = StackRun(L, torch, dev, ls, ms_, ds, fs, FMT, hs, seed=977 + rank)
+    srun = StackRun(L, torch, dev, layers, m, d, f, FMT, hist, seed=seed + rank)
     if args.graph:
         srun.capture()
-    ks = max(3, min(args.steps, 40))
-    sclk = ClockSampler(local, "_stack")
+    ks = max(3, min(args.steps, k_max))
+    sclk = ClockSampler(local, f"_stack{d}x{layers}")
     sclk.start()
     sms, slaunch = timed_steps(torch, srun, ks, 3, flush, barrier, sclk)
     sclk = sclk.stop()
     sms = max_over_ranks(sms)
     L.sync_status()
-    stack = {"value": stack_flops_per_step(ls, ms_, ds, fs) * ks * world / (sms / 1e3) / 1e12,
+    flops = stack_flops_per_step(layers, m, d, f)
+    stack = {"value": flops * ks * world / (sms / 1e3) / 1e12,
              "unit": "TFLOP/s", "ms_per_step": sms / ks, "steps": ks, "gpu_launches": slaunch,
              "frac_of_fp8_peak": None, "cuda_graph": bool(args.graph), "clocks": sclk,
-             "config": {"workload": f"transformer-block FP8 module stack fwd+bwd: {ls} layers x (LayerNormLinear "
-                                    f"{ds}->{3 * ds}, Linear {ds}->{ds}, LayerNormMLP {ds}->{fs}->{ds}), {ms_} "
-                                    f"tokens, {FMT.upper()}, amax_history_len {hs}, one state-update launch for "
-                                    f"all {6 * ls} state sets",
-                        "layers": ls, "tokens": ms_, "d_model": ds, "ffn": fs, "amax_history_len": hs,
-                        "inputs": "device-resident: first layer's h N(0,1) + 0.1% x50; per layer attention output "
-                                  "N(0,1), dQKV and dY N(0, 0.01); forward chained as a pre-LN block (residual adds "
-                                  "fused into the next LayerNorm), backward per layer",
+             "config": {"workload": f"transformer-block FP8 module stack fwd+bwd: {layers} layers x (LayerNormLinear "
+                                    f"{d}->{3 * d}, Linear {d}->{d}, LayerNormMLP {d}->{f}->{d}), {m} "
+                                    f"tokens, {FMT.upper()}, amax_history_len {hist}, one state-update launch for "
+                                    f"all {6 * layers} state sets",
+                        "layers": layers, "tokens": m, "d_model": d, "ffn": f, "amax_history_len": hist,
+                        "inputs": "drawn once on the device and replayed every step: first layer's h N(0,1) + 0.1% "
+                                  "x50; per layer attention output N(0,1), dQKV and dY N(0, 0.01); forward chained "
+                                  "as a pre-LN block (residual adds fused into the next LayerNorm), backward per layer",
                         "flops": "six GEMMs per module"}}
     stack["frac_of_fp8_peak"] = stack["value"] / world / fp8_peak
     # per-kernel times of the same step (the library's event pairs as graph nodes)
@@ -614,15 +684,131 @@ def run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local,
         sprof = L.profile_collect()
         L.profile_enable(False)
         tot = sum(v[0] for v in sprof.values()) or 1.0
-        stack["per_kernel"] = {k: {"ms_per_step": v[0] / 3, "launches_per_step": v[1] / 3, "share": v[0] / tot}
-                               for k, v in sorted(sprof.items(), key=lambda kv: -kv[1][0])}
+        nbytes = stack_hbm_bytes(layers, m, d, f)
+        pk = {}
+        for k, v in sorted(sprof.items(), key=lambda kv: -kv[1][0]):
+            pk[k] = {"ms_per_step": v[0] / 3, "launches_per_step": v[1] / 3, "share": v[0] / tot}
+            if k in nbytes:
+                gbs = nbytes[k] / (v[0] / 3 / 1e3) / 1e9
+                pk[k].update({"algorithmic_bytes_per_step": nbytes[k], "gbs": gbs, "frac_hbm": gbs / hbm})
+        stack["per_kernel"] = pk
+        stack["per_kernel_timing"] = ("CUDA events around each launch inside replays of the captured step; each "
+                                      "time includes the launch gap the event nodes add (a few us), so short "
+                                      "kernels read low")
         gk = [v for k, v in sprof.items() if k.startswith("gemm")]
         if gk:
-            stack["gemm_family_tflops"] = stack_flops_per_step(ls, ms_, ds, fs) / (sum(v[0] for v in gk) / 3 / 1e3) / 1e12
+            stack["gemm_family_tflops"] = flops / (sum(v[0] for v in gk) / 3 / 1e3) / 1e12
     del srun
     torch.cuda.empty_cache()
-
     return stack
+
+
+def run_config1(L, torch, dev, args, flush, fp8_peak, hbm):
+    """LayerNormLinear forward 768 -> 2304 over 256 tokens (8 x 32), E4M3, history 16:
+    one step, latency-bound; the median device time of replays of the captured call,
+    for the library's automatic choice (the one-launch fused path here) and for the
+    separate launches."""
+    import numpy as np
+    from fp8_delayed_scaling_row_gb300 import synth
+    m, k, n, hist = 256, 768, 2304, 16
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    p = synth.linear_params(n, k, seed=1234)
+    x, g, b, w, bias = bf(synth.activations(m, k, seed=1234)), bf(p["gamma"]), bf(p["beta"]), bf(p["w"]), bf(p["b"])
+    rec = L.Recipe("e4m3", hist)
+    flops = 2.0 * m * k * n
+    nbytes = m * k * (2 + 1) + 8 * m + n * k * (2 + 1) + m * n * 2  # x in, codes; W in, codes; y out
+
+    def time_path(path):
+        meta = L.ScalingMeta(2, hist, device=dev)
+        ctx, y = L.linear_ctx(m, k, n, device=dev), torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+
+        def call():
+            L.ln_linear_fwd(x, g, b, w, bias, meta, rec, y=y, ctx=ctx, path=path)
+
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            c0 = L.launch_count()
+            call()
+            launches = L.launch_count() - c0
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        gr = None
+        if args.graph:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                call()
+        run = gr.replay if gr is not None else call
+        steps = max(20, min(10 * args.steps, 500))
+        for _ in range(5):
+            run()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, e in ev:
+            flush.zero_()
+            a.record()
+            run()
+            e.record()
+        torch.cuda.synchronize()
+        L.sync_status()
+        t = sorted(a.elapsed_time(e) for a, e in ev)
+        med = t[len(t) // 2]
+        return {"value": med * 1e3, "unit": "us/step", "min_us": t[0] * 1e3, "steps": steps,
+                "tflops": flops / (med / 1e3) / 1e12, "frac_of_fp8_peak": flops / (med / 1e3) / 1e12 / fp8_peak,
+                "gbs": nbytes / (med / 1e3) / 1e9, "frac_hbm": nbytes / (med / 1e3) / 1e9 / hbm,
+                "gpu_launches_per_step": launches, "cuda_graph": gr is not None}
+
+    auto = time_path(L.PATH_AUTO)
+    sep = time_path(L.PATH_SEPARATE)
+    out = dict(auto, higher_is_better=False, path="automatic (one fused launch + the state update at 256 tokens)")
+    out["separate_launches"] = sep
+    out["config"] = {"workload": "LayerNormLinear forward 768 -> 2304 over 256 tokens (8 x 32), E4M3 activations and "
+                                 "weights, amax_history_len 16, bias 0: LayerNorm + amax + cast, weight cast, FP8 GEMM, "
+                                 "state update", "tokens": m, "in_features": k, "out_features": n,
+                     "x_dist": "N(0,1)", "l2": "flushed between timed calls",
+                     "timing": "median of per-call CUDA events"}
+    return out
+
+
+def run_sweep(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak):
+    """Standalone LayerNormMLP 2048 -> 8192 -> 2048 fwd+bwd over tokens in {2048, 8192,
+    32768, 65536}, E4M3 and HYBRID, N(0,1) and Student-t(3) activations, history 16
+    and 1024: every point timed like the main workload (inputs drawn on the device)."""
+    import numpy as np
+    from fp8_delayed_scaling_row_gb300 import synth
+    d, f = 2048, 8192
+    params = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).to(dev)
+              for k, v in synth.mlp_params(d, f, seed=2048).items()}
+    clk = ClockSampler(local, "_sweep")
+    clk.start()
+    clk.mark_start()
+    points = []
+    for m in (2048, 8192, 32768, 65536):
+        for fmt in ("e4m3", "hybrid"):
+            for dist in ("normal", "t3"):
+                for hist in (16, 1024):
+                    run = MlpRun(L, torch, dev, m, d, f, fmt, hist, dist, 2, seed=m + 7 * hist + rank,
+                                 inputs="device", params=params)
+                    if args.graph:
+                        run.capture()
+                    k = max(3, min(args.steps, 20))
+                    ms = max_over_ranks(timed_steps(torch, run, k, 3, flush, barrier)[0])
+                    L.sync_status()
+                    v = flops_per_step(m, d, f) * k * world / (ms / 1e3) / 1e12
+                    points.append({"tokens": m, "fp8_format": fmt, "x_dist": DIST_TEXT[dist],
+                                   "amax_history_len": hist, "value": v, "unit": "TFLOP/s",
+                                   "ms_per_step": ms / k, "steps": k, "frac_of_fp8_peak": v / world / fp8_peak})
+                    del run
+                    torch.cuda.empty_cache()
+    clk.mark_stop()
+    return {"points": points, "clocks": clk.stop(),
+            "config": {"workload": "LayerNormMLP 2048 -> 8192 -> 2048 fwd+bwd sweep: tokens x format x "
+                                   "activation distribution x amax_history_len, each point timed alone",
+                       "inputs": "2 X / dY batches per point drawn on the device, cycled; weights N(0, 0.02)",
+                       "l2": "flushed (256 MiB write) between timed steps"}}
 
 
 def run_gpu(args):
@@ -651,10 +837,13 @@ def run_gpu(args):
         return float(t.item())
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    if args.stack_only:  # diagnostic: the stack step alone (e.g. a one-layer case to profile)
-        pk, _ = peaks()
-        fp8_peak = (_num(pk, "bf16_tflops", "bf16_tflops_burst") or FALLBACK["bf16_tflops"]) * FP8_PER_BF16
-        stack = run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak)
+    pk, how = peaks()
+    bf16 = _num(pk, "bf16_tflops", "bf16_tflops_burst") or FALLBACK["bf16_tflops"]
+    fp8_peak = bf16 * FP8_PER_BF16
+    hbm = _num(pk, "hbm_gbs", "hbm_GBs", "hbm_copy_gbs") or FALLBACK["hbm_gbs"]
+    if args.stack_only:  # diagnostic: the d 2048 stack step alone (e.g. a one-layer case to profile)
+        stack = run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local, rank, fp8_peak, hbm,
+                          args.stack_layers, 16384, 2048, 8192, 1024, seed=977)
         if rank == 0:
             print(json.dumps({"stack": stack}), flush=True)
         return 0
@@ -701,9 +890,6 @@ def run_gpu(args):
     gemm_kinds = {k: v for k, v in prof.items() if k.startswith("gemm")}
     g_ms = sum(v[0] for v in gemm_kinds.values())
     g_n = sum(v[1] for v in gemm_kinds.values())
-    pk, how = peaks()
-    bf16 = _num(pk, "bf16_tflops", "bf16_tflops_burst") or FALLBACK["bf16_tflops"]
-    fp8_peak = bf16 * FP8_PER_BF16
     g_flops = flops_per_step()  # the six GEMMs, 2 * M * D * F each
     achieved = g_flops / (g_ms / prof_steps / 1e3) / 1e12 if g_n else None
     roofline = {"kernel": "fp8 GEMM family (tcgen05 kind::f8f6f4): the step's six GEMMs in four launches",
@@ -713,7 +899,6 @@ def run_gpu(args):
                 "flops_per_launch": g_flops, "launch": "one step's GEMM launches (summed device time)",
                 "gemm_launches_per_step": g_n / prof_steps, "launches_timed": g_n, "timed_from": prof_how,
                 "share_of_step": g_ms / sum(v[0] for v in prof.values()) if prof else None}
-    hbm = _num(pk, "hbm_gbs", "hbm_GBs", "hbm_copy_gbs") or FALLBACK["hbm_gbs"]
     per_kernel = {}
     for k, (kms, cnt) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
         per_kernel[k] = {"ms_per_launch": kms / cnt, "launches_per_step": cnt / prof_steps,
@@ -734,25 +919,19 @@ def run_gpu(args):
     e2e_steps = min(args.steps, 200)
     e2e = end_to_end(torch, run, e2e_steps, dev, barrier, max_over_ranks, world, graph=bool(args.graph))
 
-    # ---- D = 2048: LayerNormMLP 2048 -> 8192 -> 2048 over 16384 tokens (the scale-up width)
-    d2048 = None
-    if not args.no_d2048:
-        m2, d2, f2 = 16384, 2048, 8192
-        del run
-        torch.cuda.empty_cache()
-        run2 = MlpRun(L, torch, dev, m2, d2, f2, FMT, HIST, "normal", 4, seed=4321 + rank)
-        if args.graph:
-            run2.capture()
-        k2 = max(3, min(args.steps, 100))
-        ms2 = max_over_ranks(timed_steps(torch, run2, k2, 3, flush, barrier)[0])
-        d2048 = {"value": flops_per_step(m2, d2, f2) * k2 * world / (ms2 / 1e3) / 1e12, "unit": "TFLOP/s",
-                 "ms_per_step": ms2 / k2, "steps": k2, "frac_of_fp8_peak": None,
-                 "config": workload(m2, d2, f2, FMT, HIST, "normal")}
-        d2048["frac_of_fp8_peak"] = d2048["value"] / world / fp8_peak
-        del run2
+    del run
+    torch.cuda.empty_cache()
 
+    # ---- the other workloads: the LN -> QKV forward alone (latency), the 4-layer d 768 and
+    # 12-layer d 2048 module stacks, and the d 2048 LayerNormMLP format / size sweep
+    config1 = None if args.no_config1 else run_config1(L, torch, dev, args, flush, fp8_peak, hbm)
+    stack768 = None if args.no_stack else run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local,
+                                                    rank, fp8_peak, hbm, 4, 8192, 768, 3072, 16, seed=768, k_max=50)
     stack = None if args.no_stack else run_stack(L, torch, dev, args, flush, barrier, max_over_ranks, world, local,
-                                                    rank, fp8_peak)
+                                                 rank, fp8_peak, hbm, args.stack_layers, 16384, 2048, 8192, 1024,
+                                                 seed=977)
+    sweep = None if args.no_sweep else run_sweep(L, torch, dev, args, flush, barrier, max_over_ranks, world, local,
+                                                 rank, fp8_peak)
 
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0
     cpu = None
@@ -767,10 +946,11 @@ def run_gpu(args):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)", "data": "synthetic",
-                "config": dict(workload(), cuda_graph=bool(args.graph)), "frac_of_fp8_peak": value / world / fp8_peak,
+                "config": dict(workload(n_sets=n_sets), cuda_graph=bool(args.graph)), "frac_of_fp8_peak": value / world / fp8_peak,
                 "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline,
-                "per_kernel": per_kernel, "hbm_peak_gbs": hbm, "cpu_baseline": cpu, "d2048": d2048,
-                "stack2048x12": stack}
+                "per_kernel": per_kernel, "hbm_peak_gbs": hbm, "cpu_baseline": cpu,
+                "config1_ln_linear_fwd": config1, "stack768x4": stack768, "stack2048x12": stack,
+                "sweep2048": sweep}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -786,8 +966,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512, help="tokens per oracle step of the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--no-d2048", action="store_true")
-    ap.add_argument("--no-stack", action="store_true", help="skip the 12-layer d 2048 stack step")
+    ap.add_argument("--no-config1", action="store_true", help="skip the LN -> QKV forward latency leg")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the d 2048 LayerNormMLP format / size sweep")
+    ap.add_argument("--no-stack", action="store_true", help="skip the d 768 and d 2048 module stack steps")
     ap.add_argument("--stack-only", action="store_true", help="run only the stack step (prints its own line)")
     ap.add_argument("--stack-layers", type=int, default=12)
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph (1) or call (0)")

@@ -50,6 +50,10 @@ bool pdl_enabled() {
   return on;
 }
 
+// Token counts up to which ln_linear_fwd's automatic choice takes the one-launch
+// fused path (when its other conditions hold).
+constexpr int64_t kFusedAutoMaxTokens = 0;
+
 // LNFP8_NO_PAIR=1 runs the FC2 data and weight gradients as two launches (for comparison)
 bool pair_disabled() {
   static const bool off = getenv("LNFP8_NO_PAIR") != nullptr;
@@ -253,7 +257,7 @@ extern "C" {
 
 const char* lnfp8_last_error(void) { return g_msg; }
 
-int lnfp8_version(void) { return 300; }
+int lnfp8_version(void) { return 400; }
 
 long long lnfp8_launch_count(void) { return g_launches.load(); }
 
@@ -546,6 +550,46 @@ int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F) {
                              gemm_plan(M, D, F, EPI_STORE, true), gemm_plan(F, D, M, EPI_STORE, true)});
 }
 
+int lnfp8_ctx_offsets(int op, int64_t M, int64_t D, int64_t F, int64_t* offsets, int max_offsets) {
+  if (M < 0 || D < 0 || F < 0 || !offsets) return -1;
+  int64_t sizes[8];
+  int n = 0;
+  if (op == LNFP8_OP_LN_LINEAR || op == LNFP8_OP_LINEAR) {
+    sizes[n++] = M * D;  // xq
+    sizes[n++] = F * D;  // wq
+    if (op == LNFP8_OP_LN_LINEAR) {
+      sizes[n++] = 4 * M;  // mu
+      sizes[n++] = 4 * M;  // rsigma
+    }
+    sizes[n++] = 4 * 2;  // sinv_saved
+  } else if (op == LNFP8_OP_LN_MLP) {
+    sizes[n++] = M * D;      // lnq
+    sizes[n++] = F * D;      // w1q
+    sizes[n++] = D * F;      // w2q
+    sizes[n++] = 2 * M * F;  // h
+    sizes[n++] = M * F;      // aq
+    sizes[n++] = 4 * M;      // mu
+    sizes[n++] = 4 * M;      // rsigma
+    sizes[n++] = 4 * 4;      // sinv_saved
+  } else {
+    return -1;
+  }
+  if (max_offsets < n + 1) return -1;
+  int64_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    offsets[i] = off;
+    off += (sizes[i] + 255) / 256 * 256;
+  }
+  offsets[n] = off;
+  return n;
+}
+
+int64_t lnfp8_ctx_bytes(int op, int64_t M, int64_t D, int64_t F) {
+  int64_t off[9];
+  const int n = lnfp8_ctx_offsets(op, M, D, F, off, 9);
+  return n < 0 ? -1 : off[n];
+}
+
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream stream) {
   const char* who = "ln_linear_fwd";
   clear_error();
@@ -583,6 +627,37 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
   }
   const int fdt = fwd_dtype(&a->recipe);
   const lnfp8_meta& m = a->meta;
+  if (a->path < LNFP8_PATH_AUTO || a->path > LNFP8_PATH_SEPARATE)
+    return set_error(LNFP8_ERR_INVALID_ARG, "%s: path = %d", who, a->path);
+  const bool fused_ok = a->residual == nullptr && ln_linear_small_fits(a->M, a->K, a->N);
+  if (a->path == LNFP8_PATH_FUSED && !fused_ok)
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "%s: the fused path needs 1 <= M, K <= 768 and no residual", who);
+  if (a->path == LNFP8_PATH_FUSED || (a->path == LNFP8_PATH_AUTO && fused_ok && a->M <= kFusedAutoMaxTokens)) {
+    SmallLinearArgs sa;
+    sa.M = a->M;
+    sa.N = a->N;
+    sa.K = a->K;
+    sa.x = a->x;
+    sa.gamma = a->gamma;
+    sa.beta = a->beta;
+    sa.eps = a->eps;
+    sa.w = w8 ? nullptr : a->w;
+    sa.wq_in = w8 ? a->wq : nullptr;
+    sa.bias = a->bias;
+    sa.y = a->y;
+    sa.xq = a->xq;
+    sa.wq = w8 ? nullptr : a->wq;
+    sa.mu = a->mu;
+    sa.rsigma = a->rsigma;
+    sa.ydbg = a->ln_out_debug;
+    sa.scale = m.scale;
+    sa.scale_inv = m.scale_inv;
+    sa.w_scale_inv = w8 ? a->w_scale_inv : nullptr;
+    sa.amax_cur = m.amax_cur;
+    TRY(ln_linear_small_launch(sa, fdt, st));
+    TRY(finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st));
+    return w8 ? save_weight_sinv(a->sinv_saved + 1, a->w_scale_inv, st) : LNFP8_OK;
+  }
   if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
   if (ln)
     TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,

@@ -315,6 +315,11 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -988,6 +993,7 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
 }
 
 #include "gemm_pair.cuh"
+#include "gemm_small.cuh"
 
 template <int BN, int EPI, int QDT>
 lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
@@ -999,6 +1005,49 @@ lnfp8_status launch_layouts(bool a_mn, bool b_mn, const CUtensorMap& ta, const C
 }
 
 }  // namespace
+
+bool ln_linear_small_fits(int64_t M, int64_t K, int64_t N) {
+  return M > 0 && M <= 0x7FFFFFFF && N > 0 && N <= 0x7FFFFFFF && K > 0 && K <= kSmallMaxK;
+}
+
+lnfp8_status ln_linear_small_launch(const SmallLinearArgs& a, int dtype, cudaStream_t st) {
+  if (!ln_linear_small_fits(a.M, a.K, a.N))
+    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_linear small path: M, N > 0 and K <= %d", kSmallMaxK);
+  SmallParams sp;
+  sp.M = (int)a.M;
+  sp.N = (int)a.N;
+  sp.K = (int)a.K;
+  sp.x = a.x;
+  sp.gamma = a.gamma;
+  sp.beta = a.beta;
+  sp.eps = a.eps;
+  sp.w = a.w;
+  sp.wq_in = a.wq_in;
+  sp.bias = a.bias;
+  sp.y = a.y;
+  sp.xq = a.xq;
+  sp.wq = a.wq;
+  sp.mu = a.mu;
+  sp.rsigma = a.rsigma;
+  sp.ydbg = a.ydbg;
+  sp.scale = a.scale;
+  sp.scale_inv = a.scale_inv;
+  sp.w_scale_inv = a.w_scale_inv;
+  sp.amax_cur = a.amax_cur;
+  sp.idesc = make_idesc(128, kSmallBN, dtype, dtype, false, false);
+  const int nv = (int)((a.K + 255) / 256);
+  const bool ln = a.gamma != nullptr;
+#define SMALL(NV)                                                                                  \
+  if (nv == NV) {                                                                                  \
+    if (dtype == LNFP8_E4M3) return ln ? small_launch_t<NV, LNFP8_E4M3, true>(sp, st) : small_launch_t<NV, LNFP8_E4M3, false>(sp, st); \
+    return ln ? small_launch_t<NV, LNFP8_E5M2, true>(sp, st) : small_launch_t<NV, LNFP8_E5M2, false>(sp, st); \
+  }
+  SMALL(1)
+  SMALL(2)
+  SMALL(3)
+#undef SMALL
+  return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_linear small path: K = %lld", (long long)a.K);
+}
 
 lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st) {
   LaunchScope ls("selftest_wait", st);

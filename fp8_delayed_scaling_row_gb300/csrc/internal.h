@@ -97,6 +97,33 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
 GemmPlan pair_plan(const GemmArgs& g1);
 
 lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st);
+
+// The LayerNormLinear / Linear forward of few tokens as one launch (K6,
+// gemm_small.cuh): LayerNorm (gamma non-NULL) or plain cast of x, the weight
+// cast (or FP8-stored codes wq_in), the GEMM, dequantisation and bias. Results
+// equal the separate launches' bit for bit; the state update is not included.
+struct SmallLinearArgs {
+  int64_t M, N, K;
+  const uint16_t* x;
+  const uint16_t* gamma;
+  const uint16_t* beta;
+  float eps;
+  const uint16_t* w;
+  const uint8_t* wq_in;
+  const uint16_t* bias;
+  uint16_t* y;
+  uint8_t* xq;
+  uint8_t* wq;
+  float* mu;
+  float* rsigma;
+  float* ydbg;
+  const float* scale;
+  const float* scale_inv;
+  const float* w_scale_inv;
+  float* amax_cur;
+};
+bool ln_linear_small_fits(int64_t M, int64_t K, int64_t N);
+lnfp8_status ln_linear_small_launch(const SmallLinearArgs& a, int dtype, cudaStream_t st);
 lnfp8_status selftest_timeout_launch(int64_t limit_ns, cudaStream_t st);
 
 }  // namespace lnfp8

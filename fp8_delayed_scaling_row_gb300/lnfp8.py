@@ -33,7 +33,9 @@ EXPORTED = [
     "fp8_quantize", "fp8_weight_quantize", "ln_fwd_cast", "ln_bwd", "fp8_gemm", "ln_linear_fwd", "ln_linear_bwd",
     "ln_linear_bwd_noalloc", "ln_mlp_fwd", "ln_mlp_bwd", "lnfp8_gemm_workspace_size",
     "lnfp8_ln_linear_bwd_workspace_size", "lnfp8_ln_mlp_bwd_workspace_size", "lnfp8_ln_mlp_fwd_workspace_size",
+    "lnfp8_ctx_bytes", "lnfp8_ctx_offsets",
 ]
+OP_LN_LINEAR, OP_LINEAR, OP_LN_MLP = 0, 1, 2
 
 
 class LnFp8Error(RuntimeError):
@@ -60,7 +62,10 @@ class CLnLinearFwd(C.Structure):
     _fields_ = [("M", _I64), ("K", _I64), ("N", _I64), ("x", _P), ("gamma", _P), ("beta", _P), ("eps", C.c_float),
                 ("w", _P), ("bias", _P), ("y", _P), ("xq", _P), ("wq", _P), ("mu", _P), ("rsigma", _P),
                 ("sinv_saved", _P), ("meta", CMeta), ("recipe", CRecipe), ("defer_update", C.c_int),
-                ("ln_out_debug", _P), ("w_scale_inv", _P), ("residual", _P), ("x_sum", _P)]
+                ("ln_out_debug", _P), ("w_scale_inv", _P), ("residual", _P), ("x_sum", _P), ("path", C.c_int)]
+
+
+PATH_AUTO, PATH_FUSED, PATH_SEPARATE = 0, 1, 2
 
 
 class CLnLinearBwd(C.Structure):
@@ -119,6 +124,8 @@ _c_gemm_ws = _sig("lnfp8_gemm_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_lin_bwd_ws = _sig("lnfp8_ln_linear_bwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_mlp_bwd_ws = _sig("lnfp8_ln_mlp_bwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
 _c_mlp_fwd_ws = _sig("lnfp8_ln_mlp_fwd_workspace_size", [_I64, _I64, _I64], C.c_int64)
+_c_ctx_bytes = _sig("lnfp8_ctx_bytes", [C.c_int, _I64, _I64, _I64], C.c_int64)
+_c_ctx_offsets = _sig("lnfp8_ctx_offsets", [C.c_int, _I64, _I64, _I64, C.POINTER(_I64), C.c_int], C.c_int)
 _c_lin_fwd = _sig("ln_linear_fwd", [C.POINTER(CLnLinearFwd), _P])
 _c_lin_bwd = _sig("ln_linear_bwd", [C.POINTER(CLnLinearBwd), _P])
 _c_lin_bwd_noalloc = _sig("ln_linear_bwd_noalloc", [C.POINTER(CLnLinearBwd), _P])
@@ -371,21 +378,53 @@ def _e(shape, dtype, dev):
     return torch.empty(shape, dtype=dtype, device=dev)
 
 
+def ctx_bytes(op: int, M: int, D: int, F: int) -> int:
+    return int(_c_ctx_bytes(op, M, D, F))
+
+
+def ctx_offsets(op: int, M: int, D: int, F: int) -> list:
+    """Start of each saved-context buffer, then the total (the library's layout)."""
+    off = (_I64 * 9)()
+    n = int(_c_ctx_offsets(op, M, D, F, off, 9))
+    if n < 0:
+        raise LnFp8Error(ERR_INVALID_ARG, f"lnfp8_ctx_offsets({op}, {M}, {D}, {F})")
+    return [int(off[i]) for i in range(n + 1)]
+
+
+def _carve(op, M, D, F, shapes, device):
+    """The saved context as views of one allocation laid out by lnfp8_ctx_offsets;
+    shapes: (shape, dtype) per buffer in the library's order."""
+    off = ctx_offsets(op, M, D, F)
+    buf = torch.empty(off[-1], dtype=torch.uint8, device=device)
+    views = []
+    for (shape, dtype), start in zip(shapes, off):
+        nbytes = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+        views.append(buf[start:start + nbytes].view(dtype).view(shape))
+    return buf, views
+
+
 def linear_ctx(M, K, N, *, ln=True, device="cuda", debug=False, weight_codes=True) -> LinearCtx:
-    return LinearCtx(xq=_e((M, K), torch.uint8, device),
-                     wq=_e((N, K), torch.uint8, device) if weight_codes else None,
-                     mu=_e((M,), torch.float32, device) if ln else None,
-                     rsigma=_e((M,), torch.float32, device) if ln else None,
-                     sinv_saved=_e((2,), torch.float32, device),
+    """Saved tensors of one LayerNormLinear / Linear forward, views of one allocation in
+    the library's saved-context layout (weight_codes=False leaves wq to an FP8Weight)."""
+    u8, f32 = torch.uint8, torch.float32
+    if ln:
+        _, (xq, wq, mu, rs, sinv) = _carve(OP_LN_LINEAR, M, K, N, [((M, K), u8), ((N, K), u8), ((M,), f32),
+                                                                   ((M,), f32), ((2,), f32)], device)
+    else:
+        _, (xq, wq, sinv) = _carve(OP_LINEAR, M, K, N, [((M, K), u8), ((N, K), u8), ((2,), f32)], device)
+        mu = rs = None
+    return LinearCtx(xq=xq, wq=wq if weight_codes else None, mu=mu, rsigma=rs, sinv_saved=sinv,
                      ln_out_debug=_e((M, K), torch.float32, device) if debug else None)
 
 
 def ln_linear_fwd(x, gamma, beta, w, bias, meta: ScalingMeta, recipe: Recipe, *, eps=1e-5, y=None,
-                  ctx: LinearCtx | None = None, defer_update=False, debug=False, residual=None, stream=None):
+                  ctx: LinearCtx | None = None, defer_update=False, debug=False, residual=None, path=PATH_AUTO,
+                  stream=None):
     """LayerNormLinear (gamma given) or Linear (gamma None) forward; returns (y, ctx).
     w is a bf16 weight (cast every call) or an FP8Weight (its codes are used as they are).
     residual: optional bf16 [M, K]; the input becomes h = bf16(x + residual), returned as
-    ctx.x_sum (pass it as the backward's x)."""
+    ctx.x_sum (pass it as the backward's x). path: PATH_AUTO, PATH_FUSED (one launch for
+    the LayerNorm, casts and GEMM; K <= 768) or PATH_SEPARATE."""
     M, K = x.shape
     N = w.shape[0]
     dev = x.device
@@ -402,7 +441,7 @@ def ln_linear_fwd(x, gamma, beta, w, bias, meta: ScalingMeta, recipe: Recipe, *,
                      mu=_ptr(ctx.mu), rsigma=_ptr(ctx.rsigma), sinv_saved=_ptr(ctx.sinv_saved), meta=meta.c(),
                      recipe=recipe.c(), defer_update=int(defer_update), ln_out_debug=_ptr(ctx.ln_out_debug),
                      w_scale_inv=_ptr(w.scale_inv) if w8 else None, residual=_ptr(residual),
-                     x_sum=_ptr(ctx.x_sum) if residual is not None else None)
+                     x_sum=_ptr(ctx.x_sum) if residual is not None else None, path=int(path))
     _check(_c_lin_fwd(C.byref(a), _stream(stream)))
     return y, ctx
 
@@ -479,11 +518,12 @@ def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False, weight_codes=Tr
     readiness counters with which the forward runs FC1 and FC2 as one launch (same
     results; at 8192 x 768 -> 3072 -> 768 the two launches are still faster).
     weight_codes=False leaves w1q/w2q to FP8-stored weights."""
-    return MlpCtx(lnq=_e((M, D), torch.uint8, device), mu=_e((M,), torch.float32, device),
-                  rsigma=_e((M,), torch.float32, device),
-                  w1q=_e((F, D), torch.uint8, device) if weight_codes else None,
-                  w2q=_e((D, F), torch.uint8, device) if weight_codes else None, h=_e((M, F), torch.bfloat16, device),
-                  aq=_e((M, F), torch.uint8, device), sinv_saved=_e((4,), torch.float32, device),
+    u8, f32 = torch.uint8, torch.float32
+    _, (lnq, w1q, w2q, h, aq, mu, rs, sinv) = _carve(
+        OP_LN_MLP, M, D, F, [((M, D), u8), ((F, D), u8), ((D, F), u8), ((M, F), torch.bfloat16), ((M, F), u8),
+                             ((M,), f32), ((M,), f32), ((4,), f32)], device)
+    return MlpCtx(lnq=lnq, mu=mu, rsigma=rs, w1q=w1q if weight_codes else None, w2q=w2q if weight_codes else None,
+                  h=h, aq=aq, sinv_saved=sinv,
                   ln_out_debug=_e((M, D), torch.float32, device) if debug else None,
                   act_debug=_e((M, F), torch.float32, device) if debug else None,
                   gemm_ws=_ws(ln_mlp_fwd_workspace_size(M, D, F), device) if fused else None)

@@ -102,7 +102,8 @@ const char* lnfp8_last_error(void);
  * call, LNFP8_ERR_CUDA on an asynchronous CUDA error, else LNFP8_OK. */
 lnfp8_status lnfp8_sync_status(lnfp8_stream stream);
 
-/* Library version, as major*10000 + minor*100 + patch. */
+/* Library version, as major*10000 + minor*100 + patch (400: the saved-context
+ * layout queries lnfp8_ctx_bytes / lnfp8_ctx_offsets). */
 int lnfp8_version(void);
 
 /* Diagnostic of the failure path: enqueues one kernel whose bounded mbarrier
@@ -282,7 +283,20 @@ typedef struct {
    * residual) and normalises. The backward takes x_sum as its x. */
   const uint16_t* residual;
   uint16_t* x_sum;
+  /* How the forward runs (results are the same bit for bit):
+   *   LNFP8_PATH_AUTO      the library's choice (the fused launch for few tokens)
+   *   LNFP8_PATH_FUSED     one launch computing the LayerNorm (or the input cast),
+   *                        the weight cast, the GEMM and the bias into its output
+   *                        tiles, the LayerNorm / cast fused into the GEMM's
+   *                        A-operand producer; then the state update. Needs
+   *                        M >= 1, K <= 768 and no residual, else
+   *                        LNFP8_ERR_UNSUPPORTED_SHAPE.
+   *   LNFP8_PATH_SEPARATE  the weight cast, the LayerNorm + cast, the GEMM and
+   *                        the state update as launches of their own. */
+  int path;
 } lnfp8_ln_linear_fwd_args;
+
+enum { LNFP8_PATH_AUTO = 0, LNFP8_PATH_FUSED = 1, LNFP8_PATH_SEPARATE = 2 };
 
 typedef struct {
   int64_t M, K, N;
@@ -320,7 +334,10 @@ typedef struct {
  * into the LayerNorm kernel and written to x_sum. */
 lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* args, lnfp8_stream stream);
 
-/* LayerNormLinear backward: dyq = fp8(dy * gscale[0]) (E5M2 under HYBRID);
+/* LayerNormLinear backward (TE tutorial, code block 3: loss.backward() through
+ * the modules under fp8_autocast; Turbo-charging guide, "Playing with
+ * lower-precision formats: BF16 vs FP8": gradients go back to BF16/FP32 for
+ * the optimizer): dyq = fp8(dy * gscale[0]) (E5M2 under HYBRID);
  * dbias = sum_rows dy; dln = (dyq . wq) * (gscale_inv[0] * sinv_saved[1]);
  * dw = (dyq^T . xq) * (gscale_inv[0] * sinv_saved[0]); dx = LN backward of dln
  * (dx = dln without LayerNorm); then the backward state update. */
@@ -451,7 +468,10 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* args, lnfp8_stream stream);
  * results are identical. */
 int64_t lnfp8_ln_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t F);
 
-/* LayerNormMLP backward (gradients E5M2 under HYBRID):
+/* LayerNormMLP backward (TE tutorial, code block 3: loss.backward() through
+ * te.LayerNormMLP under fp8_autocast; Turbo-charging guide, "Playing with
+ * lower-precision formats: BF16 vs FP8": HYBRID mixes E4M3 and E5M2, so the
+ * gradients are cast to E5M2, and they come back in BF16/FP32):
  *   dyq = fp8(dy * gscale[0]); db2 = sum_rows dy;
  *   dh = (dyq . w2q) * gsinv[0]*sinv[3] * gelu'(h) (fp32); dhq = fp8(dh * gscale[1]);
  *   db1 = sum_rows dh; dw2 = (dyq^T . aq) * gsinv[0]*sinv[2];
@@ -464,6 +484,37 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* args, lnfp8_stream stream);
  * none would split, -1 for negative sizes. As for ln_linear_bwd, a smaller or
  * NULL workspace runs them unsplit. */
 int64_t lnfp8_ln_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t F);
+
+/* The saved context ---------------------------------------------------------
+ * What a forward keeps for its backward: the state of the module between
+ * `m(x)` and `loss.backward()` (TE tutorial, code blocks 1 and 3: the module
+ * call and the backward under fp8_autocast; code block 4: the FP8 codes are
+ * cast with the scales kept in fp8_meta). The caller owns it; these queries
+ * give one layout for it, so that it can live in a single allocation: the
+ * buffers in the order listed, each starting at a multiple of 256 bytes.
+ *   LNFP8_OP_LN_LINEAR (in features D, out features F; ln_linear_* with gamma)
+ *     0 xq [M, D] u8, 1 wq [F, D] u8, 2 mu [M] f32, 3 rsigma [M] f32,
+ *     4 sinv_saved [2] f32
+ *   LNFP8_OP_LINEAR (ln_linear_* without LayerNorm)
+ *     0 xq [M, D] u8, 1 wq [F, D] u8, 2 sinv_saved [2] f32
+ *   LNFP8_OP_LN_MLP (hidden D, FFN width F)
+ *     0 lnq [M, D] u8, 1 w1q [F, D] u8, 2 w2q [D, F] u8, 3 h [M, F] bf16,
+ *     4 aq [M, F] u8, 5 mu [M] f32, 6 rsigma [M] f32, 7 sinv_saved [4] f32
+ * (x, or x_sum after a fused residual add, is the caller's input tensor and
+ * is not part of it; nor are the backward's workspaces dyq, dhq, dln.) */
+typedef enum { LNFP8_OP_LN_LINEAR = 0, LNFP8_OP_LINEAR = 1, LNFP8_OP_LN_MLP = 2 } lnfp8_op;
+
+/* Total bytes of the saved context of `op` (the end of its last buffer,
+ * rounded up to 256);
+ * -1 for an unknown op or a negative size. */
+int64_t lnfp8_ctx_bytes(int op, int64_t M, int64_t D, int64_t F);
+
+/* Byte offsets of the saved context's buffers: offsets (host array of
+ * max_offsets entries) receives the start of each buffer in the order above,
+ * then the total. Returns the number of buffers (5, 3 or 8), or -1 for an
+ * unknown op, a negative size, a NULL offsets or max_offsets smaller than
+ * that number plus one. */
+int lnfp8_ctx_offsets(int op, int64_t M, int64_t D, int64_t F, int64_t* offsets, int max_offsets);
 
 #ifdef __cplusplus
 }

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.version() == 300
+    assert lib.version() == 400
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
@@ -152,3 +152,22 @@ def test_update_many_and_new_entry_points_reject_bad_arguments(lib):
     # FP8 weights of an MLP come in pairs
     m = _mlp_args(lib, w1_scale_inv=FAKE)
     assert lib._c_mlp_fwd(ctypes.byref(m), None) == 1 and "together" in lib.last_error()
+
+
+def test_saved_context_layout_by_hand(lib):
+    # LayerNormMLP, M = 300 tokens, D = 64, F = 128: lnq 19200 B, w1q 8192, w2q 8192, h 76800, aq 38400,
+    # mu 1200, rsigma 1200, sinv 16; each starts at a multiple of 256
+    off = lib.ctx_offsets(lib.OP_LN_MLP, 300, 64, 128)
+    sizes = [19200, 8192, 8192, 76800, 38400, 1200, 1200, 16]
+    want, o = [], 0
+    for n in sizes:
+        want.append(o)
+        o += (n + 255) // 256 * 256
+    assert off == want + [o] and lib.ctx_bytes(lib.OP_LN_MLP, 300, 64, 128) == o == 153600
+    # LayerNormLinear 768 -> 2304 over 256 tokens: xq, wq, mu, rsigma, sinv
+    assert lib.ctx_offsets(lib.OP_LN_LINEAR, 256, 768, 2304) == [0, 196608, 196608 + 1769472, 196608 + 1769472 + 1024,
+                                                               196608 + 1769472 + 2048, 196608 + 1769472 + 2304]
+    assert lib.ctx_offsets(lib.OP_LINEAR, 0, 16, 32) == [0, 0, 512, 768]
+    assert lib.ctx_bytes(5, 1, 16, 16) == -1 and lib.ctx_bytes(lib.OP_LN_MLP, 1, -16, 16) == -1
+    with pytest.raises(lib.LnFp8Error):
+        lib.ctx_offsets(9, 1, 16, 16)

@@ -18,7 +18,13 @@ PROGRAM = r"""
 #define CHECK(c) do { if (!(c)) { printf("FAIL line %d: %s\n", __LINE__, #c); return 1; } } while (0)
 
 int main(void) {
-  CHECK(lnfp8_version() == 300);
+  CHECK(lnfp8_version() == 400);
+  /* the saved-context layout: buffers at multiples of 256 bytes, then the total */
+  int64_t off[9];
+  CHECK(lnfp8_ctx_offsets(LNFP8_OP_LN_MLP, 300, 64, 128, off, 9) == 8);
+  CHECK(off[0] == 0 && off[1] == 19200 && off[2] == 19200 + 8192 && off[8] == lnfp8_ctx_bytes(LNFP8_OP_LN_MLP, 300, 64, 128));
+  CHECK(lnfp8_ctx_offsets(LNFP8_OP_LN_MLP, 300, 64, 128, off, 8) == -1);
+  CHECK(lnfp8_ctx_bytes(7, 1, 16, 16) == -1 && lnfp8_ctx_bytes(LNFP8_OP_LINEAR, -1, 16, 16) == -1);
   /* size queries: pure host arithmetic */
   CHECK(lnfp8_ln_mlp_fwd_workspace_size(8192, 768, 3072) == 256);
   CHECK(lnfp8_ln_mlp_fwd_workspace_size(0, 768, 3072) == 0);

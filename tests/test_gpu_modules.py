@@ -217,7 +217,7 @@ def test_mlp_d2048_sampled_rows(L):
 
 
 # ------------------------------------------------------------------ LayerNormLinear / Linear
-def run_linear(L, M, K, N, steps, ln=True, fmt="hybrid", hist=16, bias_std=0.02, seed=21):
+def run_linear(L, M, K, N, steps, ln=True, fmt="hybrid", hist=16, bias_std=0.02, seed=21, path=0):
     rec = L.Recipe(fmt, hist)
     orec = ORecipe(fmt, hist)
     p = synth.linear_params(N, K, ln=ln, bias_std=bias_std, seed=seed)
@@ -231,7 +231,7 @@ def run_linear(L, M, K, N, steps, ln=True, fmt="hybrid", hist=16, bias_std=0.02,
         dy = synth.grad(M, N, seed=seed, step=step)
         xt = bf16_dev(x)
         fpre, bpre = _state_from_gpu(fm), _state_from_gpu(bm)
-        y, ctx = L.ln_linear_fwd(xt, gma, bta, w, b, fm, rec, debug=ln)
+        y, ctx = L.ln_linear_fwd(xt, gma, bta, w, b, fm, rec, debug=ln, path=path)
         g = L.ln_linear_bwd(bf16_dev(dy), xt, gma, ctx, bm, rec)
         L.sync_status()
         _assert_state_equal(fm, _teacher_forced(fpre, fm, [ffmt] * 2), f"fwd {step}")
@@ -256,9 +256,17 @@ def run_linear(L, M, K, N, steps, ln=True, fmt="hybrid", hist=16, bias_std=0.02,
     return fm, bm
 
 
-def test_linear_config1_qkv_forward_e4m3(L):
-    # LayerNormLinear 768 -> 2304 over 256 tokens (8 x 32), E4M3, history 16, one step, bias 0
-    run_linear(L, M=256, K=768, N=2304, steps=1, fmt="e4m3", bias_std=0.0, seed=1234)
+@pytest.mark.parametrize("path", [1, 2])
+def test_linear_config1_qkv_forward_e4m3(L, path):
+    # LayerNormLinear 768 -> 2304 over 256 tokens (8 x 32), E4M3, history 16, one step, bias 0;
+    # the one-launch fused forward (path 1) and the separate launches (path 2)
+    run_linear(L, M=256, K=768, N=2304, steps=1, fmt="e4m3", bias_std=0.0, seed=1234, path=path)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_linear_small_multistep_both_paths(L, path):
+    run_linear(L, M=100, K=192, N=400, steps=3, hist=2, path=path)
+    run_linear(L, M=70, K=256, N=128, steps=2, ln=False, path=path)
 
 
 def test_linear_with_ln_multistep_ragged(L):
