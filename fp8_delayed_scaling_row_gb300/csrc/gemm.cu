@@ -609,6 +609,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     for (int u = u0; u < num_units; u += 2 * ncl) {
       const int m_blk = unit_m(u), n_blk = unit_n(u);
       const int sp = u % S;
+      // this warp's half of the tile's bias, 4 columns per lane, requested before the
+      // accumulator wait so that its latency is hidden; chunks take it by shuffles
+      uint2 btile = make_uint2(0u, 0u);
+      if constexpr (EPI != EPI_DGELU) {
+        const int64_t c = (int64_t)n_blk * BN + half * HALF_COLS + lane * 4;
+        if (p.bias && lane * 4 < HALF_COLS && c < p.N) btile = __ldg(reinterpret_cast<const uint2*>(p.bias + c));
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       const int64_t m = (int64_t)m_blk * BM + quarter * 32 + r;
@@ -667,12 +674,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int col0 = half * HALF_COLS + ch * 32;
         const int64_t n0 = (int64_t)n_blk * BN + col0;
         uint32_t rr[32];
-        uint4 bias8[4];  // this chunk's bias, requested before the tensor-memory load
+        uint4 bias8[4];  // this chunk's bias: columns 8g..8g+7 come from lanes 8ch + 2g and 8ch + 2g + 1
         if constexpr (EPI != EPI_DGELU) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            bias8[g] = p.bias && n0 + g * 8 < p.N ? __ldg(reinterpret_cast<const uint4*>(p.bias + n0 + g * 8))
-                                                   : make_uint4(0u, 0u, 0u, 0u);
+          for (int g = 0; g < 4; ++g) {
+            const int l0 = ch * 8 + 2 * g;
+            bias8[g] = make_uint4(__shfl_sync(0xFFFFFFFFu, btile.x, l0), __shfl_sync(0xFFFFFFFFu, btile.y, l0),
+                                  __shfl_sync(0xFFFFFFFFu, btile.x, l0 + 1), __shfl_sync(0xFFFFFFFFu, btile.y, l0 + 1));
+          }
         }
         if (p.num_kb > 0) {
           tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + col0), rr);

@@ -69,17 +69,22 @@ __device__ __forceinline__ uint32_t panel_off(int r, int c) {
 // One row of A (LayerNorm + cast, or the plain cast) or B (the weight cast): each
 // lane takes the 8-element chunks lane, lane + 32, ... (the LayerNorm kernel's
 // warp-per-row order), writes its codes into the panel, and returns its amax.
-template <int NV, int DT, bool LN>
-__device__ __forceinline__ float small_row(const uint16_t* __restrict__ src, bool row_ok, int K, int kpad,
-                                           const uint4* sgb, int nvec, float eps, float inv_k, float s,
-                                           uint8_t* panel, int r, uint8_t* gcodes, float* ydbg, float* mu_out,
-                                           float* rs_out, int lane) {
-  uint4 raw[NV];
+template <int NV>
+__device__ __forceinline__ void small_load(uint4 (&raw)[NV], const uint16_t* __restrict__ src, bool row_ok, int K,
+                                           int lane) {
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     const int c = (lane + 32 * j) * 8;
     raw[j] = row_ok && c < K ? __ldg(reinterpret_cast<const uint4*>(src + c)) : make_uint4(0u, 0u, 0u, 0u);
   }
+}
+
+// processes a row whose chunks small_load fetched
+template <int NV, int DT, bool LN>
+__device__ __forceinline__ float small_row(const uint4 (&raw)[NV], bool row_ok, int K, int kpad,
+                                           const uint4* sgb, int nvec, float eps, float inv_k, float s,
+                                           uint8_t* panel, int r, uint8_t* gcodes, float* ydbg, float* mu_out,
+                                           float* rs_out, int lane) {
   uint64_t v2[NV][4];
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
@@ -197,38 +202,50 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ln_linear_small_kernel(const
   const bool first_n = n_blk == 0, first_m = m_blk == 0;
   const bool w8 = p.wq_in != nullptr;
 
-  // ---- A: this tile's 128 token rows
-  float am_a = 0.f;
-  const float sx = p.scale[0];
-  for (int r = warp; r < 128; r += kSmallThreads / 32) {
-    const int64_t m = (int64_t)m_blk * 128 + r;
-    const bool row_ok = m < p.M;
-    const int64_t mr = row_ok ? m : 0;
-    am_a = nanmax(am_a, small_row<NV, DT, LN>(p.x + mr * p.K, row_ok, p.K, kpad, sgb, nvec, p.eps, inv_k, sx, sa, r,
-                                             first_n && row_ok ? p.xq + mr * p.K : nullptr,
-                                             first_n && row_ok && p.ydbg ? p.ydbg + mr * p.K : nullptr,
-                                             first_n && LN ? p.mu + mr : nullptr, first_n && LN ? p.rsigma + mr : nullptr,
-                                             lane));
-  }
-  // ---- B: this tile's 128 weight rows (cast, or the stored codes)
-  float am_w = 0.f;
-  const float sw = p.scale[1];
-  for (int r = warp; r < 128; r += kSmallThreads / 32) {
-    const int64_t n = (int64_t)n_blk * kSmallBN + r;
-    const bool row_ok = n < p.N;
-    const int64_t nr = row_ok ? n : 0;
-    if (!w8) {
-      am_w = nanmax(am_w, small_row<NV, DT, false>(p.w + nr * p.K, row_ok, p.K, kpad, sgb, nvec, p.eps, inv_k, sw, sb,
-                                                  r, first_m && row_ok ? p.wq + nr * p.K : nullptr, nullptr, nullptr,
-                                                  nullptr, lane));
-    } else {
+  // ---- A (this tile's 128 token rows) and B (its 128 weight rows, cast or stored codes):
+  // warp w takes rows w, w + 16, ... of each; every iteration has two A rows and two B
+  // rows in flight before any is reduced, so the loads' latency overlaps
+  float am_a = 0.f, am_w = 0.f;
+  const float sx = p.scale[0], sw = p.scale[1];
+  constexpr int kWarps = kSmallThreads / 32;
+  for (int r0 = warp; r0 < 128; r0 += 2 * kWarps) {
+    uint4 ra[2][NV], rb[2][NV];
+    int64_t ma[2], nb[2];
+    bool oka[2], okb[2];
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const int c = (lane + 32 * j) * 8;
-        if (c >= kpad) continue;
-        uint2 q = make_uint2(0u, 0u);
-        if (row_ok && c < p.K) q = __ldg(reinterpret_cast<const uint2*>(p.wq_in + nr * p.K + c));
-        *reinterpret_cast<uint2*>(sb + panel_off(r, c)) = q;
+    for (int i = 0; i < 2; ++i) {
+      const int r = r0 + i * kWarps;
+      ma[i] = (int64_t)m_blk * 128 + r;
+      oka[i] = ma[i] < p.M;
+      if (!oka[i]) ma[i] = 0;
+      small_load<NV>(ra[i], p.x + ma[i] * p.K, oka[i], p.K, lane);
+      nb[i] = (int64_t)n_blk * kSmallBN + r;
+      okb[i] = nb[i] < p.N;
+      if (!okb[i]) nb[i] = 0;
+      if (!w8) small_load<NV>(rb[i], p.w + nb[i] * p.K, okb[i], p.K, lane);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = r0 + i * kWarps;
+      const int64_t m = ma[i];
+      am_a = nanmax(am_a, small_row<NV, DT, LN>(ra[i], oka[i], p.K, kpad, sgb, nvec, p.eps, inv_k, sx, sa, r,
+                                                first_n && oka[i] ? p.xq + m * p.K : nullptr,
+                                                first_n && oka[i] && p.ydbg ? p.ydbg + m * p.K : nullptr,
+                                                first_n && LN ? p.mu + m : nullptr,
+                                                first_n && LN ? p.rsigma + m : nullptr, lane));
+      if (!w8) {
+        am_w = nanmax(am_w, small_row<NV, DT, false>(rb[i], okb[i], p.K, kpad, sgb, nvec, p.eps, inv_k, sw, sb, r,
+                                                     first_m && okb[i] ? p.wq + nb[i] * p.K : nullptr, nullptr,
+                                                     nullptr, nullptr, lane));
+      } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int c = (lane + 32 * j) * 8;
+          if (c >= kpad) continue;
+          uint2 q = make_uint2(0u, 0u);
+          if (okb[i] && c < p.K) q = __ldg(reinterpret_cast<const uint2*>(p.wq_in + nb[i] * p.K + c));
+          *reinterpret_cast<uint2*>(sb + panel_off(r, c)) = q;
+        }
       }
     }
   }
