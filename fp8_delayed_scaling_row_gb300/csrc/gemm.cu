@@ -674,15 +674,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int col0 = half * HALF_COLS + ch * 32;
         const int64_t n0 = (int64_t)n_blk * BN + col0;
         uint32_t rr[32];
-        uint4 bias8[4];  // this chunk's bias: columns 8g..8g+7 come from lanes 8ch + 2g and 8ch + 2g + 1
-        if constexpr (EPI != EPI_DGELU) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int l0 = ch * 8 + 2 * g;
-            bias8[g] = make_uint4(__shfl_sync(0xFFFFFFFFu, btile.x, l0), __shfl_sync(0xFFFFFFFFu, btile.y, l0),
-                                  __shfl_sync(0xFFFFFFFFu, btile.x, l0 + 1), __shfl_sync(0xFFFFFFFFu, btile.y, l0 + 1));
-          }
-        }
         if (p.num_kb > 0) {
           tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + col0), rr);
         } else {
@@ -720,9 +711,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           if (ch + 1 < CHUNKS) issue_h(u, ch + 1);
           else if (u + 2 * ncl < num_units) issue_h(u + 2 * ncl, 0);
         }
+        // the previous chunk's TMA stores have read the staging boxes: each 8-column group
+        // below writes its results into them as soon as they are computed
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
         float v[32];
-        uint4 ob[4];  // bf16 output row chunk
-        uint2 oq[4];  // FP8 output row chunk
         const bool full = row_ok && n0 + 32 <= p.N;  // every element of this chunk is inside the tensor
         const uint64_t s2 = f2(s, s);
 #pragma unroll
@@ -734,13 +727,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           for (int i = 0; i < 4; ++i) e2[i] = f2(__uint_as_float(rr[g * 8 + 2 * i]), __uint_as_float(rr[g * 8 + 2 * i + 1]));
           uint64_t b2[4] = {0ull, 0ull, 0ull, 0ull};
           if constexpr (EPI != EPI_DGELU) {
-            {
-              const uint4 bu = bias8[g];
-              b2[0] = bf2_to_f2(bu.x);
-              b2[1] = bf2_to_f2(bu.y);
-              b2[2] = bf2_to_f2(bu.z);
-              b2[3] = bf2_to_f2(bu.w);
-            }
+            // this group's bias: columns 8g..8g+7 of the chunk sit in lanes 8ch + 2g and 8ch + 2g + 1
+            const int l0 = ch * 8 + 2 * g;
+            b2[0] = bf2_to_f2(__shfl_sync(0xFFFFFFFFu, btile.x, l0));
+            b2[1] = bf2_to_f2(__shfl_sync(0xFFFFFFFFu, btile.y, l0));
+            b2[2] = bf2_to_f2(__shfl_sync(0xFFFFFFFFu, btile.x, l0 + 1));
+            b2[3] = bf2_to_f2(__shfl_sync(0xFFFFFFFFu, btile.y, l0 + 1));
           }
           if constexpr (EPI == EPI_STORE) {
             uint32_t w[4];
@@ -749,7 +741,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               const uint64_t y = fma2(e2[i], s2, b2[i]);
               w[i] = pack_bf16x2(lo(y), hi(y));
             }
-            ob[g] = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(so + sw64(r, g)) = make_uint4(w[0], w[1], w[2], w[3]);
           } else if constexpr (EPI == EPI_GELU) {
             // h = bf16(acc * s + b); a = h/2 * (1 + tanh(h * (k + k c h^2)))
             const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC), H2 = f2(0.5f, 0.5f);
@@ -774,10 +766,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 d4[1] = make_float4(lo(a2[2]), hi(a2[2]), lo(a2[3]), hi(a2[3]));
               }
             }
-            ob[g] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(so + sw64(r, g)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             const uint64_t q2 = f2(scale_q, scale_q);
-            oq[g].x = (uint32_t)cvt_pair<QDT>(mul2(a2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[1], q2)) << 16);
-            oq[g].y = (uint32_t)cvt_pair<QDT>(mul2(a2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[3], q2)) << 16);
+            *reinterpret_cast<uint2*>(sq + sw32(r, g >> 1) + (g & 1) * 8) =
+                make_uint2((uint32_t)cvt_pair<QDT>(mul2(a2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[1], q2)) << 16),
+                           (uint32_t)cvt_pair<QDT>(mul2(a2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[3], q2)) << 16));
           } else {  // EPI_DGELU
             // dh = (acc * s) * gelu'(h), gelu'(h) = (1+t)/2 + h/2 (1 - t^2) (k + 3 k c h^2)
             const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC);
@@ -796,8 +789,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               d2[i] = mul2(mul2(e2[i], s2), gp);
             }
             const uint64_t q2 = f2(scale_q, scale_q);
-            oq[g].x = (uint32_t)cvt_pair<QDT>(mul2(d2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[1], q2)) << 16);
-            oq[g].y = (uint32_t)cvt_pair<QDT>(mul2(d2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[3], q2)) << 16);
+            *reinterpret_cast<uint2*>(sq + sw32(r, g >> 1) + (g & 1) * 8) =
+                make_uint2((uint32_t)cvt_pair<QDT>(mul2(d2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[1], q2)) << 16),
+                           (uint32_t)cvt_pair<QDT>(mul2(d2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(d2[3], q2)) << 16));
             if (full || ok) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(d2[i])), hi(d2[i]));
@@ -814,18 +808,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
           }
         }
-        // stage the 32 x 32 results in swizzled shared memory, then one TMA
-        // store per box (rows past M and columns past N are clipped by TMA)
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
-        if constexpr (EPI != EPI_DGELU) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(so + sw64(r, j)) = ob[j];
-        }
-        if constexpr (EPI != EPI_STORE) {
-          *reinterpret_cast<uint4*>(sq + sw32(r, 0)) = make_uint4(oq[0].x, oq[0].y, oq[1].x, oq[1].y);
-          *reinterpret_cast<uint4*>(sq + sw32(r, 1)) = make_uint4(oq[2].x, oq[2].y, oq[3].x, oq[3].y);
-        }
+        // one TMA store per box (rows past M and columns past N are clipped by TMA)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {

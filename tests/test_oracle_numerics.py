@@ -113,9 +113,19 @@ def test_gemm_equals_brute_force_on_exact_inputs(fa, fb):
     assert np.array_equal(c, (av.astype(np.float64) @ bv.T.astype(np.float64)) * 0.125 + bias)
 
 
-def test_gemm_dequant_scale_is_a_fp32_product():
-    s = gemm.dequant_scale(np.float32(1 / 3), np.float32(1 / 7))
-    assert s.dtype == np.float32 and s == np.float32(np.float32(1 / 3) * np.float32(1 / 7))
+def test_gemm_dequant_factor_is_the_fp32_rounded_product():
+    """The two scale_inv are multiplied in fp32 before the product is scaled (the
+    state is fp32). 3 * fp32(1/3) is exactly 1 + 2^-25; in fp32 that rounds to
+    1.0 (less than half an ulp away), in fp64 it stays above 1.
+    A 1 x 1 GEMM of the codes of 1.0 then gives exactly 1.0 only if the factor is
+    the fp32-rounded product."""
+    from fractions import Fraction
+    third = np.float32(1 / 3)
+    exact = Fraction(3) * Fraction(float(third))
+    assert exact == 1 + Fraction(1, 2 ** 25)  # below half an ulp (2^-24) of 1.0 in fp32
+    one = fp8.encode(np.array([[1.0]], np.float32), fp8.E4M3)
+    c = gemm.fp8_gemm(one, fp8.E4M3, one, fp8.E4M3, np.float32(3.0), third)
+    assert c[0, 0] == 1.0 and float(exact) != 1.0
 
 
 def test_bf16_rounding_matches_torch():
