@@ -115,6 +115,34 @@ __device__ __forceinline__ float group_sum(float v, float* xch) {
   }
 }
 
+// Two independent sums over the TPR threads of a row group in one exchange round
+// (each added in the same order as group_sum would). `xch` holds 2 * kThreads/32 floats.
+template <int TPR>
+__device__ __forceinline__ float2 group_sum2(float a, float b, float* xch) {
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if constexpr (TPR == 32) {
+    return make_float2(a, b);
+  } else {
+    const int warp = threadIdx.x >> 5;
+    const int group = threadIdx.x / TPR;
+    constexpr int WPG = TPR / 32;
+    if ((threadIdx.x & 31) == 0) {
+      xch[2 * warp] = a;
+      xch[2 * warp + 1] = b;
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(TPR) : "memory");
+    float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int w = 0; w < WPG; ++w) {
+      sa += xch[2 * (group * WPG + w)];
+      sb += xch[2 * (group * WPG + w) + 1];
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(TPR) : "memory");
+    return make_float2(sa, sb);
+  }
+}
+
 // RES: the row is h = bf16(x + resid) (a residual add fused ahead of the
 // LayerNorm); h is written to hsum (the new residual stream, which the backward
 // reads as its x) and normalised.
@@ -268,7 +296,7 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
               float* dgamma, float* dbeta) {
   constexpr int RING = bwd_ring(NV);
   constexpr int P = RING - 2;  // rows in flight ahead of the one being processed
-  __shared__ float xch[kThreads / 32];
+  __shared__ float xch[2 * (kThreads / 32)];
   // [2][D] block partials of dgamma, dbeta; gamma [D/8 uint4] bf16; the ring of x and dY chunks
   // [RING][2 NV][kThreads] uint4; then the ring of mu, rsigma [RING][2][kThreads] fp32
   extern __shared__ float colred[];
@@ -347,8 +375,9 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     }
     slot = slot + 1 == RING ? 0 : slot + 1;
     const float2 s1p = up2(s1), s2p = up2(s2);
-    const float mean_g = group_sum<TPR>(s1p.x + s1p.y, xch) * inv_d;
-    const float mean_gx = group_sum<TPR>(s2p.x + s2p.y, xch) * inv_d;
+    const float2 sums = group_sum2<TPR>(s1p.x + s1p.y, s2p.x + s2p.y, xch);
+    const float mean_g = sums.x * inv_d;
+    const float mean_gx = sums.y * inv_d;
     if (!active) continue;
     const uint64_t mg2 = pk2(mean_g, mean_g), nmgx2 = pk2(-mean_gx, -mean_gx);
 #pragma unroll
