@@ -728,8 +728,13 @@ lnfp8_status ln_linear_bwd(const lnfp8_ln_linear_bwd_args* a, lnfp8_stream strea
     TRY(gemm_launch(dg, st));
     TRY(wgrad(wg, a->dw, st));
   }
-  if (ln) TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st, false));
-  return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
+  bool updated = false;
+  if (ln) {
+    const UpdateJob job = update_job(&m, mask_all(m.n, bdt), a->recipe.margin);
+    TRY(ln_bwd_launch(dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->K, a->dx, a->dgamma, a->dbeta, st, false,
+                      a->defer_update ? nullptr : &job, &updated));
+  }
+  return updated ? LNFP8_OK : finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
 }
 
 lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
@@ -889,8 +894,12 @@ lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {
     TRY(gemm_launch(d1, st));
     TRY(wgrad(w1, a->dw1, st));
   }
-  TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st, false));
-  return finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
+  // the state update rides in extra CTAs of the LayerNorm backward, the last kernel
+  const UpdateJob job = update_job(&m, mask_all(m.n, bdt), a->recipe.margin);
+  bool updated = false;
+  TRY(ln_bwd_launch(a->dln, a->x, a->gamma, a->mu, a->rsigma, a->M, a->D, a->dx, a->dgamma, a->dbeta, st, false,
+                    a->defer_update ? nullptr : &job, &updated));
+  return updated ? LNFP8_OK : finish_state(&m, &a->recipe, bdt, nullptr, a->defer_update, st);
 }
 
 }  // extern "C"

@@ -1086,8 +1086,10 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int epi, bool may_split, boo
   }
   // without a split, 128-wide single-SM tiles when 256-wide ones leave most SMs idle
   if (pl.splits == 1 && epi == EPI_STORE && num_m * ((N + 255) / 256) < (int64_t)num_sms()) pl.bn = 128;
-  // 192-wide pair tiles (A and B K-major, N a multiple of 192) when their rounds of 3/4-size tiles take less time
-  if (pl.splits == 1 && pl.bn == 256 && epi == EPI_STORE && kmajor && N % 192 == 0) {
+  // 192-wide pair tiles (A and B K-major, N a multiple of 192) when their rounds of 3/4-size tiles take less
+  // time: e.g. 8192 x 3072 has 384 tiles of 256 x 256 on 76 pairs (six rounds, the last with four tiles) and
+  // 512 of 256 x 192 (seven rounds of 3/4 the work each)
+  if (pl.splits == 1 && pl.bn == 256 && (epi == EPI_STORE || epi == EPI_GELU) && kmajor && N % 192 == 0) {
     const int64_t r256 = (tiles + clusters - 1) / clusters, r192 = (num_m2 * (N / 192) + clusters - 1) / clusters;
     if (4 * 3 * r192 < 4 * 4 * r256 * 9 / 10) pl.bn = 192;
   }
@@ -1167,6 +1169,10 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
     return launch_layouts<128, EPI_STORE, LNFP8_E4M3>(a_mn, b_mn, ta, tb, em, kp, st);
   }
   if (g.epi == EPI_GELU && !a_mn && !b_mn) {
+    if (bn == 192) {
+      if (g.q_dtype == LNFP8_E4M3) return launch_t<192, false, false, EPI_GELU, LNFP8_E4M3>(ta, tb, em, kp, st);
+      return launch_t<192, false, false, EPI_GELU, LNFP8_E5M2>(ta, tb, em, kp, st);
+    }
     if (g.q_dtype == LNFP8_E4M3) return launch_t<256, false, false, EPI_GELU, LNFP8_E4M3>(ta, tb, em, kp, st);
     return launch_t<256, false, false, EPI_GELU, LNFP8_E5M2>(ta, tb, em, kp, st);
   }

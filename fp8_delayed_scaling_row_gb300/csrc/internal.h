@@ -20,6 +20,20 @@ lnfp8_status update_many_launch(const lnfp8_meta* const* metas, const uint64_t* 
 lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, float* sinv_before,
                            cudaStream_t st);
 
+// One tensor set's state update carried by `n` extra CTAs at the front of the
+// grid of a call's last kernel (n = 0: none). Those CTAs start after every
+// earlier kernel of the stream has finished, so the amaxes are final and no
+// later kernel of the call reads the scales they write.
+struct UpdateJob {
+  float* scale;
+  float* scale_inv;
+  float* hist;
+  float* cur;
+  uint64_t e5m2_mask;
+  int n, L, margin;
+};
+UpdateJob update_job(const lnfp8_meta* m, uint64_t e5m2_mask, int margin);
+
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st, bool clear_colsum = true);
@@ -39,7 +53,8 @@ lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint1
                            const uint16_t* resid = nullptr, uint16_t* hsum = nullptr);
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
-                           float* dbeta, cudaStream_t st, bool clear = true);
+                           float* dbeta, cudaStream_t st, bool clear = true,
+                           const UpdateJob* job = nullptr, bool* job_done = nullptr);
 
 // Epilogues of the FP8 GEMM.
 enum GemmEpilogue {

@@ -19,11 +19,15 @@
 // filled itself, and refills a slot two iterations after it last read it.
 #include "common.cuh"
 #include "internal.h"
+#include "state_update.cuh"
+
+#include <algorithm>
 
 namespace lnfp8 {
 namespace {
 
 constexpr int kThreads = 256;
+static_assert(kThreads == kUpdateThreads, "the LayerNorm backward carries state updates");
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
               const uint16_t* __restrict__ gamma, const float* __restrict__ mu_in,
               const float* __restrict__ rs_in, int64_t M, int D, uint16_t* __restrict__ dx,
-              float* dgamma, float* dbeta) {
+              float* dgamma, float* dbeta, const UpdateJob job) {
   constexpr int RING = bwd_ring(NV);
   constexpr int P = RING - 2;  // rows in flight ahead of the one being processed
   __shared__ float xch[2 * (kThreads / 32)];
@@ -308,9 +312,14 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
   const int nvec = D >> 3;
   uint4* ring = sg + nvec;
   float* rstat = reinterpret_cast<float*>(ring + RING * 2 * NV * kThreads);
-  const int64_t stride = (int64_t)gridDim.x * GPB;
   pdl_wait();
   pdl_launch_dependents();
+  if ((int)blockIdx.x < job.n) {  // an extra CTA: one slot of the call's state update
+    run_update_job(job, colred, reinterpret_cast<uint32_t*>(xch));
+    return;
+  }
+  const int64_t bid = (int64_t)blockIdx.x - job.n;
+  const int64_t stride = (int64_t)(gridDim.x - job.n) * GPB;
 
   for (int c = threadIdx.x; c < 2 * D; c += kThreads) colred[c] = 0.f;
   for (int i = threadIdx.x; i < nvec; i += kThreads) sg[i] = reinterpret_cast<const uint4*>(gamma)[i];
@@ -339,7 +348,7 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
 #pragma unroll
     for (int q = 0; q < 4; ++q) accg[j][q] = accb[j][q] = 0;
 
-  int64_t row = (int64_t)blockIdx.x * GPB + g;
+  int64_t row = bid * GPB + g;
 #pragma unroll
   for (int k = 0; k < P; ++k) issue(row + k * stride, k);
   int slot = 0;
@@ -503,7 +512,8 @@ lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint1
 
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
-                           float* dbeta, cudaStream_t st, bool clear) {
+                           float* dbeta, cudaStream_t st, bool clear, const UpdateJob* job, bool* job_done) {
+  if (job_done) *job_done = false;
   if (clear && D > 0) {
     if (cudaMemsetAsync(dgamma, 0, D * sizeof(float), st) != cudaSuccess ||
         cudaMemsetAsync(dbeta, 0, D * sizeof(float), st) != cudaSuccess)
@@ -513,15 +523,19 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
   const RowShape rsh = row_shape(D, 3);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: D = %lld > 8192", (long long)D);
   const int64_t gpb = kThreads / rsh.tpr;
-  const size_t smem = 2 * D * sizeof(float) + D * sizeof(uint16_t) +
-                      (size_t)bwd_ring(rsh.nv) * (2 * rsh.nv * 16 + 2 * 4) * kThreads;
+  // the extra CTAs of an UpdateJob keep their history window in the same shared memory
+  const UpdateJob nojob = {};
+  const UpdateJob& uj = job ? *job : nojob;
+  const size_t smem = std::max<size_t>(2 * D * sizeof(float) + D * sizeof(uint16_t) +
+                                           (size_t)bwd_ring(rsh.nv) * (2 * rsh.nv * 16 + 2 * 4) * kThreads,
+                                       (size_t)uj.L * sizeof(float));
   LaunchScope ls("ln_bwd", st);
 #define LNB(TPR, NV)                                                                                   \
   do {                                                                                                 \
     auto k = ln_bwd_kernel<TPR, NV>;                                                                   \
     if (smem + 1024 > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-    const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                       \
-    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta) != cudaSuccess) \
+    const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem)) + uj.n;                \
+    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, dy, x, gamma, mu, rsigma, M, (int)D, dx, dgamma, dbeta, uj) != cudaSuccess) \
       return check_launch("ln_bwd launch");                                                            \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
@@ -541,6 +555,7 @@ lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t
     default: return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_bwd: unsupported D");
   }
 #undef LNB
+  if (job_done) *job_done = uj.n > 0;
   return check_launch("ln_bwd");
 }
 

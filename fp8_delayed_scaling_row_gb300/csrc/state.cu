@@ -10,6 +10,7 @@
 // scale_inv are reproducible bit for bit.
 #include "common.cuh"
 #include "internal.h"
+#include "state_update.cuh"
 
 namespace lnfp8 {
 namespace {
@@ -30,42 +31,6 @@ struct UpdateTable {
   int first[kMaxUpdateSets];  // first CTA of each set
   int count, margin;
 };
-
-// Slot i of one tensor set: roll its history, insert cur, reduce, rescale.
-__device__ void update_slot(float* __restrict__ scale, float* __restrict__ scale_inv, float* __restrict__ hist,
-                            float* __restrict__ cur, int n, int L, int i, bool e5m2, int margin,
-                            float* __restrict__ sinv_before, float* shist, uint32_t* red) {
-  const int t = threadIdx.x;
-  const float c = cur[i];
-  // read phase: the new row j is the old row j-1, the new row 0 is cur
-  uint32_t m = 0;
-  for (int j = t; j < L; j += kThreads) {
-    const float v = (j == 0) ? c : hist[(int64_t)(j - 1) * n + i];
-    shist[j] = v;
-    m = max(m, abs_bits(v));
-  }
-  __syncthreads();
-  for (int j = t; j < L; j += kThreads) hist[(int64_t)j * n + i] = shist[j];
-  m = warp_max_u32(m);
-  if ((t & 31) == 0) red[t >> 5] = m;
-  __syncthreads();
-  if (t == 0) {
-    uint32_t a_bits = 0;
-    for (int w = 0; w < kThreads / 32; ++w) a_bits = max(a_bits, red[w]);
-    const float a = __uint_as_float(a_bits);
-    if (sinv_before) sinv_before[i] = scale_inv[i];
-    cur[i] = 0.f;
-    const float fmax = e5m2 ? 57344.0f : 448.0f;
-    if (isfinite(a) && a > 0.f) {
-      float s = fmax / a;
-      if (margin > 0) s = s / (float)(1u << margin);
-      if (isfinite(s)) {
-        scale[i] = s;
-        scale_inv[i] = 1.0f / s;
-      }
-    }
-  }
-}
 
 __global__ void __launch_bounds__(kThreads)
 update_kernel(float* __restrict__ scale, float* __restrict__ scale_inv, float* __restrict__ hist,
@@ -125,6 +90,10 @@ lnfp8_status meta_init_launch(const lnfp8_meta* m, cudaStream_t st) {
   LaunchScope ls("state_init", st);
   init_kernel<<<blocks, 256, 0, st>>>(m->scale, m->scale_inv, m->amax_history, m->amax_cur, m->n, m->history_len);
   return check_launch("lnfp8_meta_init");
+}
+
+UpdateJob update_job(const lnfp8_meta* m, uint64_t e5m2_mask, int margin) {
+  return UpdateJob{m->scale, m->scale_inv, m->amax_history, m->amax_cur, e5m2_mask, m->n, m->history_len, margin};
 }
 
 lnfp8_status update_launch(const lnfp8_meta* m, uint64_t e5m2_mask, int margin, float* sinv_before,
