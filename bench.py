@@ -630,17 +630,17 @@ def end_to_end(torch, run, steps, dev, barrier, max_over_ranks, world, graph=Tru
 def stack_hbm_bytes(layers, m, d, f):
     """Algorithmic bytes per stack step of the HBM-bound kernel kinds (each tensor read
     or written once): LayerNorm forward (x, and with the fused residual add r and the sum
-    h, read/written as bf16; codes written; mu, rsigma), LayerNorm backward (dLN, x read,
-    dX written), the gradient casts with column sums (dY of the MLP and the projection,
-    dQKV), the plain casts (QKV and projection weights, the projection's input) and the
-    MLP weight pair."""
+    h, read/written as bf16; codes written; mu, rsigma; the launch also casts the module's
+    weights: QKV, or W1 and W2), LayerNorm backward (dLN, x read, dX written), the gradient
+    casts with column sums (dY of the MLP and the projection, dQKV) and the plain casts
+    (the projection's weight and input)."""
     row = 8 * m
     return {
-        "ln_fwd_cast": (3 * m * d + row) + (2 * layers - 1) * (7 * m * d + row),
+        "ln_fwd_cast": (3 * m * d + row) + (2 * layers - 1) * (7 * m * d + row)
+                       + layers * 3 * (3 * d * d + 2 * f * d),
         "ln_bwd": 2 * layers * (6 * m * d + row),
         "cast_colsum": layers * (3 * (m * d + m * d + 3 * m * d) + 4 * (d + d + 3 * d)),
-        "cast": layers * (3 * (3 * d * d + d * d) + 3 * m * d),
-        "cast_pair": layers * 3 * 2 * f * d,
+        "cast": layers * (3 * d * d + 3 * m * d),
     }
 
 
@@ -906,10 +906,10 @@ def run_gpu(args):
                          "share": kms / sum(v[0] for v in prof.values())}
     # LayerNorm / cast kernels against HBM (algorithmic bytes per launch)
     hbm_kernels = {
-        "ln_fwd_cast": M_TOK * D_MODEL * (2 + 1) + M_TOK * 8,        # X read, codes written, mu/rsigma
+        # X read, codes written, mu/rsigma; the same launch casts W1 and W2 (read, codes written)
+        "ln_fwd_cast": M_TOK * D_MODEL * (2 + 1) + M_TOK * 8 + 2 * FFN * D_MODEL * (2 + 1),
         "ln_bwd": M_TOK * D_MODEL * (2 + 2 + 2) + M_TOK * 8,         # dLN, X read, dX written, mu/rsigma
         "cast_colsum": M_TOK * D_MODEL * (2 + 1) + D_MODEL * 4,       # dY read, codes written, db2
-        "cast_pair": 2 * FFN * D_MODEL * (2 + 1),                     # W1, W2 read, codes written
     }
     for k, nbytes in hbm_kernels.items():
         if k in per_kernel:

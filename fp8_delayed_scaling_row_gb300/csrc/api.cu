@@ -658,12 +658,16 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
     TRY(finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st));
     return w8 ? save_weight_sinv(a->sinv_saved + 1, a->w_scale_inv, st) : LNFP8_OK;
   }
-  if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
-  if (ln)
+  if (ln) {
+    // the weight cast rides in the LayerNorm launch
+    WeightCastJob wc = {};
+    if (!w8) weight_cast_add(wc, 0, a->w, a->N, a->K, m.scale + 1, m.amax_cur + 1, a->wq);
     TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,
-                      a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum));
-  else
+                      a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc));
+  } else {
+    if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
     TRY(cast_launch(a->x, false, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, nullptr, nullptr, st));
+  }
   GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, m.scale_inv + 0,
                          w8 ? a->w_scale_inv : m.scale_inv + 1);
   g.bias = a->bias;
@@ -781,13 +785,18 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   // FC1 and FC2 in one launch when the caller gave room for the FC1 tiles' readiness counters
   const int64_t ready_bytes = lnfp8_ln_mlp_fwd_workspace_size(a->M, a->D, a->F);
   const bool fused = a->M > 0 && a->gemm_ws && ready_bytes > 0 && a->gemm_ws_bytes >= ready_bytes && !pair_disabled();
-  if (!w8)
-    TRY(cast2_launch(a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q, a->w2, a->D, a->F, m.scale + 3,
-                     m.amax_cur + 3, a->w2q, fdt, st, fused ? a->gemm_ws : nullptr, fused ? ready_bytes : 0));
-  else if (fused)
-    TRY(zero_launch({{a->gemm_ws, ready_bytes}}, st));
+  // the weight casts (and the FC1 tiles' readiness counters) ride in the LayerNorm launch
+  WeightCastJob wc = {};
+  if (!w8) {
+    weight_cast_add(wc, 0, a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q);
+    weight_cast_add(wc, 1, a->w2, a->D, a->F, m.scale + 3, m.amax_cur + 3, a->w2q);
+  }
+  if (fused) {
+    wc.zero = static_cast<uint32_t*>(a->gemm_ws);
+    wc.zero_n = (ready_bytes + 3) / 4;
+  }
   TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
-                    a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum));
+                    a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc));
   GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0,
                           w8 ? a->w1_scale_inv : m.scale_inv + 1);
   f1.epi = EPI_GELU;

@@ -48,7 +48,7 @@ __device__ __forceinline__ void load8<float>(const float* p, float* v) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// One tensor of a (multi-tensor) cast launch; blockIdx.z picks the tensor.
+// The tensor of a strip-form cast launch.
 struct CastT {
   const void* in;
   int64_t rows, cols, rows_per_cta;
@@ -57,18 +57,13 @@ struct CastT {
   uint8_t* out;
   uint8_t* out_t;
   float* colsum;
-  uint32_t* zero;  // optional words for block (0, 0, 0) to clear (counters a later kernel of the call uses)
-  int64_t zero_n;
 };
 
 template <typename T, int DT, int TR>
 __global__ void __launch_bounds__(kThreads)
-cast_kernel(const CastT t0, const CastT t1) {
+cast_kernel(const CastT ct) {
   pdl_wait();
   pdl_launch_dependents();
-  const CastT& ct = blockIdx.z ? t1 : t0;
-  if (ct.zero && blockIdx.x == 0 && blockIdx.y == 0)
-    for (int64_t i = threadIdx.x; i < ct.zero_n; i += blockDim.x) ct.zero[i] = 0u;
   const T* __restrict__ in = static_cast<const T*>(ct.in);
   const int64_t rows = ct.rows, cols = ct.cols, rows_per_cta = ct.rows_per_cta;
   const float* __restrict__ scale_p = ct.scale;
@@ -76,7 +71,6 @@ cast_kernel(const CastT t0, const CastT t1) {
   uint8_t* __restrict__ out = ct.out;
   uint8_t* __restrict__ out_t = ct.out_t;
   float* colsum = ct.colsum;
-  // blocks past this tensor's extent (the grid covers the larger tensor) leave at once
   if ((int64_t)blockIdx.x * kTC >= cols || (int64_t)blockIdx.y * rows_per_cta >= rows) return;
   // TR rows x 64 columns per iteration; each thread owns one 8-column vector
   // of TR/32 rows and issues all of their loads before converting any.
@@ -321,9 +315,9 @@ Grid2 cast_grid(int64_t rows, int64_t cols, int64_t want) {
 }
 
 template <typename T>
-lnfp8_status cast_dispatch(dim3 grid, int dtype, const CastT& a, const CastT& b, cudaStream_t st) {
-  const cudaError_t e = dtype == LNFP8_E4M3 ? launch_pdl(cast_kernel<T, LNFP8_E4M3, kTR>, grid, dim3(kThreads), 0, st, a, b)
-                                             : launch_pdl(cast_kernel<T, LNFP8_E5M2, kTR>, grid, dim3(kThreads), 0, st, a, b);
+lnfp8_status cast_dispatch(dim3 grid, int dtype, const CastT& a, cudaStream_t st) {
+  const cudaError_t e = dtype == LNFP8_E4M3 ? launch_pdl(cast_kernel<T, LNFP8_E4M3, kTR>, grid, dim3(kThreads), 0, st, a)
+                                             : launch_pdl(cast_kernel<T, LNFP8_E5M2, kTR>, grid, dim3(kThreads), 0, st, a);
   if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8_quantize launch: %s", cudaGetErrorString(e));
   return check_launch("fp8_quantize");
 }
@@ -400,29 +394,10 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
   const Grid2 g = cast_grid(rows, cols, 8LL * num_sms());
   if (g.strips > 0x7FFFFFFF || g.ysplit > 65535)
     return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "fp8_quantize: tensor too large");
-  const CastT t{in, rows, cols, g.rows_per_cta, scale, amax_cur, out, out_t, colsum, nullptr, 0};
+  const CastT t{in, rows, cols, g.rows_per_cta, scale, amax_cur, out, out_t, colsum};
   LaunchScope ls(colsum ? "cast_colsum" : "cast", st);
   const dim3 grid((unsigned)g.strips, (unsigned)g.ysplit, 1);
-  return in_fp32 ? cast_dispatch<float>(grid, dtype, t, t, st) : cast_dispatch<uint16_t>(grid, dtype, t, t, st);
-}
-
-lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
-                          uint8_t* out0, const uint16_t* in1, int64_t rows1, int64_t cols1, const float* scale1,
-                          float* amax1, uint8_t* out1, int dtype, cudaStream_t st, void* zero, int64_t zero_bytes) {
-  if (rows0 == 0 || cols0 == 0 || rows1 == 0 || cols1 == 0) {
-    if (zero && zero_bytes > 0) TRY_CAST(zero_launch({{zero, zero_bytes}}, st));
-    TRY_CAST(cast_launch(in0, false, rows0, cols0, dtype, scale0, amax0, out0, nullptr, nullptr, st));
-    return cast_launch(in1, false, rows1, cols1, dtype, scale1, amax1, out1, nullptr, nullptr, st);
-  }
-  const Grid2 g0 = cast_grid(rows0, cols0, 4LL * num_sms()), g1 = cast_grid(rows1, cols1, 4LL * num_sms());
-  if (max64(g0.strips, g1.strips) > 0x7FFFFFFF || max64(g0.ysplit, g1.ysplit) > 65535)
-    return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "weight cast: tensor too large");
-  const CastT a{in0, rows0, cols0, g0.rows_per_cta, scale0, amax0, out0, nullptr, nullptr,
-                static_cast<uint32_t*>(zero), zero ? (zero_bytes + 3) / 4 : 0};
-  const CastT b{in1, rows1, cols1, g1.rows_per_cta, scale1, amax1, out1, nullptr, nullptr, nullptr, 0};
-  LaunchScope ls("cast_pair", st);
-  const dim3 grid((unsigned)max64(g0.strips, g1.strips), (unsigned)max64(g0.ysplit, g1.ysplit), 2);
-  return cast_dispatch<uint16_t>(grid, dtype, a, b, st);
+  return in_fp32 ? cast_dispatch<float>(grid, dtype, t, st) : cast_dispatch<uint16_t>(grid, dtype, t, st);
 }
 
 namespace {

@@ -38,19 +38,32 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st, bool clear_colsum = true);
 
-// Two bf16 tensors cast in one launch (the weights of a LayerNormMLP).
 // Zeroes each (pointer, bytes) span (bytes a multiple of 4; NULL or 0 skipped), one launch.
 lnfp8_status zero_launch(std::initializer_list<std::pair<void*, int64_t>> spans, cudaStream_t st);
 
-lnfp8_status cast2_launch(const uint16_t* in0, int64_t rows0, int64_t cols0, const float* scale0, float* amax0,
-                          uint8_t* out0, const uint16_t* in1, int64_t rows1, int64_t cols1, const float* scale1,
-                          float* amax1, uint8_t* out1, int dtype, cudaStream_t st, void* zero = nullptr,
-                          int64_t zero_bytes = 0);
+// Up to two bf16 weight tensors cast to FP8 (the forward dtype) inside the
+// LayerNorm forward launch: tensor k is [rows[k], cols[k]] row-major with cols a
+// multiple of 8; tiles[k] = 0 skips it. `zero` (optional) names words that
+// the launch clears (counters that a later kernel of the call uses).
+struct WeightCastJob {
+  const uint16_t* in[2];
+  int64_t rows[2], cols[2];
+  const float* scale[2];
+  float* amax[2];
+  uint8_t* out[2];
+  int64_t tiles[2];
+  uint32_t* zero;
+  int64_t zero_n;
+};
+// Adds tensor k to the job (rows or cols 0: nothing to cast).
+void weight_cast_add(WeightCastJob& j, int k, const uint16_t* in, int64_t rows, int64_t cols, const float* scale,
+                     float* amax, uint8_t* out);
 
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st,
-                           const uint16_t* resid = nullptr, uint16_t* hsum = nullptr);
+                           const uint16_t* resid = nullptr, uint16_t* hsum = nullptr,
+                           const WeightCastJob* wc = nullptr);
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
                            float* dbeta, cudaStream_t st, bool clear = true,

@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "state_update.cuh"
+#include "weight_cast.cuh"
 
 #include <algorithm>
 
@@ -28,6 +29,7 @@ namespace {
 
 constexpr int kThreads = 256;
 static_assert(kThreads == kUpdateThreads, "the LayerNorm backward carries state updates");
+static_assert(kThreads == kWThreads, "the LayerNorm forward carries weight casts");
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
@@ -156,7 +158,7 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
               const uint16_t* __restrict__ beta, float eps, int64_t M, int D,
               const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
               float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg,
-              const uint16_t* __restrict__ resid, uint16_t* __restrict__ hsum) {
+              const uint16_t* __restrict__ resid, uint16_t* __restrict__ hsum, const WeightCastJob wc) {
   constexpr int NVR = RES ? 2 * NV : NV;  // 16-byte chunks per row and thread in the ring
   constexpr int RING = fwd_ring(NVR);
   constexpr int P = RING - 2;  // rows in flight ahead of the one being normalised
@@ -200,6 +202,10 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   int64_t row = (int64_t)blockIdx.x * GPB + g;
 #pragma unroll
   for (int k = 0; k < P; ++k) issue(row + k * stride, k);
+  // the call's weight casts, while the first rows' loads are in flight
+  if (wc.zero && blockIdx.x == 0)
+    for (int64_t i = threadIdx.x; i < wc.zero_n; i += kThreads) wc.zero[i] = 0u;
+  if (wc.tiles[0] + wc.tiles[1] > 0) weight_cast_tiles<DT>(wc);
   int slot = 0;
   // every thread of the block runs the same trip count (group_sum may use barriers)
   for (; row - g < M; row += stride) {
@@ -456,7 +462,7 @@ template <int DT, bool RES>
 lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
                              const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int D,
                              const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
-                             float* ydbg, const uint16_t* resid, uint16_t* hsum) {
+                             float* ydbg, const uint16_t* resid, uint16_t* hsum, const WeightCastJob& wc) {
   const int nvr = RES ? 2 * rsh.nv : rsh.nv;
   const size_t smem = (size_t)D * 2 * sizeof(uint16_t) + (size_t)fwd_ring(nvr) * nvr * kThreads * 16;
   const int64_t gpb = kThreads / rsh.tpr;
@@ -464,8 +470,9 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
   do {                                                                                                  \
     auto k = ln_fwd_kernel<TPR, NV, DT, RES>;                                                           \
     if (smem + 1024 > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-    const int64_t blocks = min64((M + gpb - 1) / gpb, resident_blocks(k, smem));                        \
-    if (launch_pdl(k, dim3((unsigned)blocks), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg, resid, hsum) != cudaSuccess) \
+    /* the weight tiles are shared by at least as many CTAs as the rows need, up to a full wave */     \
+    const int64_t blocks = min64(max64((M + gpb - 1) / gpb, wc.tiles[0] + wc.tiles[1]), resident_blocks(k, smem)); \
+    if (launch_pdl(k, dim3((unsigned)max64(blocks, 1)), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg, resid, hsum, wc) != cudaSuccess) \
       return check_launch("ln_fwd_cast launch");                                                        \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
@@ -490,24 +497,37 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
 
 }  // namespace
 
+void weight_cast_add(WeightCastJob& j, int k, const uint16_t* in, int64_t rows, int64_t cols, const float* scale,
+                     float* amax, uint8_t* out) {
+  j.in[k] = in;
+  j.rows[k] = rows;
+  j.cols[k] = cols;
+  j.scale[k] = scale;
+  j.amax[k] = amax;
+  j.out[k] = out;
+  j.tiles[k] = rows > 0 && cols > 0 ? ((rows + kWTileRows - 1) / kWTileRows) * ((cols + kWTileCols - 1) / kWTileCols) : 0;
+}
+
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st,
-                           const uint16_t* resid, uint16_t* hsum) {
-  if (M == 0) return LNFP8_OK;
+                           const uint16_t* resid, uint16_t* hsum, const WeightCastJob* wcp) {
+  const WeightCastJob nojob = {};
+  const WeightCastJob& wc = wcp ? *wcp : nojob;
+  if (M == 0 && wc.tiles[0] + wc.tiles[1] == 0 && !(wc.zero && wc.zero_n > 0)) return LNFP8_OK;
   const RowShape rsh = row_shape(D, 4);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: D = %lld > 8192", (long long)D);
   LaunchScope ls("ln_fwd_cast", st);
   const bool res = resid != nullptr;
   if (dtype == LNFP8_E4M3)
     return res ? ln_fwd_dispatch<LNFP8_E4M3, true>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                   rsigma, ydbg, resid, hsum)
+                                                   rsigma, ydbg, resid, hsum, wc)
                : ln_fwd_dispatch<LNFP8_E4M3, false>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                    rsigma, ydbg, nullptr, nullptr);
+                                                    rsigma, ydbg, nullptr, nullptr, wc);
   return res ? ln_fwd_dispatch<LNFP8_E5M2, true>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                 rsigma, ydbg, resid, hsum)
+                                                 rsigma, ydbg, resid, hsum, wc)
              : ln_fwd_dispatch<LNFP8_E5M2, false>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                  rsigma, ydbg, nullptr, nullptr);
+                                                  rsigma, ydbg, nullptr, nullptr, wc);
 }
 
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,

@@ -301,11 +301,11 @@ def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profile
     direct = L.profile_collect()
     L.profile_enable(False)
     L.sync_status()
-    # forward: weight casts, LayerNorm, FC1, FC2, state; backward: clears, dY cast, the FC2 data and weight
-    # gradients in one launch, the FC1 data and weight gradients in one launch, LayerNorm with the state
-    # update in extra CTAs of the same launch
-    assert sum(n for _, n in direct.values()) == 10 and all(ms > 0 for ms, _ in direct.values())
-    assert direct["state_update"][1] == 1 and direct["ln_bwd"][1] == 1
+    # forward: LayerNorm with the weight casts in the same launch, FC1, FC2, state; backward: clears, dY cast,
+    # the FC2 data and weight gradients in one launch, the FC1 data and weight gradients in one launch,
+    # LayerNorm with the state update in extra CTAs of the same launch
+    assert sum(n for _, n in direct.values()) == 9 and all(ms > 0 for ms, _ in direct.values())
+    assert direct["state_update"][1] == 1 and direct["ln_bwd"][1] == 1 and "cast_pair" not in direct
 
     fm1, bm1, ctx1, g1 = make()
     y1 = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
@@ -405,3 +405,36 @@ def test_mlp_forward_fused_launch_equals_two_launches(L, M, D, F):
         assert torch.equal(c0.h, c1.h) and torch.equal(c0.aq, c1.aq)
         for name in ("scale", "scale_inv", "amax_history"):
             assert torch.equal(getattr(m0, name), getattr(m1, name)), name
+
+
+@pytest.mark.parametrize("M", [0, 1, 300])
+def test_forward_weight_casts_in_the_layernorm_launch(L, M):
+    """The forward's weight casts run inside its LayerNorm launch: W1, W2 (LayerNormMLP)
+    and W (LayerNormLinear) codes equal the oracle's cast bit for bit, and their amaxes
+    reach the history, also with no tokens at all (the launch then only casts) and with
+    one token (the grid is sized by the weight tiles). The widths leave ragged 128 x 64
+    weight tiles (272 = 4 x 64 + 16 columns, 1040 = 8 x 128 + 16 rows)."""
+    D, F, N = 272, 1040, 784
+    rec, orec = L.Recipe("hybrid", 4), ORecipe("hybrid", 4)
+    ffmt = orec.fwd_fmt()
+    p = synth.mlp_params(D, F, seed=17, bias_std=0.02)
+    lw = synth.weight(N, D, seed=17, tid=synth.TID["w1"], layer=1)
+    dev = {k: bf16_dev(v) for k, v in p.items()}
+    fm, lm = L.ScalingMeta(4, 4), L.ScalingMeta(2, 4)
+    W1, W2, LW = bf16_to_f32(p["w1"]), bf16_to_f32(p["w2"]), bf16_to_f32(lw)
+    for step in range(2):
+        fpre, lpre = _state_from_gpu(fm), _state_from_gpu(lm)
+        x = bf16_dev(synth.activations(M, D, dist="outliers", seed=17, step=step)) if M else \
+            torch.empty(0, D, dtype=torch.bfloat16, device="cuda")
+        _, ctx = L.ln_mlp_fwd(x, dev["gamma"], dev["beta"], dev["w1"], dev["b1"], dev["w2"], dev["b2"], fm, rec)
+        _, lctx = L.ln_linear_fwd(x, dev["gamma"], dev["beta"], bf16_dev(lw), None, lm, rec)
+        L.sync_status()
+        assert np.array_equal(host(ctx.w1q), ofp8.quantize(W1, fpre.scale[1], ffmt)), step
+        assert np.array_equal(host(ctx.w2q), ofp8.quantize(W2, fpre.scale[3], ffmt)), step
+        assert np.array_equal(host(lctx.wq), ofp8.quantize(LW, lpre.scale[1], ffmt)), step
+        fh, lh = host(fm.amax_history)[0], host(lm.amax_history)[0]
+        assert fh[1] == ofp8.amax(W1) and fh[3] == ofp8.amax(W2) and lh[1] == ofp8.amax(LW), step
+        _assert_state_equal(fm, _teacher_forced(fpre, fm, [ffmt] * 4), f"fwd step {step}")
+        _assert_state_equal(lm, _teacher_forced(lpre, lm, [ffmt] * 2), f"linear step {step}")
+        if M == 0:
+            assert fh[0] == 0 and fh[2] == 0 and lh[0] == 0  # no rows: no activation amax
