@@ -627,20 +627,27 @@ def end_to_end(torch, run, steps, dev, barrier, max_over_ranks, world, graph=Tru
                       "overlapping the neighbouring steps' compute (two device buffer sets)"}
 
 
+# A weight of this many elements or more is cast by its own (row-streaming) launch; a smaller
+# one rides in its module's LayerNorm forward launch (the library's rule).
+ROW_CAST_MIN_ELEMS = 1 << 24
+
+
 def stack_hbm_bytes(layers, m, d, f):
     """Algorithmic bytes per stack step of the HBM-bound kernel kinds (each tensor read
     or written once): LayerNorm forward (x, and with the fused residual add r and the sum
     h, read/written as bf16; codes written; mu, rsigma; the launch also casts the module's
-    weights: QKV, or W1 and W2), LayerNorm backward (dLN, x read, dX written), the gradient
-    casts with column sums (dY of the MLP and the projection, dQKV) and the plain casts
-    (the projection's weight and input)."""
+    weights below ROW_CAST_MIN_ELEMS: QKV, W1, W2), LayerNorm backward (dLN, x read, dX
+    written), the gradient casts with column sums (dY of the MLP and the projection, dQKV)
+    and the plain casts (the projection's weight and input, and the large weights)."""
     row = 8 * m
+    weights = [3 * d * d, f * d, f * d]  # QKV, W1, W2 elements
+    folded = sum(w for w in weights if w < ROW_CAST_MIN_ELEMS)
+    own = sum(w for w in weights if w >= ROW_CAST_MIN_ELEMS)
     return {
-        "ln_fwd_cast": (3 * m * d + row) + (2 * layers - 1) * (7 * m * d + row)
-                       + layers * 3 * (3 * d * d + 2 * f * d),
+        "ln_fwd_cast": (3 * m * d + row) + (2 * layers - 1) * (7 * m * d + row) + layers * 3 * folded,
         "ln_bwd": 2 * layers * (6 * m * d + row),
         "cast_colsum": layers * (3 * (m * d + m * d + 3 * m * d) + 4 * (d + d + 3 * d)),
-        "cast": layers * (3 * d * d + 3 * m * d),
+        "cast": layers * (3 * d * d + 3 * m * d + 3 * own),
     }
 
 

@@ -659,9 +659,12 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
     return w8 ? save_weight_sinv(a->sinv_saved + 1, a->w_scale_inv, st) : LNFP8_OK;
   }
   if (ln) {
-    // the weight cast rides in the LayerNorm launch
+    // a small weight cast rides in the LayerNorm launch, a large one streams through its own
     WeightCastJob wc = {};
-    if (!w8) weight_cast_add(wc, 0, a->w, a->N, a->K, m.scale + 1, m.amax_cur + 1, a->wq);
+    if (!w8 && cast_streams_rows(a->N, a->K))
+      TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
+    else if (!w8)
+      weight_cast_add(wc, 0, a->w, a->N, a->K, m.scale + 1, m.amax_cur + 1, a->wq);
     TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,
                       a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc));
   } else {
@@ -785,11 +788,18 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   // FC1 and FC2 in one launch when the caller gave room for the FC1 tiles' readiness counters
   const int64_t ready_bytes = lnfp8_ln_mlp_fwd_workspace_size(a->M, a->D, a->F);
   const bool fused = a->M > 0 && a->gemm_ws && ready_bytes > 0 && a->gemm_ws_bytes >= ready_bytes && !pair_disabled();
-  // the weight casts (and the FC1 tiles' readiness counters) ride in the LayerNorm launch
+  // small weight casts (and the FC1 tiles' readiness counters) ride in the LayerNorm launch,
+  // large ones stream through their own launches
   WeightCastJob wc = {};
   if (!w8) {
-    weight_cast_add(wc, 0, a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q);
-    weight_cast_add(wc, 1, a->w2, a->D, a->F, m.scale + 3, m.amax_cur + 3, a->w2q);
+    if (cast_streams_rows(a->F, a->D))
+      TRY(cast_launch(a->w1, false, a->F, a->D, fdt, m.scale + 1, m.amax_cur + 1, a->w1q, nullptr, nullptr, st));
+    else
+      weight_cast_add(wc, 0, a->w1, a->F, a->D, m.scale + 1, m.amax_cur + 1, a->w1q);
+    if (cast_streams_rows(a->D, a->F))
+      TRY(cast_launch(a->w2, false, a->D, a->F, fdt, m.scale + 3, m.amax_cur + 3, a->w2q, nullptr, nullptr, st));
+    else
+      weight_cast_add(wc, 1, a->w2, a->D, a->F, m.scale + 3, m.amax_cur + 3, a->w2q);
   }
   if (fused) {
     wc.zero = static_cast<uint32_t*>(a->gemm_ws);

@@ -375,6 +375,8 @@ lnfp8_status rows_dispatch(RowsShape rs, const uint16_t* in, int64_t rows, int64
 }
 }  // namespace
 
+bool cast_streams_rows(int64_t rows, int64_t cols) { return rows_shape(cols).tpr && rows * cols >= kRowsMinElems; }
+
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st, bool clear_colsum) {
@@ -384,7 +386,7 @@ lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t col
   // large bf16 tensors without a transposed copy stream through the row form (on small ones
   // its per-block column reduction costs more than it saves)
   const RowsShape rs = rows_shape(cols);
-  if (!in_fp32 && !out_t && out && rs.tpr && rows * cols >= kRowsMinElems) {
+  if (!in_fp32 && !out_t && out && cast_streams_rows(rows, cols)) {
     LaunchScope ls(colsum ? "cast_colsum" : "cast", st);
     return dtype == LNFP8_E4M3
                ? rows_dispatch<LNFP8_E4M3>(rs, static_cast<const uint16_t*>(in), rows, cols, scale, amax_cur, out, colsum, st)

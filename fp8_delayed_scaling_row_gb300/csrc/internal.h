@@ -34,6 +34,9 @@ struct UpdateJob {
 };
 UpdateJob update_job(const lnfp8_meta* m, uint64_t e5m2_mask, int margin);
 
+// Whether a bf16 cast of this shape (no transposed copy) takes the row-streaming
+// form, which reaches a larger share of HBM on large tensors.
+bool cast_streams_rows(int64_t rows, int64_t cols);
 lnfp8_status cast_launch(const void* in, bool in_fp32, int64_t rows, int64_t cols, int dtype,
                          const float* scale, float* amax_cur, uint8_t* out, uint8_t* out_t,
                          float* colsum, cudaStream_t st, bool clear_colsum = true);
@@ -44,7 +47,10 @@ lnfp8_status zero_launch(std::initializer_list<std::pair<void*, int64_t>> spans,
 // Up to two bf16 weight tensors cast to FP8 (the forward dtype) inside the
 // LayerNorm forward launch: tensor k is [rows[k], cols[k]] row-major with cols a
 // multiple of 8; tiles[k] = 0 skips it. `zero` (optional) names words that
-// the launch clears (counters that a later kernel of the call uses).
+// the launch clears (counters that a later kernel of the call uses). The
+// forward calls put a weight here when it is small enough that its own launch
+// would be latency-bound (below the row-streaming cast's size); a larger one
+// gets its own row-streaming cast launch.
 struct WeightCastJob {
   const uint16_t* in[2];
   int64_t rows[2], cols[2];

@@ -43,13 +43,18 @@ def test_clock_summary_keeps_samples_inside_the_region():
 def test_stack_hbm_bytes_by_hand():
     # one layer at d 2048 over 16384 tokens: the QKV LayerNorm reads x (2 B) and writes codes (1 B),
     # the MLP LayerNorm adds the residual (x, r read, h written, codes: 7 B); 8 B of mu, rsigma per row;
-    # the two LayerNorm launches also cast the QKV weight and W1, W2 (2 B read, 1 B written each)
+    # the QKV LayerNorm launch also casts the QKV weight (6144 x 2048, below 2^24 elements: 2 B read,
+    # 1 B written); W1 and W2 (8192 x 2048 = 2^24 each) stream through their own cast launches
     md = 16384 * 2048
     b = bench.stack_hbm_bytes(1, 16384, 2048, 8192)
-    assert b["ln_fwd_cast"] == 3 * md + 7 * md + 2 * 8 * 16384 + 3 * 3 * 2048 * 2048 + 3 * 2 * 8192 * 2048
+    assert b["ln_fwd_cast"] == 3 * md + 7 * md + 2 * 8 * 16384 + 3 * 3 * 2048 * 2048
     assert b["ln_bwd"] == 2 * (6 * md + 8 * 16384)
     assert b["cast_colsum"] == 3 * 5 * md + 4 * 5 * 2048         # dY of MLP and projection, dQKV (3d wide)
-    assert b["cast"] == 3 * 2048 * 2048 + 3 * md                  # projection weight and input
+    assert b["cast"] == 3 * 2048 * 2048 + 3 * md + 3 * 2 * 8192 * 2048  # projection weight and input, W1, W2
     assert "cast_pair" not in b
     twelve = bench.stack_hbm_bytes(12, 16384, 2048, 8192)
-    assert twelve["ln_fwd_cast"] == 3 * md + 23 * 7 * md + 24 * 8 * 16384 + 12 * 3 * (3 * 2048 * 2048 + 2 * 8192 * 2048)
+    assert twelve["ln_fwd_cast"] == 3 * md + 23 * 7 * md + 24 * 8 * 16384 + 12 * 3 * 3 * 2048 * 2048
+    # at d 768 every weight rides in a LayerNorm launch
+    s768 = bench.stack_hbm_bytes(4, 8192, 768, 3072)
+    assert s768["ln_fwd_cast"] == 3 * 8192 * 768 + 7 * 7 * 8192 * 768 + 8 * 8 * 8192 + 4 * 3 * (3 * 768 * 768 + 2 * 3072 * 768)
+    assert s768["cast"] == 4 * (3 * 768 * 768 + 3 * 8192 * 768)
