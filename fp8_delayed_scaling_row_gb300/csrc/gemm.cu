@@ -761,20 +761,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               const uint64_t h = bf2_to_f2(hw[i]);
               const uint64_t u = mul2(h, fma2(mul2(h, h), KC2, K2));
               const uint64_t t = f2(tanh_fast(lo(u)), tanh_fast(hi(u)));
-              const uint64_t hh = mul2(h, H2);
-              a2[i] = fma2(hh, t, hh);
+              a2[i] = fma2(h, t, h);  // 2a: a = h/2 (1 + t) is exactly half of the rounded h + h t
             }
             if (full || ok) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(a2[i])), hi(a2[i]));
+              for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(a2[i])), hi(a2[i]));  // 2 amax, halved at the end
               if (p.dbg) {
+                const uint64_t o0 = mul2(a2[0], H2), o1 = mul2(a2[1], H2), o2 = mul2(a2[2], H2), o3 = mul2(a2[3], H2);
                 float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.N + n);
-                d4[0] = make_float4(lo(a2[0]), hi(a2[0]), lo(a2[1]), hi(a2[1]));
-                d4[1] = make_float4(lo(a2[2]), hi(a2[2]), lo(a2[3]), hi(a2[3]));
+                d4[0] = make_float4(lo(o0), hi(o0), lo(o1), hi(o1));
+                d4[1] = make_float4(lo(o2), hi(o2), lo(o3), hi(o3));
               }
             }
             *reinterpret_cast<uint4*>(so + sw64(r, g)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            const uint64_t q2 = f2(scale_q, scale_q);
+            const uint64_t q2 = f2(0.5f * scale_q, 0.5f * scale_q);  // (2a)(scale/2) rounds as a * scale
             *reinterpret_cast<uint2*>(sq + sw32(r, g >> 1) + (g & 1) * 8) =
                 make_uint2((uint32_t)cvt_pair<QDT>(mul2(a2[0], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[1], q2)) << 16),
                            (uint32_t)cvt_pair<QDT>(mul2(a2[2], q2)) | ((uint32_t)cvt_pair<QDT>(mul2(a2[3], q2)) << 16));
@@ -864,6 +864,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (lane == 0) bulk_wait0();
     __syncwarp();
     if constexpr (EPI != EPI_STORE) {
+      if constexpr (EPI == EPI_GELU) am_f *= 0.5f;  // the GELU epilogue tracked 2a (halving is exact)
       const uint32_t am = warp_max_u32(abs_bits(am_f));
       if (lane == 0 && am != 0u) atomic_max_amax(p.amax_q, am);
     }

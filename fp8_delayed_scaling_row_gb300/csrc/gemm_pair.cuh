@@ -522,7 +522,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         uint2 oq[4];
         const uint64_t s2 = f2(s0, s0);
         const uint64_t K2 = f2(kGeluK, kGeluK), KC2 = f2(kGeluK * kGeluC, kGeluK * kGeluC), H2 = f2(0.5f, 0.5f);
-        const uint64_t q2 = f2(scale_q, scale_q);
+        const uint64_t q2 = f2(0.5f * scale_q, 0.5f * scale_q);  // (2a)(scale/2) rounds as a * scale
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int64_t n = n0 + g * 8;
@@ -539,16 +539,16 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
             const uint64_t h = bf2_to_f2(hw[i]);
             const uint64_t uu = mul2(h, fma2(mul2(h, h), KC2, K2));
             const uint64_t t = f2(tanh_fast(lo(uu)), tanh_fast(hi(uu)));
-            const uint64_t hh = mul2(h, H2);
-            a2[i] = fma2(hh, t, hh);
+            a2[i] = fma2(h, t, h);  // 2a: a = h/2 (1 + t) is exactly half of the rounded h + h t
           }
           if (ok) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(a2[i])), hi(a2[i]));
+            for (int i = 0; i < 4; ++i) am_f = maxabs(maxabs(am_f, lo(a2[i])), hi(a2[i]));  // 2 amax, halved at the end
             if (p.dbg) {
+              const uint64_t o0 = mul2(a2[0], H2), o1 = mul2(a2[1], H2), o2 = mul2(a2[2], H2), o3 = mul2(a2[3], H2);
               float4* d4 = reinterpret_cast<float4*>(p.dbg + m * p.p0.N + n);
-              d4[0] = make_float4(lo(a2[0]), hi(a2[0]), lo(a2[1]), hi(a2[1]));
-              d4[1] = make_float4(lo(a2[2]), hi(a2[2]), lo(a2[3]), hi(a2[3]));
+              d4[0] = make_float4(lo(o0), hi(o0), lo(o1), hi(o1));
+              d4[1] = make_float4(lo(o2), hi(o2), lo(o3), hi(o3));
             }
           }
           ob[g] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -719,6 +719,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
+    if constexpr (PEPI == EPI_GELU) am_f *= 0.5f;  // the GELU epilogue tracked 2a (halving is exact)
     const uint32_t am = warp_max_u32(abs_bits(am_f));
     if (lane == 0 && am != 0u) atomic_max_amax(p.amax_q, am);
   }
