@@ -62,6 +62,11 @@ struct PairParams {
   // secondary epilogue
   const uint16_t* bias1;
   int splits1, kbs1;  // K pieces per secondary tile (1 or 2) and K blocks per piece
+  // Uneven pieces (bf16-store primary): the first s_tail secondary positions hold the long
+  // pieces (K blocks s_small..) of tiles 0..s_tail-1, the last s_tail positions their short
+  // pieces (K blocks 0..s_small-1), the positions between both halves of the other tiles.
+  // The last positions fall on the clusters with one primary tile more (see pair_launch_t).
+  int s_tail, s_small;
   float* ws;          // split exchange: [tile][warp][chunk][8][32] x 16 B
   unsigned* flags;    // [tile][piece][warp]
   unsigned* ready;    // forward: per row block, the epilogue warps (both CTAs, every FC1 tile) done with its codes; zero at launch
@@ -74,8 +79,22 @@ struct PairParams {
 // pair's schedule (no cycles), and by the time a producer gets there those
 // tiles' epilogues have usually finished on all SMs, so the wait rarely holds
 // up the next FC1 tile's loads.
+// Secondary position v -> its tile and K piece.
+__device__ __forceinline__ int s_tile(const PairParams& p, int v) {
+  if (p.splits1 == 1) return v;
+  if (v < p.s_tail) return v;
+  if (v >= p.p1.units - p.s_tail) return v - (p.p1.units - p.s_tail);
+  return p.s_tail + (v - p.s_tail) / 2;
+}
+__device__ __forceinline__ int s_piece(const PairParams& p, int v) {
+  if (p.splits1 == 1) return 0;
+  if (v < p.s_tail) return 1;
+  if (v >= p.p1.units - p.s_tail) return 0;
+  return (v - p.s_tail) & 1;
+}
+
 __device__ __forceinline__ int fwd_release_round(const PairParams& p, int v, int ncl) {
-  const int m2 = (v / p.splits1) / p.p1.num_n;
+  const int m2 = s_tile(p, v) / p.p1.num_n;
   return (p.p0.num_n * (m2 + 1) - 1) / ncl + 1;
 }
 
@@ -98,11 +117,13 @@ struct PairSched {
   }
   __device__ int p_unit(int i) const { return c + i * ncl; }
   __device__ int s_unit(int j) const { return c + (nP + j) * ncl - U0; }  // j-th secondary unit of the cluster
-  __device__ static int s_kb0(const PairParams& p, int v) { return (v % p.splits1) * p.kbs1; }
+  __device__ static int s_kb0(const PairParams& p, int v) {
+    return s_piece(p, v) == 0 ? 0 : (s_tile(p, v) < p.s_tail ? p.s_small : p.kbs1);
+  }
   __device__ static int s_len(const PairParams& p, int v) {
     const int k0 = s_kb0(p, v);
-    const int k1 = min(p.p1.num_kb, k0 + p.kbs1);
-    return k1 - k0;
+    if (s_piece(p, v) == 1 || p.splits1 == 1) return p.p1.num_kb - k0;
+    return s_tile(p, v) < p.s_tail ? p.s_small : min(p.p1.num_kb, p.kbs1);
   }
   __device__ int gaps() const { return nP > 0 ? nP : 1; }
   __device__ int64_t gap_end(int i) const { return nP > 0 ? KS * (i + 1) / nP : KS; }
@@ -205,18 +226,18 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
   constexpr uint16_t kPair = 3;
   PairSched sc;
   sc.init(p, cid, ncl);
-  // tile coordinates: primary unit u = tile; secondary unit v = tile * splits1 + piece
+  // tile coordinates: primary unit u = tile; secondary position v -> s_tile, s_piece
   constexpr bool DEP = PEPI == EPI_GELU;  // forward: FC2 depends on this launch's FC1 output
   auto p_m = [&](int u) {
     return (DEP ? u / p.p0.num_n : tile_mn(u, p.p0.num_m2, p.p0.num_n, p.p0.group_m).x) * CL + rank;
   };
   auto p_n = [&](int u) { return DEP ? u % p.p0.num_n : tile_mn(u, p.p0.num_m2, p.p0.num_n, p.p0.group_m).y; };
   auto s_m = [&](int v) {
-    const int t = v / p.splits1;
+    const int t = s_tile(p, v);
     return (DEP ? t / p.p1.num_n : tile_mn(t, p.p1.num_m2, p.p1.num_n, p.p1.group_m).x) * CL + rank;
   };
   auto s_n = [&](int v) {
-    const int t = v / p.splits1;
+    const int t = s_tile(p, v);
     return DEP ? t % p.p1.num_n : tile_mn(t, p.p1.num_m2, p.p1.num_n, p.p1.group_m).y;
   };
 
@@ -281,7 +302,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
         if (ok)
           ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int v, int k0, int k1, bool, bool) {
             for (int kb = k0; kb < k1; ++kb) {
-              if (DEP && !wait_ready((v / p.splits1) / p.p1.num_n)) return false;
+              if (DEP && !wait_ready(s_tile(p, v) / p.p1.num_n)) return false;
               if (!load(false, s_m(v), s_n(v), kb)) return false;
             }
             return true;
@@ -707,7 +728,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
       }
       if (ok)
         ok = cur.run_gap(sc, p, sc.gap_end(i), [&](int v, int, int, bool, bool last) {
-          return last ? store_tile(1, s_m(v), s_n(v), p.splits1 > 1 ? v % p.splits1 : 0, p.splits1, &tmO1, p.bias1,
+          return last ? store_tile(1, s_m(v), s_n(v), s_piece(p, v), p.splits1, &tmO1, p.bias1,
                                    p.p1.N, p.p1.M, s1)
                       : true;
         }, i, DEP);
@@ -768,11 +789,30 @@ lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaSt
   const int clusters = units < max_clusters ? units : max_clusters;
   // the two K pieces of a secondary tile exchange partials: they must run on different clusters
   if (pp.splits1 > 1 && clusters < 2) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm pair: split on one cluster");
+  // With a bf16-store primary the launch is MMA-bound: the first U0 % clusters clusters run one
+  // primary tile more, and when the secondary positions wrap onto those clusters once, the
+  // tiles whose pieces land there are cut unevenly (a short piece there, the long one on a
+  // cluster with fewer primaries), evening out the clusters' K blocks.
+  PairParams pq = pp;
+  pq.s_tail = pq.s_small = 0;
+  if (PEPI == EPI_STORE && pq.splits1 == 2) {
+    const int U0 = pq.p0.units, U1 = pq.p1.units, c0 = U0 % clusters, tail = U1 - (clusters - c0);
+    const int lo = U0 / clusters, kb0 = pq.p0.num_kb, kb1 = pq.p1.num_kb;
+    if (c0 > 0 && tail > 0 && tail <= c0 && U1 >= 2 * tail && U1 <= clusters) {
+      const int small = max(1, min(kb1 / 2, (kb1 - kb0) / 2));
+      const int before = (lo + 1) * kb0 + pq.kbs1;
+      const int after = max((lo + 1) * kb0 + small, lo * kb0 + kb1 - small);
+      if (after < before) {
+        pq.s_tail = tail;
+        pq.s_small = small;
+      }
+    }
+  }
   cfg.gridDim = dim3(clusters * CL);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   static const char* kind = PEPI == EPI_DGELU ? "gemm_dgelu_wgrad" : PEPI == EPI_GELU ? "gemm_gelu_fc2" : "gemm_dgrad_wgrad";
   LaunchScope ls(kind, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], pp);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], pq);
   if (e != cudaSuccess) return set_error(LNFP8_ERR_CUDA, "fp8 gemm pair launch: %s", cudaGetErrorString(e));
   return check_launch("fp8 gemm pair");
 }
