@@ -25,18 +25,22 @@
 // This file is part of gemm.cu's translation unit (it uses its PTX wrappers,
 // tile constants and status word).
 
-constexpr int kPairStages = 4;
-
+// Shared memory of a paired launch. The dGELU and GELU primaries stage H and
+// FP8 codes per epilogue warp and (dGELU) column-sum partials, which leaves room
+// for a 4-stage operand ring; a bf16-store primary needs none of them and runs
+// 6 stages (its MMAs, not its epilogue, set the launch's time).
+template <int PEPI>
 struct PairCfg {
-  static constexpr int STAGES = kPairStages;
+  static constexpr bool STORE = PEPI == EPI_STORE;
+  static constexpr int STAGES = STORE ? 6 : 4;
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = 128 * BK;  // this CTA's half of the 256-wide B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int OUT_OFF = STAGES * STAGE_BYTES;      // bf16 staging box per warp (secondary stores)
-  static constexpr int H_OFF = OUT_OFF + kEpiWarps * 2048;  // bf16 H box per warp (primary loads)
-  static constexpr int Q_OFF = H_OFF + kEpiWarps * 2048;    // FP8 staging box per warp (primary stores)
-  static constexpr int CSUM_OFF = Q_OFF + kEpiWarps * 1024; // [tile parity][row quarter][256] fp32 column-sum partials
-  static constexpr int BAR_OFF = CSUM_OFF + 2 * 4 * 256 * 4;
+  static constexpr int OUT_OFF = STAGES * STAGE_BYTES;                           // bf16 staging box per warp (bf16 stores)
+  static constexpr int H_OFF = OUT_OFF + kEpiWarps * 2048;                       // bf16 H box per warp (primary loads)
+  static constexpr int Q_OFF = H_OFF + (STORE ? 0 : kEpiWarps * 2048);           // FP8 staging box per warp (primary stores)
+  static constexpr int CSUM_OFF = Q_OFF + (STORE ? 0 : kEpiWarps * 1024);        // [tile parity][row quarter][256] fp32 column-sum partials
+  static constexpr int BAR_OFF = CSUM_OFF + (STORE ? 0 : 2 * 4 * 256 * 4);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -164,7 +168,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmH0,
             const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
             const __grid_constant__ CUtensorMap tmO1, const PairParams p) {
-  using C = PairCfg;
+  using C = PairCfg<PEPI>;
   constexpr int STAGES = C::STAGES;
   constexpr int BN = 256;
   extern __shared__ uint8_t smem_raw[];
@@ -760,7 +764,7 @@ lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaSt
   auto k = pair_kernel<PEPI, B0_MN, A1_MN, B1_MN, QDT>;
   static bool smem_set = false;
   if (!smem_set) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg<PEPI>::SMEM) != cudaSuccess)
       return check_launch("fp8 gemm pair: shared memory attribute");
     smem_set = true;
   }
@@ -773,7 +777,7 @@ lnfp8_status pair_launch_t(const CUtensorMap* maps, const PairParams& pp, cudaSt
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = PairCfg::SMEM;
+  cfg.dynamicSmemBytes = PairCfg<PEPI>::SMEM;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
