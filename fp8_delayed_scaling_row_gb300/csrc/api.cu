@@ -805,8 +805,11 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
     wc.zero = static_cast<uint32_t*>(a->gemm_ws);
     wc.zero_n = (ready_bytes + 3) / 4;
   }
+  // the LayerNorm launch also saves the scale_inv this forward casts with (for FC2 and the backward)
+  const SinvSnapshot snap = {a->sinv_saved, {m.scale_inv + 0, w8 ? a->w1_scale_inv : m.scale_inv + 1, m.scale_inv + 2,
+                                             w8 ? a->w2_scale_inv : m.scale_inv + 3}, 4};
   TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->D, fdt, m.scale + 0, m.amax_cur + 0, a->lnq, a->mu,
-                    a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc));
+                    a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc, &snap));
   GemmArgs f1 = gemm_args(a->lnq, 0, fdt, a->w1q, 0, fdt, a->M, a->F, a->D, m.scale_inv + 0,
                           w8 ? a->w1_scale_inv : m.scale_inv + 1);
   f1.epi = EPI_GELU;
@@ -817,8 +820,8 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
   f1.scale_q = m.scale + 2;
   f1.amax_q = m.amax_cur + 2;
   f1.dbg = a->act_debug;
-  GemmArgs f2 = gemm_args(a->aq, 0, fdt, a->w2q, 0, fdt, a->M, a->D, a->F, m.scale_inv + 2,
-                          w8 ? a->w2_scale_inv : m.scale_inv + 3);
+  // FC2 dequantises with the saved scale_inv: the state update may run while it does
+  GemmArgs f2 = gemm_args(a->aq, 0, fdt, a->w2q, 0, fdt, a->M, a->D, a->F, a->sinv_saved + 2, a->sinv_saved + 3);
   f2.bias = a->b2;
   f2.out = a->y;
   if (fused) {
@@ -826,13 +829,14 @@ lnfp8_status ln_mlp_fwd(const lnfp8_ln_mlp_fwd_args* a, lnfp8_stream stream) {
     f1.ws_bytes = a->gemm_ws_bytes;
     TRY(gemm_pair_launch(f1, f2, st));
   } else {
+    // every amax of the forward is final when FC2 starts: it carries the state update
+    if (a->M > 0 && !a->defer_update) f2.upd = update_job(&m, mask_all(m.n, fdt), a->recipe.margin);
     TRY(gemm_launch(f1, st));
     TRY(gemm_launch(f2, st));
+    if (f2.upd.n > 0) return LNFP8_OK;
   }
-  TRY(finish_state(&m, &a->recipe, fdt, a->sinv_saved, a->defer_update, st));
-  if (!w8) return LNFP8_OK;
-  TRY(save_weight_sinv(a->sinv_saved + 1, a->w1_scale_inv, st));
-  return save_weight_sinv(a->sinv_saved + 3, a->w2_scale_inv, st);
+  // the snapshot is taken: only the update remains (none when deferred)
+  return finish_state(&m, &a->recipe, fdt, nullptr, a->defer_update, st);
 }
 
 lnfp8_status ln_mlp_bwd(const lnfp8_ln_mlp_bwd_args* a, lnfp8_stream stream) {

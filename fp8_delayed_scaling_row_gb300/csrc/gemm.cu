@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "state_update.cuh"
 
 namespace lnfp8 {
 
@@ -113,6 +114,9 @@ struct KParams {
   float* ws;
   unsigned* flags;
   int group_m;  // M pairs per raster group (see tile_mn)
+  // A state update carried by the launch (upd.n > 0): the grid's first cluster runs it
+  // (its leader CTA, every slot) while the others compute the GEMM.
+  UpdateJob upd;
 };
 
 // Output tile t of a [num_m2 x num_n] grid of CTA-pair tiles in grouped raster
@@ -391,6 +395,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   auto csum_bar = [&](int a, int h) { return bar0 + 8u * (2 * STAGES + 5 + 2 * a + h); };
   auto hload_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 9 + w); };
 
+  // the first cluster of a launch that carries a state update runs it and leaves: its leader
+  // updates every slot (all amaxes it reads were final when the launch started; the GEMM
+  // itself reads none of the state it writes)
+  const bool has_upd = p.upd.n > 0;
+  if (has_upd && (int)blockIdx.x < CL) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0) {
+      __shared__ uint32_t ured[kThreads / 32];
+      run_update_all<kThreads>(p.upd, reinterpret_cast<float*>(smem), ured);
+    }
+    return;
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -439,7 +457,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
   // Work units: one N tile and CL consecutive M tiles, one per CTA of a cluster.
   const int rank = CL == 2 ? (int)cluster_rank() : 0;
-  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  const int cid = blockIdx.x / CL - (has_upd ? 1 : 0), ncl = gridDim.x / CL - (has_upd ? 1 : 0);
   const int num_m2 = (p.num_m + CL - 1) / CL;
   const int S = p.splits;
   const int num_units = num_m2 * p.num_n * S;
@@ -984,7 +1002,9 @@ lnfp8_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMap
   const int clusters = units < max_clusters ? units : max_clusters;
   // a split-K reducer waits for the tile's later pieces, which must not queue behind it
   if (kp.splits > clusters) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: %d K splits on %d clusters", kp.splits, clusters);
-  cfg.gridDim = dim3(clusters * CL);
+  if (kp.upd.n > 0 && kp.splits > 1) return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: a state update with split K");
+  // one more cluster, the first, when the launch carries a state update
+  cfg.gridDim = dim3((clusters + (kp.upd.n > 0 ? 1 : 0)) * CL);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   static const char* kind = EPI == EPI_GELU ? "gemm_gelu" : EPI == EPI_DGELU ? "gemm_dgelu" :
                             (A_MN ? (B_MN ? "gemm_mn_mn" : "gemm_mn_k") : (B_MN ? "gemm_k_mn" : "gemm_k_k"));
@@ -1167,6 +1187,9 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.splits = pl.splits;
   kp.kb_per_split = pl.kb_per_split;
   kp.flags = pl.splits > 1 ? reinterpret_cast<unsigned*>(g.ws) : nullptr;
+  kp.upd = g.upd;
+  if (kp.upd.n > 0 && (pl.splits > 1 || (size_t)kp.upd.L * sizeof(float) > (size_t)Cfg<128, false>::EPI_OUT_OFF))
+    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: a carried state update needs an unsplit GEMM and L <= the ring");
   kp.ws = pl.splits > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g.ws) + flag_off) : nullptr;
 
   if (g.epi == EPI_STORE) {

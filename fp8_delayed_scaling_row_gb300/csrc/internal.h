@@ -65,11 +65,20 @@ struct WeightCastJob {
 void weight_cast_add(WeightCastJob& j, int k, const uint16_t* in, int64_t rows, int64_t cols, const float* scale,
                      float* amax, uint8_t* out);
 
+// The scale_inv a forward casts with, saved by its first kernel for the rest of
+// the call and the backward: dst[k] = *src[k] for k < n (n <= 4; a slot whose
+// weight is stored in FP8 takes that weight's own scale_inv).
+struct SinvSnapshot {
+  float* dst;
+  const float* src[4];
+  int n;
+};
+
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st,
                            const uint16_t* resid = nullptr, uint16_t* hsum = nullptr,
-                           const WeightCastJob* wc = nullptr);
+                           const WeightCastJob* wc = nullptr, const SinvSnapshot* snap = nullptr);
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,
                            const float* rsigma, int64_t M, int64_t D, uint16_t* dx, float* dgamma,
                            float* dbeta, cudaStream_t st, bool clear = true,
@@ -109,6 +118,9 @@ struct GemmArgs {
   void* ws = nullptr;
   int64_t ws_bytes = 0;
   int64_t ws_flag_bytes = 0;
+  // optional: a state update the launch carries in an extra cluster (upd.n = 0: none); the
+  // GEMM itself must read none of the state it writes
+  UpdateJob upd = {};
 };
 
 struct GemmPlan {

@@ -158,7 +158,8 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
               const uint16_t* __restrict__ beta, float eps, int64_t M, int D,
               const float* __restrict__ scale_p, float* amax_cur, uint8_t* __restrict__ out,
               float* __restrict__ mu_out, float* __restrict__ rs_out, float* __restrict__ ydbg,
-              const uint16_t* __restrict__ resid, uint16_t* __restrict__ hsum, const WeightCastJob wc) {
+              const uint16_t* __restrict__ resid, uint16_t* __restrict__ hsum, const WeightCastJob wc,
+              const SinvSnapshot snap) {
   constexpr int NVR = RES ? 2 * NV : NV;  // 16-byte chunks per row and thread in the ring
   constexpr int RING = fwd_ring(NVR);
   constexpr int P = RING - 2;  // rows in flight ahead of the one being normalised
@@ -174,6 +175,10 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   uint4* ring = sgb + 2 * nvec;  // [RING][NVR][kThreads]: x chunks, then (RES) residual chunks
   pdl_wait();
   pdl_launch_dependents();
+  if (blockIdx.x == 0 && (int)threadIdx.x < snap.n) {  // the call's scale_inv snapshot (selects, not a runtime index)
+    const int k = threadIdx.x;
+    snap.dst[k] = *(k == 0 ? snap.src[0] : k == 1 ? snap.src[1] : k == 2 ? snap.src[2] : snap.src[3]);
+  }
   for (int i = threadIdx.x; i < nvec; i += kThreads) {
     sgb[i] = reinterpret_cast<const uint4*>(gamma)[i];
     sgb[nvec + i] = reinterpret_cast<const uint4*>(beta)[i];
@@ -462,7 +467,8 @@ template <int DT, bool RES>
 lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
                              const uint16_t* gamma, const uint16_t* beta, float eps, int64_t M, int D,
                              const float* scale, float* amax_cur, uint8_t* out, float* mu, float* rsigma,
-                             float* ydbg, const uint16_t* resid, uint16_t* hsum, const WeightCastJob& wc) {
+                             float* ydbg, const uint16_t* resid, uint16_t* hsum, const WeightCastJob& wc,
+                             const SinvSnapshot& snap) {
   const int nvr = RES ? 2 * rsh.nv : rsh.nv;
   const size_t smem = (size_t)D * 2 * sizeof(uint16_t) + (size_t)fwd_ring(nvr) * nvr * kThreads * 16;
   const int64_t gpb = kThreads / rsh.tpr;
@@ -472,7 +478,7 @@ lnfp8_status ln_fwd_dispatch(RowShape rsh, cudaStream_t st, const uint16_t* x,
     if (smem + 1024 > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     /* the weight tiles are shared by at least as many CTAs as the rows need, up to a full wave */     \
     const int64_t blocks = min64(max64((M + gpb - 1) / gpb, wc.tiles[0] + wc.tiles[1]), resident_blocks(k, smem)); \
-    if (launch_pdl(k, dim3((unsigned)max64(blocks, 1)), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg, resid, hsum, wc) != cudaSuccess) \
+    if (launch_pdl(k, dim3((unsigned)max64(blocks, 1)), dim3(kThreads), smem, st, x, gamma, beta, eps, M, D, scale, amax_cur, out, mu, rsigma, ydbg, resid, hsum, wc, snap) != cudaSuccess) \
       return check_launch("ln_fwd_cast launch");                                                        \
   } while (0)
   switch (rsh.tpr * 10 + rsh.nv) {
@@ -511,23 +517,25 @@ void weight_cast_add(WeightCastJob& j, int k, const uint16_t* in, int64_t rows, 
 lnfp8_status ln_fwd_launch(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, float eps,
                            int64_t M, int64_t D, int dtype, const float* scale, float* amax_cur,
                            uint8_t* out, float* mu, float* rsigma, float* ydbg, cudaStream_t st,
-                           const uint16_t* resid, uint16_t* hsum, const WeightCastJob* wcp) {
+                           const uint16_t* resid, uint16_t* hsum, const WeightCastJob* wcp, const SinvSnapshot* snp) {
   const WeightCastJob nojob = {};
   const WeightCastJob& wc = wcp ? *wcp : nojob;
-  if (M == 0 && wc.tiles[0] + wc.tiles[1] == 0 && !(wc.zero && wc.zero_n > 0)) return LNFP8_OK;
+  const SinvSnapshot nosnap = {};
+  const SinvSnapshot& snap = snp ? *snp : nosnap;
+  if (M == 0 && wc.tiles[0] + wc.tiles[1] == 0 && !(wc.zero && wc.zero_n > 0) && snap.n == 0) return LNFP8_OK;
   const RowShape rsh = row_shape(D, 4);
   if (rsh.tpr == 0 || D > 8192) return set_error(LNFP8_ERR_UNSUPPORTED_SHAPE, "ln_fwd_cast: D = %lld > 8192", (long long)D);
   LaunchScope ls("ln_fwd_cast", st);
   const bool res = resid != nullptr;
   if (dtype == LNFP8_E4M3)
     return res ? ln_fwd_dispatch<LNFP8_E4M3, true>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                   rsigma, ydbg, resid, hsum, wc)
+                                                   rsigma, ydbg, resid, hsum, wc, snap)
                : ln_fwd_dispatch<LNFP8_E4M3, false>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                    rsigma, ydbg, nullptr, nullptr, wc);
+                                                    rsigma, ydbg, nullptr, nullptr, wc, snap);
   return res ? ln_fwd_dispatch<LNFP8_E5M2, true>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                 rsigma, ydbg, resid, hsum, wc)
+                                                 rsigma, ydbg, resid, hsum, wc, snap)
              : ln_fwd_dispatch<LNFP8_E5M2, false>(rsh, st, x, gamma, beta, eps, M, (int)D, scale, amax_cur, out, mu,
-                                                  rsigma, ydbg, nullptr, nullptr, wc);
+                                                  rsigma, ydbg, nullptr, nullptr, wc, snap);
 }
 
 lnfp8_status ln_bwd_launch(const uint16_t* dy, const uint16_t* x, const uint16_t* gamma, const float* mu,

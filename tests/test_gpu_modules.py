@@ -301,11 +301,12 @@ def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profile
     direct = L.profile_collect()
     L.profile_enable(False)
     L.sync_status()
-    # forward: LayerNorm with the weight casts in the same launch, FC1, FC2, state; backward: clears, dY cast,
-    # the FC2 data and weight gradients in one launch, the FC1 data and weight gradients in one launch,
-    # LayerNorm with the state update in extra CTAs of the same launch
-    assert sum(n for _, n in direct.values()) == 9 and all(ms > 0 for ms, _ in direct.values())
-    assert direct["state_update"][1] == 1 and direct["ln_bwd"][1] == 1 and "cast_pair" not in direct
+    # forward: LayerNorm with the weight casts and the scale_inv snapshot in the same launch, FC1, FC2 with
+    # the state update in an extra cluster; backward: clears, dY cast, the FC2 data and weight gradients in
+    # one launch, the FC1 data and weight gradients in one launch, LayerNorm with the state update in extra
+    # CTAs of the same launch
+    assert sum(n for _, n in direct.values()) == 8 and all(ms > 0 for ms, _ in direct.values())
+    assert direct["ln_bwd"][1] == 1 and "state_update" not in direct and "cast_pair" not in direct
 
     fm1, bm1, ctx1, g1 = make()
     y1 = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
