@@ -1188,8 +1188,11 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   kp.kb_per_split = pl.kb_per_split;
   kp.flags = pl.splits > 1 ? reinterpret_cast<unsigned*>(g.ws) : nullptr;
   kp.upd = g.upd;
-  if (kp.upd.n > 0 && (pl.splits > 1 || (size_t)kp.upd.L * sizeof(float) > (size_t)Cfg<128, false>::EPI_OUT_OFF))
-    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: a carried state update needs an unsplit GEMM and L <= the ring");
+  // the update keeps its history window in the operand ring's shared memory (at least 140 KB in
+  // every configuration; a validated history holds at most 16384 floats)
+  static_assert(16384 * sizeof(float) <= (size_t)Cfg<192, true>::EPI_OUT_OFF, "history window in the ring");
+  if (kp.upd.n > 0 && (pl.splits > 1 || kp.upd.L > 16384 || kp.upd.n > 64))
+    return set_error(LNFP8_ERR_UNSUPPORTED, "fp8 gemm: a carried state update needs an unsplit GEMM and a validated state");
   kp.ws = pl.splits > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g.ws) + flag_off) : nullptr;
 
   if (g.epi == EPI_STORE) {
