@@ -175,15 +175,6 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   uint4* ring = sgb + 2 * nvec;  // [RING][NVR][kThreads]: x chunks, then (RES) residual chunks
   pdl_wait();
   pdl_launch_dependents();
-  if (blockIdx.x == 0 && (int)threadIdx.x < snap.n) {  // the call's scale_inv snapshot (selects, not a runtime index)
-    const int k = threadIdx.x;
-    snap.dst[k] = *(k == 0 ? snap.src[0] : k == 1 ? snap.src[1] : k == 2 ? snap.src[2] : snap.src[3]);
-  }
-  for (int i = threadIdx.x; i < nvec; i += kThreads) {
-    sgb[i] = reinterpret_cast<const uint4*>(gamma)[i];
-    sgb[nvec + i] = reinterpret_cast<const uint4*>(beta)[i];
-  }
-  __syncthreads();
   const float s = *scale_p;
   const float inv_d = 1.0f / (float)D;
   const int64_t stride = (int64_t)gridDim.x * GPB;
@@ -207,10 +198,20 @@ ln_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma
   int64_t row = (int64_t)blockIdx.x * GPB + g;
 #pragma unroll
   for (int k = 0; k < P; ++k) issue(row + k * stride, k);
-  // the call's weight casts, while the first rows' loads are in flight
+  // while the first rows' loads are in flight: the call's scale_inv snapshot (selects, not a
+  // runtime index), the counters it clears, gamma and beta into shared memory, the weight casts
+  if (blockIdx.x == 0 && (int)threadIdx.x < snap.n) {
+    const int k = threadIdx.x;
+    snap.dst[k] = *(k == 0 ? snap.src[0] : k == 1 ? snap.src[1] : k == 2 ? snap.src[2] : snap.src[3]);
+  }
   if (wc.zero && blockIdx.x == 0)
     for (int64_t i = threadIdx.x; i < wc.zero_n; i += kThreads) wc.zero[i] = 0u;
+  for (int i = threadIdx.x; i < nvec; i += kThreads) {
+    sgb[i] = reinterpret_cast<const uint4*>(gamma)[i];
+    sgb[nvec + i] = reinterpret_cast<const uint4*>(beta)[i];
+  }
   if (wc.tiles[0] + wc.tiles[1] > 0) weight_cast_tiles<DT>(wc);
+  __syncthreads();
   int slot = 0;
   // every thread of the block runs the same trip count (group_sum may use barriers)
   for (; row - g < M; row += stride) {
@@ -332,10 +333,6 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
   const int64_t bid = (int64_t)blockIdx.x - job.n;
   const int64_t stride = (int64_t)(gridDim.x - job.n) * GPB;
 
-  for (int c = threadIdx.x; c < 2 * D; c += kThreads) colred[c] = 0.f;
-  for (int i = threadIdx.x; i < nvec; i += kThreads) sg[i] = reinterpret_cast<const uint4*>(gamma)[i];
-  __syncthreads();
-
   auto issue = [&](int64_t r, int slot) {
     if (r < M) {
 #pragma unroll
@@ -362,6 +359,10 @@ ln_bwd_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
   int64_t row = bid * GPB + g;
 #pragma unroll
   for (int k = 0; k < P; ++k) issue(row + k * stride, k);
+  // while the first rows' loads are in flight: clear the column partials, gamma into shared memory
+  for (int c = threadIdx.x; c < 2 * D; c += kThreads) colred[c] = 0.f;
+  for (int i = threadIdx.x; i < nvec; i += kThreads) sg[i] = reinterpret_cast<const uint4*>(gamma)[i];
+  __syncthreads();
   int slot = 0;
   for (; row - g < M; row += stride) {
     issue(row + P * stride, slot + P < RING ? slot + P : slot + P - RING);
