@@ -49,15 +49,6 @@ __device__ __forceinline__ void cp_async_wait() {
 __host__ __device__ constexpr int fwd_ring(int nv) { return nv <= 2 ? 6 : 4; }
 __host__ __device__ constexpr int bwd_ring(int nv) { return nv <= 2 ? 5 : (nv == 3 ? 4 : 3); }
 
-__device__ __forceinline__ void unpack8(uint4 u, float* v) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-  }
-}
-
 // Packed fp32 pairs: two values in one 64-bit register, for the f32x2 add,
 // sub, mul and fma of the sm_100-family cores (one instruction per pair).
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
