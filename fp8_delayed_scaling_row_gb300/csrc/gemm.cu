@@ -1249,13 +1249,18 @@ lnfp8_status gemm_pair_launch(const GemmArgs& g0, const GemmArgs& g1, cudaStream
   const bool a1_mn = g1.a_layout == 1, b1_mn = g1.b_layout == 1;
   GemmPlan pl = pair_plan(g1);
   const int64_t flag_off = g1.ws_flag_bytes > 0 ? g1.ws_flag_bytes : pl.flag_bytes;
-  // The dGELU pair's weight gradient runs under its primary epilogue. Two K pieces per tile
-  // spread it over more clusters while its tiles are fewer than the clusters; with at least as
-  // many tiles as clusters the exchange of partial products only costs. Measured on the d 2048
-  // backward: whole tiles 3-12% faster at 2048 to 16384 tokens, even at 32768 and 65536; at
-  // d 768 (36 tiles on 76 clusters) the launch runs 5% faster in two pieces.
+  // Two K pieces per weight-gradient tile spread the weight gradient over more clusters while
+  // its tiles are fewer than the clusters. With at least as many tiles as clusters the dGELU
+  // pair (its weight gradient's MMAs hidden under the primary epilogue) runs whole tiles: the
+  // exchange of partial products only costs. The MMA-bound bf16-store pair runs whole tiles
+  // only up to 64 K blocks: the exchange costs the same per tile at any K, while whole tiles
+  // leave the clusters' MMA work less even as K grows. Measured on the d 2048 backward: whole
+  // dGELU tiles 3-12% faster per step at 2048 to 16384 tokens, even at 32768 and 65536; whole
+  // FC1 tiles 8% / 4% faster per step at 2048 / 8192 tokens, about 1% slower at 16384; at d 768
+  // (36 tiles on 76 clusters) the dGELU launch runs 5% faster in two pieces.
   const int64_t sec_tiles = (((g1.M + BM - 1) / BM + CL - 1) / CL) * ((g1.N + 255) / 256);
-  const bool whole_sec = g0.epi == EPI_DGELU && sec_tiles >= num_sms() / CL;
+  const int64_t sec_kb = (g1.K + BK - 1) / BK;
+  const bool whole_sec = sec_tiles >= num_sms() / CL && (g0.epi == EPI_DGELU || sec_kb <= 64);
   if (pl.splits > 1 &&
       (whole_sec || !g1.ws || flag_off < pl.flag_bytes || flag_off % 256 || g1.ws_bytes < flag_off + pl.slot_bytes)) {
     pl.splits = 1;
