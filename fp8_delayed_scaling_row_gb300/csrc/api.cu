@@ -665,12 +665,23 @@ lnfp8_status ln_linear_fwd(const lnfp8_ln_linear_fwd_args* a, lnfp8_stream strea
       TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
     else if (!w8)
       weight_cast_add(wc, 0, a->w, a->N, a->K, m.scale + 1, m.amax_cur + 1, a->wq);
+    // the LayerNorm launch also saves the scale_inv this forward casts with (for the GEMM and the backward)
+    const SinvSnapshot snap = {a->sinv_saved, {m.scale_inv + 0, w8 ? a->w_scale_inv : m.scale_inv + 1}, 2};
     TRY(ln_fwd_launch(a->x, a->gamma, a->beta, a->eps, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, a->mu,
-                      a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc));
-  } else {
-    if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
-    TRY(cast_launch(a->x, false, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, nullptr, nullptr, st));
+                      a->rsigma, a->ln_out_debug, st, a->residual, a->x_sum, &wc, &snap));
+    // the GEMM dequantises with the saved scale_inv, so it can carry the state update: both
+    // amaxes are final when it starts
+    GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, a->sinv_saved + 0, a->sinv_saved + 1);
+    g.bias = a->bias;
+    g.out = a->y;
+    if (a->M > 0 && !a->defer_update) g.upd = update_job(&m, mask_all(m.n, fdt), a->recipe.margin);
+    TRY(gemm_launch(g, st));
+    if (g.upd.n > 0) return LNFP8_OK;
+    // the snapshot is taken: only the update remains (none when deferred)
+    return finish_state(&m, &a->recipe, fdt, nullptr, a->defer_update, st);
   }
+  if (!w8) TRY(cast_launch(a->w, false, a->N, a->K, fdt, m.scale + 1, m.amax_cur + 1, a->wq, nullptr, nullptr, st));
+  TRY(cast_launch(a->x, false, a->M, a->K, fdt, m.scale + 0, m.amax_cur + 0, a->xq, nullptr, nullptr, st));
   GemmArgs g = gemm_args(a->xq, 0, fdt, a->wq, 0, fdt, a->M, a->N, a->K, m.scale_inv + 0,
                          w8 ? a->w_scale_inv : m.scale_inv + 1);
   g.bias = a->bias;

@@ -291,8 +291,12 @@ typedef struct {
    *                        A-operand producer; then the state update. Needs
    *                        M >= 1, K <= 768 and no residual, else
    *                        LNFP8_ERR_UNSUPPORTED_SHAPE.
-   *   LNFP8_PATH_SEPARATE  the weight cast, the LayerNorm + cast, the GEMM and
-   *                        the state update as launches of their own. */
+   *   LNFP8_PATH_SEPARATE  the LayerNorm + cast (which also casts a small
+   *                        weight; a large one gets a launch of its own), then
+   *                        the GEMM, whose launch also runs the state update.
+   *                        Without the LayerNorm: the input cast, the weight
+   *                        cast, the GEMM and the state update as launches of
+   *                        their own. */
   int path;
 } lnfp8_ln_linear_fwd_args;
 
