@@ -1,7 +1,8 @@
 #!/usr/bin/env python
 """FP8 delayed-scaling LayerNormMLP forward+backward throughput on GB300.
 
-One step = ln_mlp_fwd + ln_mlp_bwd through the C ABI over one fresh batch:
+One step = ln_mlp_fwd + ln_mlp_bwd through the C ABI over one batch (up to 8
+batches drawn once and cycled over the steps):
 8192 tokens (32 x 256) of d_model 768, FFN 3072, HYBRID (E4M3 forward, E5M2
 gradients), amax_history_len 16, X ~ N(0,1) with 0.1% x50 outliers, dY ~
 N(0, 0.01), weights ~ N(0, 0.02), bias 0. FLOPs are the six FP8 GEMMs,
