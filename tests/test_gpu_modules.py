@@ -277,6 +277,44 @@ def test_linear_without_ln(L):
     run_linear(L, M=250, K=256, N=128, steps=2, ln=False)
 
 
+@pytest.mark.parametrize("M,ln", [(256, True), (333, True), (0, True), (250, False)])
+def test_linear_forward_state_update_in_the_gemm_launch(L, M, ln):
+    """With the LayerNorm, the separate-launch forward is two launches: the LayerNorm (with
+    the weight cast and the scale_inv snapshot) and the GEMM, whose extra cluster runs the
+    state update. Over three steps its outputs and state equal, bit for bit, a deferred
+    forward followed by the standalone update; the saved scale_inv is the state's before
+    the call. Without the LayerNorm: input cast, weight cast, GEMM, state update."""
+    K, N = 768, 2304
+    rec = L.Recipe("hybrid", 16)
+    p = synth.linear_params(N, K, ln=ln, layer=2, bias_std=0.02)
+    dev = {k: bf16_dev(v) for k, v in p.items() if v is not None}
+    g, b = (dev["gamma"], dev["beta"]) if ln else (None, None)
+    runs = []
+    for carried in (True, False):
+        meta, ys = L.ScalingMeta(2, 16), []
+        for step in range(3):
+            x = bf16_dev(synth.activations(M, K, dist="outliers", seed=11, step=step)) if M else \
+                torch.empty(0, K, dtype=torch.bfloat16, device="cuda")
+            pre = meta.scale_inv.clone()
+            n0 = L.launch_count()
+            y, ctx = L.ln_linear_fwd(x, g, b, dev["w"], dev["b"], meta, rec, path=L.PATH_SEPARATE,
+                                     defer_update=not carried)
+            launches = L.launch_count() - n0
+            if carried and M > 0:
+                assert launches == (2 if ln else 4), launches
+            if not carried:
+                L.amax_history_update(meta, rec, [L.E4M3, L.E4M3])
+            L.sync_status()
+            assert torch.equal(ctx.sinv_saved, pre), step
+            ys.append(y.clone())
+        runs.append((ys, meta))
+    (ya, ma), (yb, mb) = runs
+    for step in range(3):
+        assert torch.equal(ya[step], yb[step]), step
+    for name in ("scale", "scale_inv", "amax_history", "amax_cur"):
+        assert torch.equal(getattr(ma, name), getattr(mb, name)), name
+
+
 def test_mlp_step_replayed_from_a_cuda_graph_matches_direct_calls_and_is_profiled(L):
     """The step captured into a CUDA graph (as the benchmark replays it) gives the
     direct call's results; per-kernel timing works for direct calls and for
