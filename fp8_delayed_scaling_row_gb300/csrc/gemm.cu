@@ -1220,8 +1220,10 @@ lnfp8_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
                    g.a_layout, g.b_layout);
 }
 
-// The split exchange area a paired launch needs for its secondary GEMM
-// (flag words and partial-product slots), zero when it would not split.
+// The split exchange area a paired launch may need for its secondary GEMM
+// (flag words and partial-product slots), zero when it cannot split. The launch
+// still runs whole tiles where that measured faster (gemm_pair_launch), so this
+// is what the workspace must hold, not what every launch uses.
 GemmPlan pair_plan(const GemmArgs& sec) {
   GemmPlan pl;
   pl.bn = 256;
