@@ -516,7 +516,8 @@ class MlpCtx:
 def mlp_ctx(M, D, F, *, device="cuda", debug=False, fused=False, weight_codes=True) -> MlpCtx:
     """Saved tensors of one LayerNormMLP forward. fused=True also allocates the row-block
     readiness counters with which the forward runs FC1 and FC2 as one launch (same
-    results; at 8192 x 768 -> 3072 -> 768 the two launches are still faster).
+    results; the two launches measured faster at 8192 x 768 -> 3072 -> 768 and at
+    d 2048 from 8192 to 65536 tokens, equal at 2048).
     weight_codes=False leaves w1q/w2q to FP8-stored weights."""
     u8, f32 = torch.uint8, torch.float32
     _, (lnq, w1q, w2q, h, aq, mu, rs, sinv) = _carve(
